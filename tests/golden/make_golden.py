@@ -1,0 +1,46 @@
+"""Writes oracle_tiny_seed0.json: the CPU oracle's token stream and chain
+hashes for the tiny model (seed 0, 16-token seeded prompt, 16 greedy steps).
+
+It calls only the oracle and the seeded input generator; no value in the
+fixture comes from the CUDA path. Run: python tests/golden/make_golden.py
+"""
+import json
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+sys.path.insert(0, ROOT)
+import oracle  # noqa: E402
+import synth   # noqa: E402
+
+
+def main():
+    seed, prompt_len, steps = 0, 16, 16
+    path = synth.ensure_artifact("tiny", seed)
+    m = oracle.Model(path)
+    ids = synth.prompt_ids(seed, 0, prompt_len, m.vocab)
+    s = m.new_seq(64)
+    am, lg = s.feed(ids)
+    rows, toks = [lg], [am]
+    for _ in range(steps - 1):
+        am, lg = s.feed([toks[-1]])
+        rows.append(lg)
+        toks.append(am)
+    out = {
+        "what": "CPU oracle, tiny model, seed 0, prompt index 0, greedy",
+        "seed": seed, "prompt_len": prompt_len, "steps": steps,
+        "artifact_sha256": open(path + ".sha256").read().strip(),
+        "tokens": toks,
+        "logits_hash12": oracle.chain_hash(rows).hex()[:12],
+        "tokens_hash12": oracle.chain_hash([np.array([t], np.int32) for t in toks]).hex()[:12],
+    }
+    with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "oracle_tiny_seed0.json"), "w") as f:
+        json.dump(out, f, indent=1)
+        f.write("\n")
+    print(out)
+
+
+if __name__ == "__main__":
+    main()
