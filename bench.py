@@ -1,0 +1,301 @@
+"""Decode throughput of the integer-only decoder on GB300.
+
+Workload (one "step" = one greedy decode step through every row of the hot
+path: embedding, 28 layers of NormQuant / QKV GEMM + QK-norm/RoPE/KV write /
+attention / o_proj / NormQuant / gate-up + SwiGLU / down, final norm, lm_head,
+tie-low argmax): the Qwen3-0.6B-shaped integer model, batch 1, 64-token seeded
+prompt, greedy decode (the pages' demo workload, with seeded synthetic weights
+and prompt ids). Weights (596 MB) exceed the 129 MB L2, so every step streams
+them from HBM; no L2 flush is needed.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl detint|reference]
+Prints one JSON line (rank 0). --impl reference times the CPU oracle (the
+reference arm of this method: the plain integer C program) on the same
+workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s at B=1/8 (Qwen3-0.6B shape), bit-exact; int8 GEMM TOPS, HBM GB/s"
+SHAPE = "qwen3-0.6b"
+PROMPT_LEN = 64
+SEED = 0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p:
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    """The CPU oracle on the same workload: one greedy decode step per unit."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    path = synth.ensure_artifact(SHAPE, SEED)
+    m = oracle.Model(path)
+    prompt = synth.prompt_ids(SEED, 0, PROMPT_LEN, m.vocab)
+    s = m.new_seq(PROMPT_LEN + args.warmup + args.steps + 2)
+    tok, _ = s.feed(prompt)
+    for _ in range(args.warmup):
+        tok, _ = s.feed([tok])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tok, _ = s.feed([tok])
+    dt = time.perf_counter() - t0
+    v = args.steps / dt
+    cores = oracle.max_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8/int32",
+            "data": "synthetic",
+            "config": {"workload": "qwen3-0.6b-shape integer decode, B=1, 64-token seeded prompt",
+                       "global_batch": 1, "seq_len": PROMPT_LEN, "parallelism": "replicas"},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} decode steps after a {PROMPT_LEN}-token "
+                                       f"prefill and {args.warmup} warm-up steps"},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(seconds: float = 12.0):
+    """Bounded sample of the oracle on the bench workload (B=1 decode)."""
+    import oracle
+    import synth
+    path = synth.ensure_artifact(SHAPE, SEED)
+    m = oracle.Model(path)
+    prompt = synth.prompt_ids(SEED, 0, PROMPT_LEN, m.vocab)
+    s = m.new_seq(PROMPT_LEN + 4096)
+    tok, _ = s.feed(prompt)
+    n = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        tok, _ = s.feed([tok])
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} B=1 decode steps after the {PROMPT_LEN}-token prefill "
+                      f"(~{seconds:.0f} s of CPU work)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="detint", choices=["detint", "reference"])
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import synth
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    B = args.batch
+    K, W = args.steps, args.warmup
+    path = synth.ensure_artifact(SHAPE, SEED)
+    max_ctx = PROMPT_LEN + W + 2 * K + 16
+    model = pkg.Model(path, max_batch=B, max_ctx=((max_ctx + 63) // 64) * 64)
+    V, H = model.vocab, model.hidden
+    dev = torch.device("cuda", local)
+    prompts = [synth.prompt_ids(SEED, 0, PROMPT_LEN, V)]
+    prompts += [synth.prompt_ids(SEED, 100 + i, int(n), V)
+                for i, n in enumerate(synth.coprompt_lengths(SEED, B - 1))]
+    s = model.stream
+    seq_ids = list(range(B))
+
+    def start():
+        cu = np.zeros(B + 1, np.int64)
+        cu[1:] = np.cumsum([len(p) for p in prompts])
+        flat = torch.tensor(np.concatenate(prompts), dtype=torch.int32, device=dev)
+        tok = torch.empty(B, dtype=torch.int32, device=dev)
+        with torch.cuda.stream(s):
+            model.prefill(seq_ids, flat, cu, None, tok)
+            for _ in range(W):
+                model.decode_step(seq_ids, tok, None, tok)
+        s.synchronize()
+        return tok
+
+    # ---- device-resident timed region: K decode steps, one graph each
+    tok = start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(K):
+                model.decode_step(seq_ids, tok, None, tok)
+            e1.record(s)
+        s.synchronize()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    value = B * K * ws / (ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    for sid in seq_ids:
+        model.reset_seq(sid)
+    tok = start()
+    host_in = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    host_out = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    host_in.copy_(tok.cpu())
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        for _ in range(K):
+            tok.copy_(host_in, non_blocking=True)
+            model.decode_step(seq_ids, tok, None, nxt)
+            host_out.copy_(nxt, non_blocking=True)
+            s.synchronize()
+            host_in.copy_(host_out)
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": B * K * ws / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
+           "d2h_bytes_per_step": 4 * B}
+
+    # ---- dominant kernel: the weight-streaming GEMV at the lm_head shape
+    peak, peak_kind = _peaks()
+    wmat = torch.randint(-127, 128, (V, H), dtype=torch.int8, device=dev)
+    xmat = torch.randint(-127, 128, (B, H), dtype=torch.int8, device=dev)
+    cmat = torch.empty((B, V), dtype=torch.int32, device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            pkg.detint_gemm_i8(xmat, wmat, cmat, stream=s)
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        nrep = 50
+        r0.record(s)
+        for _ in range(nrep):
+            pkg.detint_gemm_i8(xmat, wmat, cmat, stream=s)
+        r1.record(s)
+    s.synchronize()
+    kms = r0.elapsed_time(r1) / nrep
+    kbytes = V * H + B * H + 4 * B * V
+    achieved = kbytes / (kms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "k_gemv<1,EPI_RAW> (lm_head shape 151936x1024, B=%d)" % B,
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": kbytes,
+                "us_per_launch": kms * 1e3}
+    # whole-step roofline: algorithmic bytes of one decode step
+    L, nq, nkv, d, F = model.n_layers, model.n_q, model.n_kv, model.head_dim, model.ffn
+    wbytes = L * ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F) + V * H
+    ctx_mean = PROMPT_LEN + W + K / 2
+    kv = L * nkv * d * 2 * ctx_mean * B
+    step_bytes = wbytes + kv + 4 * B * V
+    step = {"bytes": step_bytes, "achieved_gbs": step_bytes / (ms / K / 1e3) / 1e9,
+            "frac": step_bytes / (ms / K / 1e3) / 1e9 / peak}
+
+    if rank == 0:
+        cb = None
+        if not args.no_cpu_baseline and ws == 1:
+            cb = cpu_baseline()
+        gpu_launches = K * (1 + L * 10 + 3)
+        line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": K,
+                "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "int8/int32", "data": "synthetic",
+                "config": {"workload": f"qwen3-0.6b-shape integer decode, B={B}, "
+                                       f"{PROMPT_LEN}-token seeded prompt, CUDA-graph step",
+                           "global_batch": B * ws, "seq_len": PROMPT_LEN, "parallelism": "replicas",
+                           "l2": "weights 596 MB > 129 MB L2 every step (no flush needed)"},
+                "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline,
+                "step_roofline": step, "clocks": clk.summary(), "cpu_baseline": cb}
+        print(json.dumps(line), flush=True)
+    model.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

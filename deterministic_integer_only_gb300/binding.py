@@ -1,0 +1,205 @@
+"""ctypes binding of libdetint (include/detint.h), with the same names.
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels behind the C ABI. PyTorch supplies device memory and streams. If the
+library is missing or cannot be loaded, every entry point raises; there is no
+CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import hashlib
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdetint.so")
+_lib = None
+
+ERRORS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "token id outside the vocabulary",
+          4: "context capacity exceeded", 5: "unreadable or malformed artifact",
+          6: "artifact sha256 mismatch", 7: "CUDA error", 8: "device out of memory",
+          9: "bad sequence id", 10: "saturation recorded"}
+
+# every entry point of include/detint.h
+SYMBOLS = ["detint_load", "detint_prefill", "detint_decode_step", "detint_gemm_i8",
+           "detint_reset_seq", "detint_seq_len", "detint_status", "detint_set_graph",
+           "detint_model_info", "detint_free", "detint_strerror", "detint_last_error"]
+
+
+class DetintError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str = ""):
+        self.code = code
+        super().__init__(f"{where}: {ERRORS.get(code, code)} ({detail})" if detail else
+                         f"{where}: {ERRORS.get(code, code)}")
+
+
+def lib():
+    """The loaded libdetint; raises if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "deterministic_integer_only_gb300.build.build()")
+        L = C.CDLL(LIB_PATH)
+        vp, i32p = C.c_void_p, C.POINTER(C.c_int32)
+        L.detint_load.argtypes = [C.c_char_p, C.c_int, C.c_int, vp, C.POINTER(vp)]
+        L.detint_prefill.argtypes = [vp, C.c_int, i32p, i32p, vp, vp, vp, vp]
+        L.detint_decode_step.argtypes = [vp, C.c_int, i32p, vp, vp, vp, vp]
+        L.detint_gemm_i8.argtypes = [vp, vp, vp, C.c_int, C.c_int, C.c_int, vp]
+        L.detint_reset_seq.argtypes = [vp, C.c_int]
+        L.detint_seq_len.argtypes = [vp, C.c_int, i32p]
+        L.detint_status.argtypes = [vp, i32p, vp]
+        L.detint_set_graph.argtypes = [vp, C.c_int]
+        L.detint_model_info.argtypes = [vp, i32p]
+        L.detint_free.argtypes = [vp]
+        L.detint_free.restype = None
+        L.detint_strerror.restype = C.c_char_p
+        L.detint_strerror.argtypes = [C.c_int]
+        L.detint_last_error.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise DetintError(rc, where, lib().detint_last_error().decode(errors="replace"))
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def detint_gemm_i8(A, B, C_out, stream=None):
+    """C_out[M,N] (int32, cuda) = A[M,K] (int8) @ B[N,K]^T (int8), exact."""
+    M, K = A.shape
+    N = B.shape[0]
+    _check(lib().detint_gemm_i8(_ptr(A), _ptr(B), _ptr(C_out), M, N, K, _stream(stream)),
+           "detint_gemm_i8")
+    return C_out
+
+
+def chain_hash(rows, prev: bytes | None = None) -> bytes:
+    """SHA-256 chain over int32 rows (little-endian) from 32 zero bytes
+    (DetLLM README, "Demo": the per-step logits chain hash)."""
+    h = prev if prev is not None else b"\0" * 32
+    for r in rows:
+        h = hashlib.sha256(h + np.ascontiguousarray(r, dtype="<i4").tobytes()).digest()
+    return h
+
+
+class Model:
+    """A loaded integer model on the current CUDA device (detint_load)."""
+
+    def __init__(self, path: str, max_batch: int, max_ctx: int, stream=None):
+        import torch
+        self.torch = torch
+        self.stream = stream if stream is not None else torch.cuda.Stream()
+        h = C.c_void_p()
+        _check(lib().detint_load(path.encode(), int(max_batch), int(max_ctx),
+                                 self.stream.cuda_stream, C.byref(h)), "detint_load")
+        self._h = h
+        info = np.zeros(16, np.int32)
+        _check(lib().detint_model_info(self._h, info.ctypes.data_as(C.POINTER(C.c_int32))),
+               "detint_model_info")
+        (self.n_layers, self.hidden, self.n_q, self.n_kv, self.head_dim, self.ffn, self.vocab,
+         self.max_pos, self.qk_norm, self.max_batch, self.max_ctx) = [int(v) for v in info[:11]]
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().detint_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_graph(self, enable: bool):
+        _check(lib().detint_set_graph(self._h, int(bool(enable))), "detint_set_graph")
+
+    def reset_seq(self, seq_id: int):
+        _check(lib().detint_reset_seq(self._h, int(seq_id)), "detint_reset_seq")
+
+    def seq_len(self, seq_id: int) -> int:
+        v = C.c_int32()
+        _check(lib().detint_seq_len(self._h, int(seq_id), C.byref(v)), "detint_seq_len")
+        return int(v.value)
+
+    def status(self) -> np.ndarray:
+        flags = np.zeros(8, np.int32)
+        lib().detint_status(self._h, flags.ctypes.data_as(C.POINTER(C.c_int32)),
+                            self.stream.cuda_stream)
+        return flags
+
+    def prefill(self, seq_ids, tokens, cu_lens, logits=None, next_tok=None):
+        """tokens: int32 cuda tensor (ragged, concatenated); cu_lens: host ints."""
+        torch = self.torch
+        seq = _i32(seq_ids)
+        cu = _i32(cu_lens)
+        n = seq.size
+        if next_tok is None:
+            next_tok = torch.empty(n, dtype=torch.int32, device=tokens.device)
+        _check(lib().detint_prefill(self._h, n, seq.ctypes.data_as(C.POINTER(C.c_int32)),
+                                    cu.ctypes.data_as(C.POINTER(C.c_int32)), _ptr(tokens),
+                                    _ptr(logits), _ptr(next_tok), self.stream.cuda_stream),
+               "detint_prefill")
+        return next_tok
+
+    def decode_step(self, seq_ids, tok, logits=None, next_tok=None):
+        torch = self.torch
+        seq = _i32(seq_ids)
+        if next_tok is None:
+            next_tok = torch.empty(seq.size, dtype=torch.int32, device=tok.device)
+        _check(lib().detint_decode_step(self._h, seq.size, seq.ctypes.data_as(C.POINTER(C.c_int32)),
+                                        _ptr(tok), _ptr(logits), _ptr(next_tok),
+                                        self.stream.cuda_stream), "detint_decode_step")
+        return next_tok
+
+    def generate(self, prompts, max_new: int, seq_ids=None, keep_logits: bool = True):
+        """Greedy decode of a ragged batch of prompts (lists of ids).
+
+        Returns (tokens [B][max_new] int32 numpy, logits rows per step (list of
+        [B, V] numpy arrays) or chain-hash digests per row when keep_logits is
+        "hash"). Step 0 is the prefill's last-position logits (README, "Usage":
+        generate(ids, max_new)).
+        """
+        torch = self.torch
+        B = len(prompts)
+        seq_ids = list(range(B)) if seq_ids is None else list(seq_ids)
+        dev = torch.device("cuda")
+        cu = np.zeros(B + 1, np.int64)
+        cu[1:] = np.cumsum([len(p) for p in prompts])
+        flat = torch.tensor(np.concatenate([np.asarray(p, np.int32) for p in prompts]),
+                            dtype=torch.int32, device=dev)
+        logits = torch.empty((B, self.vocab), dtype=torch.int32, device=dev)
+        tok = torch.empty(B, dtype=torch.int32, device=dev)
+        toks = np.zeros((B, max_new), np.int32)
+        rows = []
+        hashes = [b"\0" * 32] * B
+        with torch.cuda.stream(self.stream):
+            self.prefill(seq_ids, flat, cu, logits, tok)
+            for step in range(max_new):
+                if step:
+                    self.decode_step(seq_ids, tok, logits, tok)
+                lg = logits.cpu().numpy()
+                toks[:, step] = tok.cpu().numpy()
+                if keep_logits == "hash":
+                    hashes = [chain_hash([lg[b]], hashes[b]) for b in range(B)]
+                elif keep_logits:
+                    rows.append(lg)
+        self.stream.synchronize()
+        return toks, (hashes if keep_logits == "hash" else rows)

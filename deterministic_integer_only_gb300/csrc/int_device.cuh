@@ -1,0 +1,120 @@
+// Integer primitives for the detint kernels (device side).
+//
+// Every rule here is the frozen arithmetic of the integer-only forward pass:
+// round-to-nearest shifts with ties toward +infinity, floor divisions of
+// non-negative integers, floor square roots and 15-bit dyadic scales
+// (DetLLM blog, section "DetLLM": every tensor carries a scale m/2^k, and
+// rescaling is one integer multiply and one shift with a fixed rounding rule;
+// DetLLM README, "Layout": intmath freezes the rounding rules).
+//
+// No floating-point type, literal or intrinsic appears in this file or in any
+// kernel file, and there is no division or remainder by a value known only at
+// run time: CUDA may lower those through a floating-point reciprocal, so
+// divisions go through udiv64 below (restoring long division).
+#pragma once
+#include <stdint.h>
+
+namespace detint {
+
+typedef long long i64;
+typedef unsigned long long u64;
+
+// number of binary digits (bitlen(0) = 0)
+__device__ __forceinline__ int bitlen_u64(u64 x) { return 64 - __clzll((long long)x); }
+
+// x / 2^s rounded to nearest, ties toward +infinity; s in [0, 62]
+__device__ __forceinline__ i64 rshr(i64 x, int s) {
+    return s <= 0 ? x : ((x + (1LL << (s - 1))) >> s);
+}
+__device__ __forceinline__ int rshr32(int x, int s) {
+    return s <= 0 ? x : ((x + (1 << (s - 1))) >> s);
+}
+__device__ __forceinline__ i64 sat_b(i64 x, i64 b) { return x > b ? b : (x < -b ? -b : x); }
+__device__ __forceinline__ int sat32(i64 x) { return (int)sat_b(x, 2147483647LL); }
+__device__ __forceinline__ int sat127(i64 x) { return (int)sat_b(x, 127); }
+
+// floor(n / d) for d >= 1, by restoring long division over the quotient bits
+__device__ __noinline__ u64 udiv64(u64 n, u64 d) {
+    if (n < d) return 0;
+    int sh = bitlen_u64(n) - bitlen_u64(d);
+    u64 dd = d << sh;
+    u64 q = 0;
+    for (int i = sh; i >= 0; --i) {
+        q <<= 1;
+        if (n >= dd) { n -= dd; q |= 1ull; }
+        dd >>= 1;
+    }
+    return q;
+}
+
+// floor(sqrt(n)), digit by digit
+__device__ __noinline__ u64 isqrt_u64(u64 n) {
+    u64 r = 0, bit = 1ull << 62;
+    while (bit > n) bit >>= 2;
+    while (bit) {
+        if (n >= r + bit) { n -= r + bit; r = (r >> 1) + bit; }
+        else r >>= 1;
+        bit >>= 2;
+    }
+    return r;
+}
+
+// (m, k): m = round(N 2^k / D) (ties up) with 2^14 <= N 2^k / D < 2^15
+__device__ __noinline__ void dyadic_dev(u64 N, u64 D, int* m_out, int* k_out) {
+    int k = 14 + bitlen_u64(D) - bitlen_u64(N);
+    for (int it = 0; it < 4; ++it) {   // the estimate is within one of k
+        u64 lhs, lo;
+        if (k >= 0) { lhs = N << k; lo = D << 14; }
+        else { lhs = N; lo = D << (14 - k); }
+        if (lhs < lo) { ++k; continue; }
+        if (lhs >= (lo << 1)) { --k; continue; }
+        break;
+    }
+    u64 num, den;
+    if (k >= 0) { num = (N << (k + 1)) + D; den = D << 1; }
+    else { num = (N << 1) + (D << (-k)); den = D << (1 - k); }
+    *m_out = (int)udiv64(num, den);
+    *k_out = k;
+}
+
+// 2^(delta/1024) in Q15 for delta <= 0: a cubic on the fraction of the
+// base-2 exponent (Horner form, one rounding shift per step) and a right
+// shift for its integer part (DetLLM README, "Layout": DI-Exp)
+__device__ __forceinline__ int exp2q_dev(i64 delta) {
+    i64 ip = delta >> 10;                 // floor
+    if (ip <= -24) return 0;
+    int f = (int)(delta & 1023);
+    int inner = 7419 + rshr32(2562 * f, 10);
+    int mid = 22787 + rshr32(f * inner, 10);
+    int p2 = 32768 + rshr32(f * mid, 10);
+    return rshr32(p2, (int)(-ip));
+}
+
+// per-row quantisation multiplier R = floor(127 2^(e+16) / a), e = bitlen(a)
+__device__ __forceinline__ u64 quant_mult(u64 a, int* e_out) {
+    int e = bitlen_u64(a);
+    *e_out = e;
+    return udiv64(127ull << (e + 16), a);
+}
+
+// one SwiGLU channel from saturated Q12 gate/up values (Q10 result)
+__device__ __forceinline__ int swiglu_dev(int g, int u) {
+    i64 ag = g < 0 ? -(i64)g : (i64)g;
+    i64 z = rshr(ag * 47274LL, 17);
+    int Ez = exp2q_dev(-z);
+    unsigned D = 32768u + (unsigned)Ez;                  // [2^15, 2^16]
+    // round(2^30 / D) = floor((2^31 + D) / 2D): quotient < 2^16
+    u64 num = 0x80000000ull + D, dd = (u64)D << 16;  // 2D * 2^15
+    unsigned q = 0;
+#pragma unroll
+    for (int i = 15; i >= 0; --i) {
+        q <<= 1;
+        if (num >= dd) { num -= dd; q |= 1u; }
+        dd >>= 1;
+    }
+    i64 sg = g >= 0 ? (i64)q : 32768LL - (i64)q;
+    i64 silu = rshr((i64)g * sg, 15);
+    return sat32(rshr(silu * (i64)u, 14));
+}
+
+}  // namespace detint

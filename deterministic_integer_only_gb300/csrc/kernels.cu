@@ -1,0 +1,834 @@
+// detint CUDA kernels for sm_103a: the integer-only decoder forward pass.
+//
+// Every kernel computes exactly the frozen integer arithmetic (int8 x int8
+// -> int32 GEMMs with dyadic requantisation, per-token quantisation, integer
+// RMSNorm / QK-norm, int16 RoPE tables, shift-based exp softmax with 15-bit
+// probabilities, SwiGLU, tie-low argmax), so results are bit-identical to
+// the CPU oracle and independent of batch composition, tiling and launch
+// shape (DetLLM README, intro and "Layout"; DetLLM blog, section "DetLLM").
+// Integer sums are exact in any order, so no kernel here needs a fixed
+// reduction order; none uses atomics or floating point.
+#include "kernels.h"
+#include "int_device.cuh"
+
+namespace detint {
+
+// ------------------------------------------------------------ reductions
+__device__ __forceinline__ u64 umax64(u64 a, u64 b) { return a > b ? a : b; }
+
+__device__ __forceinline__ u64 warp_max_u64(u64 v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = umax64(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ i64 warp_sum_i64(i64 v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+// 256-thread block reductions; `sm` holds 8 slots
+__device__ __forceinline__ u64 block_max_u64(u64 v, u64* sm) {
+    v = warp_max_u64(v);
+    if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
+    __syncthreads();
+    u64 r = sm[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) r = umax64(r, sm[i]);
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ i64 block_sum_i64(i64 v, i64* sm) {
+    v = warp_sum_i64(v);
+    if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
+    __syncthreads();
+    i64 r = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r += sm[i];
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ u64 absu(i64 v) { return (u64)(v < 0 ? -v : v); }
+
+// magnitude-truncating normalisation of one residual element to 24 bits
+__device__ __forceinline__ i64 norm24(i64 v, int sig) {
+    if (sig >= 0) return v < 0 ? -((-v) >> sig) : (v >> sig);
+    return v * (1LL << (-sig));
+}
+
+// --------------------------------------------------------------- embedding
+// a1: h0 = rshr(E8[id] * m_e[id], 22 - 16); decode mode also reads each
+// sequence's current length as the token position.
+__global__ void __launch_bounds__(256) k_embed(const int32_t* __restrict__ tokens,
+                                               const int32_t* __restrict__ tok_seq,
+                                               int32_t* __restrict__ tok_pos,
+                                               const int32_t* __restrict__ seq_len, int decode,
+                                               int max_pos, const int8_t* __restrict__ E,
+                                               const int32_t* __restrict__ Em, int H, int V,
+                                               int32_t* __restrict__ h, int32_t* status) {
+    const int t = blockIdx.x;
+    int id = tokens[t];
+    if (id < 0 || id >= V) {
+        if (threadIdx.x == 0) status[ST_TOKEN] = 1;
+        id = 0;
+    }
+    if (decode && threadIdx.x == 0) {
+        int p = seq_len[tok_seq[t]];
+        if (p >= max_pos) { status[ST_CTX] = 1; p = max_pos - 1; }
+        tok_pos[t] = p;
+    }
+    const i64 m = Em[id];
+    const int8_t* er = E + (size_t)id * H;
+    int32_t* hr = h + (size_t)t * H;
+    for (int i = threadIdx.x; i < H; i += 256) hr[i] = (int32_t)rshr((i64)er[i] * m, 6);
+}
+
+// ---------------------------------------------------------------- NormQuant
+// a2/a7/a10: integer RMSNorm folded into the per-token int8 quantisation.
+__global__ void __launch_bounds__(256) k_normquant(const int32_t* __restrict__ x,
+                                                   const int32_t* __restrict__ rows, int n,
+                                                   int lg_n, const int16_t* __restrict__ gamma,
+                                                   i64 eps, int8_t* __restrict__ q,
+                                                   int32_t* __restrict__ mt,
+                                                   int32_t* __restrict__ kt) {
+    __shared__ u64 redu[8];
+    __shared__ i64 bc[2];
+    const int r = blockIdx.x, tid = threadIdx.x;
+    const int src = rows ? rows[r] : r;
+    const int32_t* xr = x + (size_t)src * n;
+    int8_t* qr = q + (size_t)r * n;
+    u64 ax = 0;
+    for (int i = tid; i < n; i += 256) ax = umax64(ax, absu(xr[i]));
+    ax = block_max_u64(ax, redu);
+    if (ax == 0) {
+        for (int i = tid; i < n; i += 256) qr[i] = 0;
+        if (tid == 0) { mt[r] = 0; kt[r] = 0; }
+        return;
+    }
+    const int sig = bitlen_u64(ax) - 24;
+    i64 ss = 0;
+    u64 az = 0;
+    for (int i = tid; i < n; i += 256) {
+        i64 xp = norm24(xr[i], sig);
+        ss += xp * xp;
+        az = umax64(az, absu(xp * (i64)gamma[i]));
+    }
+    ss = block_sum_i64(ss, (i64*)redu);
+    az = block_max_u64(az, redu);
+    if (tid == 0) {
+        i64 eps_s;
+        if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (eps >> (2 * sig));
+        else eps_s = eps * (1LL << (-2 * sig));
+        u64 ms = (u64)((ss >> lg_n) + eps_s);
+        u64 rr = isqrt_u64(ms);
+        int e;
+        u64 R = quant_mult(az, &e);
+        int m, k;
+        dyadic_dev(az, 127ull * rr, &m, &k);
+        mt[r] = m;
+        kt[r] = k + 12;
+        bc[0] = (i64)R;
+        bc[1] = e;
+    }
+    __syncthreads();
+    const i64 R = bc[0];
+    const int sh = (int)bc[1] + 16;
+    for (int i = tid; i < n; i += 256) {
+        i64 z = norm24(xr[i], sig) * (i64)gamma[i];
+        qr[i] = (int8_t)rshr(z * R, sh);
+    }
+}
+
+// ----------------------------------------------------------------- ActQuant
+// a6/a9: per-token int8 quantisation of an int32 row of fixed point F.
+__global__ void __launch_bounds__(256) k_actquant(const int32_t* __restrict__ x, int n, int F,
+                                                  int8_t* __restrict__ q,
+                                                  int32_t* __restrict__ mt,
+                                                  int32_t* __restrict__ kt) {
+    __shared__ u64 redu[8];
+    __shared__ i64 bc[2];
+    const int r = blockIdx.x, tid = threadIdx.x;
+    const int32_t* xr = x + (size_t)r * n;
+    int8_t* qr = q + (size_t)r * n;
+    u64 a = 0;
+    for (int i = tid; i < n; i += 256) a = umax64(a, absu(xr[i]));
+    a = block_max_u64(a, redu);
+    if (a == 0) {
+        for (int i = tid; i < n; i += 256) qr[i] = 0;
+        if (tid == 0) { mt[r] = 0; kt[r] = 0; }
+        return;
+    }
+    if (tid == 0) {
+        int e;
+        u64 R = quant_mult(a, &e);
+        int m, k;
+        dyadic_dev(a, 127ull, &m, &k);
+        mt[r] = m;
+        kt[r] = k + F;
+        bc[0] = (i64)R;
+        bc[1] = e;
+    }
+    __syncthreads();
+    const i64 R = bc[0];
+    const int sh = (int)bc[1] + 16;
+    for (int i = tid; i < n; i += 256) qr[i] = (int8_t)rshr((i64)xr[i] * R, sh);
+}
+
+// ------------------------------------------------------- QKV post-processing
+// a4: QK-norm, RoPE from the int16 Q14 tables, per-channel-pair key shift,
+// query quantisation, and the fixed-scale K/V quantisation written into the
+// paged int8 cache (DetLLM blog, "DetLLM": K and V use fixed calibrated
+// scales and are quantised once; footnote on QK^T: per-channel key rescale
+// with the inverse on the query). One warp per (token, q head) or
+// (token, kv head); lane l holds channels l, l+32, ... so RoPE pairs
+// (i, i + d/2) sit in one lane.
+__device__ __forceinline__ i64 warp_bcast_i64(i64 v) { return __shfl_sync(0xffffffffu, v, 0); }
+
+template <int EPL>   // channels per lane: d / 32
+__device__ void qk_norm_warp(i64 (&y)[EPL], const int16_t* gamma, int lane, int lg_d, i64 eps) {
+    u64 ax = 0;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) ax = umax64(ax, absu(y[j]));
+    ax = warp_max_u64(ax);
+    if (ax == 0) return;   // all zero: output zero
+    const int sig = bitlen_u64(ax) - 24;
+    i64 xp[EPL];
+    i64 ss = 0;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) { xp[j] = norm24(y[j], sig); ss += xp[j] * xp[j]; }
+    ss = warp_sum_i64(ss);
+    i64 rr = 0, Rr = 0;
+    if (lane == 0) {
+        i64 eps_s;
+        if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (eps >> (2 * sig));
+        else eps_s = eps * (1LL << (-2 * sig));
+        rr = (i64)isqrt_u64((u64)((ss >> lg_d) + eps_s));
+        Rr = (i64)udiv64(1ull << (bitlen_u64((u64)rr) + 23), (u64)rr);
+    }
+    rr = warp_bcast_i64(rr);
+    Rr = warp_bcast_i64(Rr);
+    const int sh = bitlen_u64((u64)rr) + 21;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) y[j] = rshr(xp[j] * (i64)gamma[lane + 32 * j] * Rr, sh);
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(128) k_qkv_post(QkvPostArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int slot = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int t = blockIdx.y;
+    const int nq = a.nq, nkv = a.nkv, d = a.d, dh2 = d >> 1;
+    if (slot >= nq + nkv) return;
+    const int lg_d = (EPL == 4) ? 7 : 6;
+    const int nqkv = (nq + 2 * nkv) * d;
+    const int pos = a.tok_pos[t];
+    const int16_t* cr = a.rope_cos + (size_t)pos * dh2;
+    const int16_t* sr = a.rope_sin + (size_t)pos * dh2;
+    const int32_t* row = a.qkv + (size_t)t * nqkv;
+    const int kvh = slot < nq ? (slot >> a.lg_grp) : (slot - nq);
+    const int32_t* kvp = a.kvp + (size_t)kvh * (8 + dh2);
+    int E = 0;
+    for (int i = 0; i < dh2; ++i) E = max(E, kvp[8 + i]);
+
+    i64 y[EPL];
+    const int base = slot < nq ? slot * d : (nq + kvh) * d;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) y[j] = row[base + lane + 32 * j];
+    if (a.qk_norm) {
+        qk_norm_warp<EPL>(y, slot < nq ? a.q_gamma : a.k_gamma, lane, lg_d, a.eps_qk);
+    } else {
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) y[j] *= 4;
+    }
+    // RoPE, rotate-dh2 pairing
+#pragma unroll
+    for (int j = 0; j < EPL / 2; ++j) {
+        const int i = lane + 32 * j;
+        const i64 c = cr[i], s = sr[i];
+        const i64 x0 = y[j], x1 = y[j + EPL / 2];
+        y[j] = rshr(x0 * c - x1 * s, 14);
+        y[j + EPL / 2] = rshr(x1 * c + x0 * s, 14);
+    }
+    if (slot < nq) {
+        // query: multiply channel c by 2^(E - e_c), then per-head ActQuant (F = 14)
+        u64 am = 0;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int i = lane + 32 * j;
+            const int ec = kvp[8 + (i & (dh2 - 1))];
+            y[j] = y[j] * (1LL << (E - ec));
+            am = umax64(am, absu(y[j]));
+        }
+        am = warp_max_u64(am);
+        int8_t* qo = a.q8 + ((size_t)t * nq + slot) * d;
+        if (am == 0) {
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) qo[lane + 32 * j] = 0;
+            if (lane == 0) { a.mq[t * nq + slot] = 0; a.kq[t * nq + slot] = 0; }
+            return;
+        }
+        i64 R = 0, e = 0;
+        if (lane == 0) {
+            int ee;
+            R = (i64)quant_mult(am, &ee);
+            e = ee;
+            int m, k;
+            dyadic_dev(am, 127ull, &m, &k);
+            a.mq[t * nq + slot] = m;
+            a.kq[t * nq + slot] = k + 14;
+        }
+        R = warp_bcast_i64(R);
+        e = warp_bcast_i64(e);
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) qo[lane + 32 * j] = (int8_t)rshr(y[j] * R, (int)e + 16);
+    } else {
+        // key and value of kv head kvh at (sequence, position) in the paged cache
+        const int seq = a.tok_seq[t];
+        const int blk = a.block_table[(size_t)seq * a.mbs + (pos >> 6)];
+        const int off = pos & (KV_BLK - 1);
+        int8_t* kd = a.kc + (((size_t)blk * nkv + kvh) * KV_BLK + off) * d;
+        int8_t* vd = a.vc + ((size_t)blk * nkv + kvh) * d * KV_BLK + off;
+        const i64 KQM = kvp[0], VQM = kvp[2];
+        const int KQS = kvp[1], VQS = kvp[3];
+        const int32_t* vrow = row + (nq + nkv + kvh) * d;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int i = lane + 32 * j;
+            const int ec = kvp[8 + (i & (dh2 - 1))];
+            kd[i] = (int8_t)sat127(rshr(y[j] * (1LL << ec) * KQM, KQS));
+            vd[(size_t)i * KV_BLK] = (int8_t)sat127(rshr((i64)vrow[i] * VQM, VQS));
+        }
+    }
+}
+
+// --------------------------------------------------------------- attention
+// a5: one CTA per (token, kv head) serving its group of q heads. Scores
+// S = q8 . k8 (dp4a), base-2 logits, exact row max, 15-bit E_j by the
+// shift-based exp, then num = sum E_j v8_j as two exact int8 products
+// (E = 256 E_hi + E_lo) and one deferred division (DetLLM blog footnote on
+// QK^T: 15-bit probabilities, P.V exactly with two int8 GEMMs).
+__device__ __forceinline__ int dp4a_us(unsigned a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+constexpr int MAXG = 8;   // q heads per kv head supported
+
+size_t attention_smem_bytes(int grp, int d, int ctx_cap) {
+    // q [G][d] + S [G][ctx] int32 + Elo/Ehi [G][ctx] bytes + reductions
+    return (size_t)grp * d + (size_t)grp * ctx_cap * 6 + 2 * 8 * 4 * (size_t)MAXG * 8 +
+           2 * 256 * (size_t)MAXG * 4 + 256;
+}
+
+__global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
+    extern __shared__ __align__(16) unsigned char sm[];
+    const int t = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+    const int d = a.d, G = 1 << a.lg_grp, nkv = a.nkv, cap = a.ctx_cap;
+    const int seq = a.tok_seq[t];
+    const int ctx = a.tok_pos[t] + 1;
+    const int ctx16 = (ctx + 15) & ~15;
+    int8_t* qs = (int8_t*)sm;                                   // [G][d]
+    int32_t* S = (int32_t*)(sm + ((G * d + 15) & ~15));        // [G][cap]
+    unsigned char* Elo = (unsigned char*)(S + (size_t)G * cap); // [G][cap]
+    unsigned char* Ehi = Elo + (size_t)G * cap;                 // [G][cap]
+    i64* red = (i64*)(((uintptr_t)(Ehi + (size_t)G * cap) + 15) & ~(uintptr_t)15);   // [8][G]
+    int* part = (int*)(red + 8 * MAXG);                         // [2][256][G]
+    __shared__ i64 umax_s[MAXG], sig_s[MAXG], rs_s[MAXG];
+
+    const int32_t* kvp = a.kvp + (size_t)g * (8 + (d >> 1));
+    const i64 CSTM = kvp[6], MV = kvp[4];
+    const int CSTK = kvp[7], KVS = kvp[5];
+    const int* bt = a.block_table + (size_t)seq * a.mbs;
+
+    for (int i = tid; i < G * d; i += 256)
+        qs[i] = a.q8[((size_t)t * a.nq + (g << a.lg_grp)) * d + i];
+    __syncthreads();
+
+    // phase 1: scores and per-head maxima
+    int smax[MAXG];
+#pragma unroll
+    for (int hh = 0; hh < MAXG; ++hh) smax[hh] = -2147483647;
+    for (int j = tid; j < ctx; j += 256) {
+        const int blk = bt[j >> 6];
+        const int4* kr = (const int4*)(a.kc + (((size_t)blk * nkv + g) * KV_BLK + (j & 63)) * d);
+        int acc[MAXG];
+#pragma unroll
+        for (int hh = 0; hh < MAXG; ++hh) acc[hh] = 0;
+        for (int v = 0; v < (d >> 4); ++v) {
+            const int4 kw = kr[v];
+#pragma unroll
+            for (int hh = 0; hh < MAXG; ++hh) {
+                if (hh < G) {
+                    const int4 qw = *(const int4*)(qs + hh * d + v * 16);
+                    acc[hh] = __dp4a(kw.x, qw.x, acc[hh]);
+                    acc[hh] = __dp4a(kw.y, qw.y, acc[hh]);
+                    acc[hh] = __dp4a(kw.z, qw.z, acc[hh]);
+                    acc[hh] = __dp4a(kw.w, qw.w, acc[hh]);
+                }
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < MAXG; ++hh)
+            if (hh < G) { S[hh * cap + j] = acc[hh]; smax[hh] = max(smax[hh], acc[hh]); }
+    }
+    {
+        const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+        for (int hh = 0; hh < MAXG; ++hh) {
+            if (hh < G) {
+                int v = smax[hh];
+#pragma unroll
+                for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+                if (lane == 0) red[w * MAXG + hh] = v;
+            }
+        }
+        __syncthreads();
+        if (tid < G) {
+            i64 v = red[tid];
+            for (int w2 = 1; w2 < 8; ++w2) v = v > red[w2 * MAXG + tid] ? v : red[w2 * MAXG + tid];
+            const i64 mq = a.mq[(size_t)t * a.nq + (g << a.lg_grp) + tid];
+            const int kq = a.kq[(size_t)t * a.nq + (g << a.lg_grp) + tid];
+            umax_s[tid] = rshr(v * mq * CSTM, kq + CSTK - 10);
+        }
+        __syncthreads();
+    }
+    // phase 2: E_j (15 bits) split into bytes, and the row sums
+    {
+        i64 sum[MAXG];
+#pragma unroll
+        for (int hh = 0; hh < MAXG; ++hh) sum[hh] = 0;
+        for (int j = tid; j < ctx16; j += 256) {
+#pragma unroll
+            for (int hh = 0; hh < MAXG; ++hh) {
+                if (hh < G) {
+                    int E = 0;
+                    if (j < ctx) {
+                        const i64 mq = a.mq[(size_t)t * a.nq + (g << a.lg_grp) + hh];
+                        const int kq = a.kq[(size_t)t * a.nq + (g << a.lg_grp) + hh];
+                        const i64 u = rshr((i64)S[hh * cap + j] * mq * CSTM, kq + CSTK - 10);
+                        E = min(32767, exp2q_dev(u - umax_s[hh]));
+                    }
+                    Elo[hh * cap + j] = (unsigned char)(E & 255);
+                    Ehi[hh * cap + j] = (unsigned char)(E >> 8);
+                    sum[hh] += E;
+                }
+            }
+        }
+        const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+        for (int hh = 0; hh < MAXG; ++hh) {
+            if (hh < G) {
+                i64 v = warp_sum_i64(sum[hh]);
+                if (lane == 0) red[w * MAXG + hh] = v;
+            }
+        }
+        __syncthreads();
+        if (tid < G) {
+            i64 v = 0;
+            for (int w2 = 0; w2 < 8; ++w2) v += red[w2 * MAXG + tid];
+            sig_s[tid] = v;
+            const int bl = bitlen_u64((u64)v);
+            rs_s[tid] = (i64)udiv64(1ull << (bl + 23), (u64)v);
+        }
+        __syncthreads();
+    }
+    // phase 3: two exact int8 products per 4 keys (E_lo u8 x v8, E_hi x v8)
+    {
+        const int parts = 256 >> (d == 128 ? 7 : 6);   // threads per channel
+        const int c = tid & (d - 1);
+        const int p = tid >> (d == 128 ? 7 : 6);
+        int lo[MAXG], hi[MAXG];
+#pragma unroll
+        for (int hh = 0; hh < MAXG; ++hh) { lo[hh] = 0; hi[hh] = 0; }
+        for (int j0 = p * 16; j0 < ctx16; j0 += parts * 16) {
+            const int blk = bt[j0 >> 6];
+            const int4 vw = *(const int4*)(a.vc + (((size_t)blk * nkv + g) * d + c) * KV_BLK + (j0 & 63));
+#pragma unroll
+            for (int hh = 0; hh < MAXG; ++hh) {
+                if (hh < G) {
+                    const uint4 el = *(const uint4*)(Elo + hh * cap + j0);
+                    const int4 eh = *(const int4*)(Ehi + hh * cap + j0);
+                    lo[hh] = dp4a_us(el.x, vw.x, lo[hh]);
+                    lo[hh] = dp4a_us(el.y, vw.y, lo[hh]);
+                    lo[hh] = dp4a_us(el.z, vw.z, lo[hh]);
+                    lo[hh] = dp4a_us(el.w, vw.w, lo[hh]);
+                    hi[hh] = __dp4a(eh.x, vw.x, hi[hh]);
+                    hi[hh] = __dp4a(eh.y, vw.y, hi[hh]);
+                    hi[hh] = __dp4a(eh.z, vw.z, hi[hh]);
+                    hi[hh] = __dp4a(eh.w, vw.w, hi[hh]);
+                }
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < MAXG; ++hh) {
+            if (hh < G) {
+                part[(0 * 256 + tid) * MAXG + hh] = lo[hh];
+                part[(1 * 256 + tid) * MAXG + hh] = hi[hh];
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < (G << (d == 128 ? 7 : 6)); idx += 256) {
+            const int hh = idx >> (d == 128 ? 7 : 6);
+            const int cc = idx & (d - 1);
+            i64 nlo = 0, nhi = 0;
+            for (int q = 0; q < parts; ++q) {
+                nlo += part[(0 * 256 + q * d + cc) * MAXG + hh];
+                nhi += part[(1 * 256 + q * d + cc) * MAXG + hh];
+            }
+            const i64 num = nhi * 256 + nlo;
+            const i64 sg = sig_s[hh];
+            const int bl = bitlen_u64((u64)sg);
+            const i64 tq = rshr(num * rs_s[hh], bl + 7);
+            const i64 ov = rshr(tq * MV, KVS + 16 - 12);
+            a.o[(size_t)t * a.nq * d + ((g << a.lg_grp) + hh) * d + cc] = (int32_t)ov;
+        }
+    }
+}
+
+// ------------------------------------------------------------- GEMV (M<=32)
+// Weights stream from HBM with 128-bit non-allocating loads straight into
+// mma.sync m16n8k32 s8 fragments: a thread's 16 contiguous bytes of weight
+// row g and of row g+8 feed two MMAs. Within a 64-byte chunk the k order is
+// permuted identically for weights and activations, which leaves the exact
+// integer dot product unchanged. The 8 warps of a CTA split K; the CTA sums
+// their partial tiles in shared memory and applies the requant epilogue.
+__device__ __forceinline__ int4 ldg_stream(const int8_t* p) {
+    int4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void mma_s8(int (&c)[4], int a0, int a1, int a2, int a3, int b0, int b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// requantised value of one accumulator for (token m, weight row n)
+__device__ __forceinline__ i64 requant_dev(int acc, const Epi& ep, int m, int n) {
+    const i64 M = (i64)ep.mt[m] * (i64)ep.mc[n];
+    return rshr((i64)acc * M, ep.kt[m] + 22 - ep.fout);
+}
+
+template <int MODE>
+__device__ __forceinline__ void epi_store(const Epi& ep, int m, int n, int acc) {
+    if (MODE == EPI_RAW) {
+        ep.out[(size_t)m * ep.ldo + n] = acc;
+    } else if (MODE == EPI_QKV) {
+        const i64 y = requant_dev(acc, ep, m, n);
+        if (y > 2147483647LL || y < -2147483647LL) ep.status[ST_SAT_QKV] = 1;
+        ep.out[(size_t)m * ep.ldo + n] = sat32(y);
+    } else if (MODE == EPI_RESADD) {
+        const i64 y = sat32(requant_dev(acc, ep, m, n));
+        int32_t* hp = ep.out + (size_t)m * ep.ldo + n;
+        const i64 s = (i64)*hp + y;
+        if (s > 2147483647LL || s < -2147483647LL) ep.status[ST_SAT_RES] = 1;
+        *hp = sat32(s);
+    }
+}
+
+template <int NT, int MODE>
+__global__ void __launch_bounds__(256) k_gemv(const int8_t* __restrict__ W,
+                                              const int8_t* __restrict__ X, int M, int N, int K,
+                                              Epi ep) {
+    extern __shared__ __align__(16) unsigned char sm[];
+    constexpr int NTOK = 8 * NT;
+    const int pitch = K + 64;                          // bank-conflict-free fragment loads
+    int8_t* xs = (int8_t*)sm;                          // [NTOK][pitch]
+    int32_t* red = (int32_t*)(sm + (size_t)NTOK * pitch);   // [8][16][NTOK]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
+    const int n0 = blockIdx.x * 16;
+
+    const int kv = K >> 4;
+    for (int r = 0; r < NTOK; ++r)
+        for (int v = tid; v < kv; v += 256) {
+            int4 val = make_int4(0, 0, 0, 0);
+            if (r < M) val = *(const int4*)(X + (size_t)r * K + v * 16);
+            *(int4*)(xs + r * pitch + v * 16) = val;
+        }
+    __syncthreads();
+
+    int acc[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0;
+    const int rlo = min(n0 + g, N - 1), rhi = min(n0 + g + 8, N - 1);
+    const int8_t* wlo = W + (size_t)rlo * K + 16 * tq;
+    const int8_t* whi = W + (size_t)rhi * K + 16 * tq;
+    const int8_t* xb = xs + g * pitch + 16 * tq;
+    const int nch = K >> 6;
+    int c = warp;
+    for (; c + 24 < nch; c += 32) {
+        int4 al[4], ah[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            al[u] = ldg_stream(wlo + (c + 8 * u) * 64);
+            ah[u] = ldg_stream(whi + (c + 8 * u) * 64);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int4 b = *(const int4*)(xb + nt * 8 * pitch + (c + 8 * u) * 64);
+                mma_s8(acc[nt], al[u].x, ah[u].x, al[u].y, ah[u].y, b.x, b.y);
+                mma_s8(acc[nt], al[u].z, ah[u].z, al[u].w, ah[u].w, b.z, b.w);
+            }
+        }
+    }
+    for (; c < nch; c += 8) {
+        const int4 al = ldg_stream(wlo + c * 64), ah = ldg_stream(whi + c * 64);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int4 b = *(const int4*)(xb + nt * 8 * pitch + c * 64);
+            mma_s8(acc[nt], al.x, ah.x, al.y, ah.y, b.x, b.y);
+            mma_s8(acc[nt], al.z, ah.z, al.w, ah.w, b.z, b.w);
+        }
+    }
+    // accumulator fragment: c0 (row g, tok 2tq), c1 (g, 2tq+1), c2 (g+8, 2tq), c3 (g+8, 2tq+1)
+    int32_t* rw = red + warp * 16 * NTOK;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        rw[g * NTOK + nt * 8 + 2 * tq] = acc[nt][0];
+        rw[g * NTOK + nt * 8 + 2 * tq + 1] = acc[nt][1];
+        rw[(g + 8) * NTOK + nt * 8 + 2 * tq] = acc[nt][2];
+        rw[(g + 8) * NTOK + nt * 8 + 2 * tq + 1] = acc[nt][3];
+    }
+    __syncthreads();
+    if (MODE == EPI_SWIGLU) {
+        // weight rows are interleaved (gate_i, up_i) pairs: rows 2i, 2i+1
+        for (int idx = tid; idx < 8 * NTOK; idx += 256) {
+            const int p = idx / NTOK, tk = idx % NTOK;   // NTOK is a compile-time power of two
+            int sg = 0, su = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                sg += red[(w * 16 + 2 * p) * NTOK + tk];
+                su += red[(w * 16 + 2 * p + 1) * NTOK + tk];
+            }
+            const int n = n0 + 2 * p;
+            if (tk < M && n < N) {
+                i64 yg = requant_dev(sg, ep, tk, n), yu = requant_dev(su, ep, tk, n + 1);
+                if (yg > (1 << 24) || yg < -(1 << 24) || yu > (1 << 24) || yu < -(1 << 24))
+                    ep.status[ST_SAT_GU] = 1;
+                yg = sat_b(yg, 1 << 24);
+                yu = sat_b(yu, 1 << 24);
+                ep.out[(size_t)tk * ep.ldo + (n >> 1)] = swiglu_dev((int)yg, (int)yu);
+            }
+        }
+    } else if (MODE == EPI_LOGITS) {
+        int32_t* lg = red;   // reuse: [16][NTOK] after the sums (warp 0 slot)
+        int vals[(16 * NTOK + 255) / 256];
+        int cnt = 0;
+        for (int idx = tid; idx < 16 * NTOK; idx += 256, ++cnt) {
+            int s = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s += red[w * 16 * NTOK + idx];
+            vals[cnt] = s;
+        }
+        __syncthreads();
+        cnt = 0;
+        for (int idx = tid; idx < 16 * NTOK; idx += 256, ++cnt) {
+            const int r = idx / NTOK, tk = idx % NTOK;
+            const int n = n0 + r;
+            int out = -2147483647;
+            if (tk < M && n < N) {
+                const i64 y = requant_dev(vals[cnt], ep, tk, n);
+                if (y > 2147483647LL || y < -2147483647LL) ep.status[ST_SAT_LOGIT] = 1;
+                out = sat32(y);
+                ep.out[(size_t)tk * ep.ldo + n] = out;
+            }
+            lg[idx] = out;
+        }
+        __syncthreads();
+        if (tid < NTOK && tid < M) {
+            int bv = lg[tid], bi = n0;
+            for (int r = 1; r < 16; ++r) {
+                const int v = lg[r * NTOK + tid];
+                if (v > bv && n0 + r < N) { bv = v; bi = n0 + r; }
+            }
+            ep.pval[(size_t)tid * ep.npart + blockIdx.x] = bv;
+            ep.pidx[(size_t)tid * ep.npart + blockIdx.x] = bi;
+        }
+    } else {
+        for (int idx = tid; idx < 16 * NTOK; idx += 256) {
+            const int r = idx / NTOK, tk = idx % NTOK;
+            int s = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s += red[w * 16 * NTOK + idx];
+            const int n = n0 + r;
+            if (tk < M && n < N) epi_store<MODE>(ep, tk, n, s);
+        }
+    }
+}
+
+static size_t gemv_smem_bytes(int NT, int K) {
+    return (size_t)8 * NT * (K + 64) + (size_t)8 * 16 * 8 * NT * 4;
+}
+constexpr size_t GEMV_SMEM_MAX = 200 * 1024;
+
+template <int NT, int MODE>
+static cudaError_t gemv_attr() {
+    return cudaFuncSetAttribute(k_gemv<NT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)GEMV_SMEM_MAX);
+}
+
+template <int NT, int MODE>
+static cudaError_t gemv_launch_t(const int8_t* W, const int8_t* X, int M, int N, int K,
+                                 const Epi& ep, cudaStream_t s) {
+    const size_t smem = gemv_smem_bytes(NT, K);
+    const int grid = (N + 15) / 16;
+    k_gemv<NT, MODE><<<grid, 256, smem, s>>>(W, X, M, N, K, ep);
+    return cudaGetLastError();
+}
+
+// the Epi of rows m0.. of a larger launch
+static Epi epi_rows(const Epi& ep, int m0) {
+    Epi e = ep;
+    if (e.out) e.out += (size_t)m0 * ep.ldo;
+    if (e.mt) e.mt += m0;
+    if (e.kt) e.kt += m0;
+    if (e.pval) e.pval += (size_t)m0 * ep.npart;
+    if (e.pidx) e.pidx += (size_t)m0 * ep.npart;
+    return e;
+}
+
+template <int MODE>
+static cudaError_t gemv_nt(const int8_t* W, const int8_t* X, int M, int N, int K, const Epi& ep,
+                           cudaStream_t s) {
+    if (M <= 8) return gemv_launch_t<1, MODE>(W, X, M, N, K, ep, s);
+    if (M <= 16 || gemv_smem_bytes(4, K) > GEMV_SMEM_MAX) {
+        if (M <= 16) return gemv_launch_t<2, MODE>(W, X, M, N, K, ep, s);
+        cudaError_t e = gemv_launch_t<2, MODE>(W, X, 16, N, K, ep, s);
+        if (e != cudaSuccess) return e;
+        return gemv_nt<MODE>(W, X + (size_t)16 * K, M - 16, N, K, epi_rows(ep, 16), s);
+    }
+    return gemv_launch_t<4, MODE>(W, X, M, N, K, ep, s);
+}
+
+cudaError_t launch_gemv(const int8_t* W, const int8_t* X, int M, int N, int K, int mode,
+                        const Epi& ep, cudaStream_t s) {
+    if (M < 1 || M > 32 || N < 1 || (K & 63) || K < 64) return cudaErrorInvalidValue;
+    switch (mode) {
+        case EPI_RAW: return gemv_nt<EPI_RAW>(W, X, M, N, K, ep, s);
+        case EPI_QKV: return gemv_nt<EPI_QKV>(W, X, M, N, K, ep, s);
+        case EPI_RESADD: return gemv_nt<EPI_RESADD>(W, X, M, N, K, ep, s);
+        case EPI_SWIGLU: return gemv_nt<EPI_SWIGLU>(W, X, M, N, K, ep, s);
+        case EPI_LOGITS: return gemv_nt<EPI_LOGITS>(W, X, M, N, K, ep, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// ----------------------------------------------------------- argmax (a11)
+// Final reduction of the per-CTA (max, lowest index) partials of one row;
+// ties go to the lowest token id (DetLLM blog, "DetLLM").
+__device__ __forceinline__ void better(int& bv, int& bi, int v, int i) {
+    if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+}
+__global__ void __launch_bounds__(256) k_argmax_final(const int32_t* __restrict__ pval,
+                                                      const int32_t* __restrict__ pidx, int npart,
+                                                      int32_t* __restrict__ next_tok,
+                                                      const int32_t* __restrict__ tok_seq,
+                                                      int32_t* __restrict__ seq_len) {
+    __shared__ int sv[8], si[8];
+    const int r = blockIdx.x, tid = threadIdx.x;
+    int bv = -2147483647 - 1, bi = 2147483647;
+    for (int i = tid; i < npart; i += 256)
+        better(bv, bi, pval[(size_t)r * npart + i], pidx[(size_t)r * npart + i]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const int v = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int i = __shfl_xor_sync(0xffffffffu, bi, o);
+        better(bv, bi, v, i);
+    }
+    if ((tid & 31) == 0) { sv[tid >> 5] = bv; si[tid >> 5] = bi; }
+    __syncthreads();
+    if (tid == 0) {
+        bv = sv[0]; bi = si[0];
+        for (int w = 1; w < 8; ++w) better(bv, bi, sv[w], si[w]);
+        next_tok[r] = bi;
+        if (seq_len) seq_len[tok_seq[r]] += 1;
+    }
+}
+
+// ------------------------------------------------------------- launchers
+cudaError_t launch_embed(const int32_t* tokens, int T, const int32_t* tok_seq, int32_t* tok_pos,
+                         const int32_t* seq_len, int decode, int max_pos, const int8_t* E,
+                         const int32_t* Em, int H, int V, int32_t* h, int32_t* status,
+                         cudaStream_t s) {
+    k_embed<<<T, 256, 0, s>>>(tokens, tok_seq, tok_pos, seq_len, decode, max_pos, E, Em, H, V, h,
+                              status);
+    return cudaGetLastError();
+}
+
+static int ilog2(int n) { int l = 0; while ((1 << l) < n) ++l; return l; }
+
+cudaError_t launch_normquant(const int32_t* x, const int32_t* rows, int R, int n,
+                             const int16_t* gamma, long long eps, int8_t* q, int32_t* mt,
+                             int32_t* kt, cudaStream_t s) {
+    k_normquant<<<R, 256, 0, s>>>(x, rows, n, ilog2(n), gamma, eps, q, mt, kt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_actquant(const int32_t* x, int R, int n, int F, int8_t* q, int32_t* mt,
+                            int32_t* kt, cudaStream_t s) {
+    k_actquant<<<R, 256, 0, s>>>(x, n, F, q, mt, kt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qkv_post(const QkvPostArgs& a, cudaStream_t s) {
+    dim3 grid((a.nq + a.nkv + 3) / 4, a.T);
+    if (a.d == 128) k_qkv_post<4><<<grid, 128, 0, s>>>(a);
+    else if (a.d == 64) k_qkv_post<2><<<grid, 128, 0, s>>>(a);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
+    const size_t smem = attention_smem_bytes(1 << a.lg_grp, a.d, a.ctx_cap);
+    dim3 grid(a.T, a.nkv);
+    k_attention<<<grid, 256, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int rows, int npart,
+                                int32_t* next_tok, const int32_t* tok_seq, int32_t* seq_len,
+                                cudaStream_t s) {
+    k_argmax_final<<<rows, 256, 0, s>>>(pval, pidx, npart, next_tok, tok_seq, seq_len);
+    return cudaGetLastError();
+}
+
+// M > 32 without the tiled GEMM: the GEMV in 32-token chunks (each chunk
+// streams the weights again)
+cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, int mode,
+                        const Epi& ep, cudaStream_t s) {
+    if (K & 63) return cudaErrorInvalidValue;
+    for (int m0 = 0; m0 < M; m0 += 32) {
+        const int mc = M - m0 < 32 ? M - m0 : 32;
+        cudaError_t e = launch_gemv(W, A + (size_t)m0 * K, mc, N, K, mode, epi_rows(ep, m0), s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <int MODE>
+static cudaError_t gemv_attr_all() {
+    cudaError_t e = gemv_attr<1, MODE>();
+    if (e == cudaSuccess) e = gemv_attr<2, MODE>();
+    if (e == cudaSuccess) e = gemv_attr<4, MODE>();
+    return e;
+}
+
+cudaError_t kernels_init() {
+    cudaError_t e = gemv_attr_all<EPI_RAW>();
+    if (e == cudaSuccess) e = gemv_attr_all<EPI_QKV>();
+    if (e == cudaSuccess) e = gemv_attr_all<EPI_RESADD>();
+    if (e == cudaSuccess) e = gemv_attr_all<EPI_SWIGLU>();
+    if (e == cudaSuccess) e = gemv_attr_all<EPI_LOGITS>();
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    return e;
+}
+
+}  // namespace detint

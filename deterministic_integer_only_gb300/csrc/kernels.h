@@ -1,0 +1,103 @@
+// Host-side launchers of the detint CUDA kernels (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace detint {
+
+// status word slots (plain stores of 1; never atomics into results)
+enum {
+    ST_TOKEN = 0,     // a token id outside [0, V) was replaced by 0
+    ST_CTX = 1,       // a position beyond the KV capacity was clamped
+    ST_SAT_RES = 2,   // a residual add saturated
+    ST_SAT_GU = 3,    // a gate/up output saturated at 2^24
+    ST_SAT_LOGIT = 4, // a logit saturated
+    ST_SAT_QKV = 5,   // a q/k/v output saturated
+    ST_N = 8
+};
+
+enum EpiMode { EPI_RAW = 0, EPI_QKV = 1, EPI_RESADD = 2, EPI_SWIGLU = 3, EPI_LOGITS = 4 };
+
+constexpr int KV_BLK = 64;   // tokens per KV-cache block
+
+struct Epi {
+    int32_t* out;          // output base (int32)
+    int ldo;               // output row stride (elements)
+    const int32_t* mt;     // per-token scale mantissa [M]
+    const int32_t* kt;     // per-token scale shift [M]
+    const int32_t* mc;     // per-weight-row scale mantissa [N]
+    int fout;              // output fixed point
+    int32_t* status;
+    int32_t* pval;         // EPI_LOGITS: argmax partial values [M][npart]
+    int32_t* pidx;         // EPI_LOGITS: argmax partial indices [M][npart]
+    int npart;
+};
+
+// C[m][n] epilogue of sum_k X[m][k] W[n][k]; W row-major [N][K], X [M][K];
+// requires K % 64 == 0, M <= 32 per call (rows of X beyond M are not read)
+cudaError_t launch_gemv(const int8_t* W, const int8_t* X, int M, int N, int K, int mode,
+                        const Epi& ep, cudaStream_t s);
+
+// tiled GEMM for any M (TMA + mma.sync); K % 16 == 0
+cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, int mode,
+                        const Epi& ep, cudaStream_t s);
+
+cudaError_t launch_embed(const int32_t* tokens, int T, const int32_t* tok_seq, int32_t* tok_pos,
+                         const int32_t* seq_len, int decode, int max_pos, const int8_t* E,
+                         const int32_t* Em, int H, int V, int32_t* h, int32_t* status,
+                         cudaStream_t s);
+
+cudaError_t launch_normquant(const int32_t* x, const int32_t* rows, int R, int n,
+                             const int16_t* gamma, long long eps, int8_t* q, int32_t* mt,
+                             int32_t* kt, cudaStream_t s);
+
+cudaError_t launch_actquant(const int32_t* x, int R, int n, int F, int8_t* q, int32_t* mt,
+                            int32_t* kt, cudaStream_t s);
+
+struct QkvPostArgs {
+    const int32_t* qkv;      // [T][(nq + 2 nkv) d] Q12
+    const int16_t* q_gamma;
+    const int16_t* k_gamma;
+    int qk_norm;
+    long long eps_qk;
+    const int16_t* rope_cos; // [max_pos][d/2]
+    const int16_t* rope_sin;
+    const int32_t* kvp;      // [nkv][8 + d/2]
+    const int32_t* tok_seq;
+    const int32_t* tok_pos;
+    const int32_t* block_table;
+    int mbs;                 // block-table entries per sequence
+    int8_t* q8;              // [T][nq][d]
+    int32_t* mq;             // [T][nq]
+    int32_t* kq;
+    int8_t* kc;              // this layer's K cache [NB][nkv][64][d]
+    int8_t* vc;              // this layer's V cache [NB][nkv][d][64]
+    int T, nq, nkv, d, lg_grp;
+};
+cudaError_t launch_qkv_post(const QkvPostArgs& a, cudaStream_t s);
+
+struct AttnArgs {
+    const int8_t* q8;
+    const int32_t* mq;
+    const int32_t* kq;
+    const int8_t* kc;
+    const int8_t* vc;
+    const int32_t* block_table;
+    int mbs;
+    const int32_t* tok_seq;
+    const int32_t* tok_pos;
+    const int32_t* kvp;
+    int32_t* o;              // [T][nq d] Q12
+    int T, nq, nkv, d, lg_grp;
+    int ctx_cap;             // keys that fit the shared-memory row
+};
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
+size_t attention_smem_bytes(int grp, int d, int ctx_cap);
+
+cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int rows, int npart,
+                                int32_t* next_tok, const int32_t* tok_seq, int32_t* seq_len,
+                                cudaStream_t s);
+
+cudaError_t kernels_init();
+
+}  // namespace detint

@@ -1,0 +1,631 @@
+// detint host runtime: artifact loading (SHA-256 checked), device memory
+// layout, the per-step launch sequence, CUDA-graph replay of decode steps,
+// and the C ABI declared in include/detint.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/detint.h"
+#include "kernels.h"
+
+using namespace detint;
+
+// ------------------------------------------------------------ last error
+static thread_local std::string g_last_error;
+static int fail(int code, const std::string& msg) {
+    g_last_error = msg;
+    return code;
+}
+#define CK(call)                                                                         \
+    do {                                                                                 \
+        cudaError_t e_ = (call);                                                         \
+        if (e_ != cudaSuccess)                                                           \
+            return fail(DETINT_E_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+    } while (0)
+
+// ------------------------------------------------ SHA-256 (FIPS 180-4)
+namespace {
+struct Sha256 {
+    uint32_t h[8];
+    uint8_t buf[64];
+    uint64_t len = 0;
+    size_t fill = 0;
+    static uint32_t rotr(uint32_t x, int n) { return (x >> n) | (x << (32 - n)); }
+    Sha256() {
+        static const uint32_t init[8] = {0x6a09e667, 0xbb67ae85, 0x3c6ef372, 0xa54ff53a,
+                                         0x510e527f, 0x9b05688c, 0x1f83d9ab, 0x5be0cd19};
+        memcpy(h, init, sizeof h);
+    }
+    void block(const uint8_t* p) {
+        static const uint32_t k[64] = {
+            0x428a2f98, 0x71374491, 0xb5c0fbcf, 0xe9b5dba5, 0x3956c25b, 0x59f111f1, 0x923f82a4,
+            0xab1c5ed5, 0xd807aa98, 0x12835b01, 0x243185be, 0x550c7dc3, 0x72be5d74, 0x80deb1fe,
+            0x9bdc06a7, 0xc19bf174, 0xe49b69c1, 0xefbe4786, 0x0fc19dc6, 0x240ca1cc, 0x2de92c6f,
+            0x4a7484aa, 0x5cb0a9dc, 0x76f988da, 0x983e5152, 0xa831c66d, 0xb00327c8, 0xbf597fc7,
+            0xc6e00bf3, 0xd5a79147, 0x06ca6351, 0x14292967, 0x27b70a85, 0x2e1b2138, 0x4d2c6dfc,
+            0x53380d13, 0x650a7354, 0x766a0abb, 0x81c2c92e, 0x92722c85, 0xa2bfe8a1, 0xa81a664b,
+            0xc24b8b70, 0xc76c51a3, 0xd192e819, 0xd6990624, 0xf40e3585, 0x106aa070, 0x19a4c116,
+            0x1e376c08, 0x2748774c, 0x34b0bcb5, 0x391c0cb3, 0x4ed8aa4a, 0x5b9cca4f, 0x682e6ff3,
+            0x748f82ee, 0x78a5636f, 0x84c87814, 0x8cc70208, 0x90befffa, 0xa4506ceb, 0xbef9a3f7,
+            0xc67178f2};
+        uint32_t w[64];
+        for (int i = 0; i < 16; ++i)
+            w[i] = (uint32_t)p[4 * i] << 24 | (uint32_t)p[4 * i + 1] << 16 |
+                   (uint32_t)p[4 * i + 2] << 8 | p[4 * i + 3];
+        for (int i = 16; i < 64; ++i) {
+            uint32_t s0 = rotr(w[i - 15], 7) ^ rotr(w[i - 15], 18) ^ (w[i - 15] >> 3);
+            uint32_t s1 = rotr(w[i - 2], 17) ^ rotr(w[i - 2], 19) ^ (w[i - 2] >> 10);
+            w[i] = w[i - 16] + s0 + w[i - 7] + s1;
+        }
+        uint32_t a = h[0], b = h[1], c = h[2], d = h[3], e = h[4], f = h[5], g = h[6], hh = h[7];
+        for (int i = 0; i < 64; ++i) {
+            uint32_t S1 = rotr(e, 6) ^ rotr(e, 11) ^ rotr(e, 25);
+            uint32_t ch = (e & f) ^ (~e & g);
+            uint32_t t1 = hh + S1 + ch + k[i] + w[i];
+            uint32_t S0 = rotr(a, 2) ^ rotr(a, 13) ^ rotr(a, 22);
+            uint32_t mj = (a & b) ^ (a & c) ^ (b & c);
+            uint32_t t2 = S0 + mj;
+            hh = g; g = f; f = e; e = d + t1; d = c; c = b; b = a; a = t1 + t2;
+        }
+        h[0] += a; h[1] += b; h[2] += c; h[3] += d; h[4] += e; h[5] += f; h[6] += g; h[7] += hh;
+    }
+    void update(const uint8_t* p, size_t n) {
+        len += n;
+        if (fill) {
+            while (n && fill < 64) { buf[fill++] = *p++; --n; }
+            if (fill == 64) { block(buf); fill = 0; }
+        }
+        while (n >= 64) { block(p); p += 64; n -= 64; }
+        while (n) { buf[fill++] = *p++; --n; }
+    }
+    std::string hex() {
+        uint64_t bits = len * 8;
+        uint8_t pad = 0x80;
+        update(&pad, 1);
+        uint8_t z = 0;
+        while (fill != 56) update(&z, 1);
+        uint8_t lb[8];
+        for (int i = 0; i < 8; ++i) lb[i] = (uint8_t)(bits >> (56 - 8 * i));
+        update(lb, 8);
+        char out[65];
+        for (int i = 0; i < 8; ++i) snprintf(out + 8 * i, 9, "%08x", h[i]);
+        return std::string(out, 64);
+    }
+};
+}  // namespace
+
+// ---------------------------------------------------------------- model
+struct LayerW {
+    int16_t *attn_gamma, *ffn_gamma, *q_gamma, *k_gamma;
+    int8_t *w_qkv, *w_o, *w_gu, *w_d;
+    int32_t *m_qkv, *m_o, *m_gu, *m_d, *kvp;
+};
+
+struct GraphEntry {
+    cudaGraphExec_t exec = nullptr;
+    int32_t* seq_dev = nullptr;
+};
+
+struct detint_model {
+    int L, H, nq, nkv, d, F, V, max_pos, qk_norm, lg_grp;
+    long long eps_h, eps_qk;
+    int max_batch, max_ctx, mbs, nblocks, ctx_cap;
+    unsigned char* wblob = nullptr;
+    int8_t* embed;
+    int32_t* embed_m;
+    int16_t *final_gamma, *rope_cos, *rope_sin;
+    std::vector<LayerW> layers;
+    int8_t *kcache = nullptr, *vcache = nullptr;
+    size_t kv_layer_elems;
+    int32_t* block_table = nullptr;
+    int32_t* seq_len_dev = nullptr;
+    std::vector<int> seq_len;
+    // scratch for up to Tcap tokens
+    int Tcap = 0;
+    unsigned char* scratch = nullptr;
+    int32_t *h, *qkv, *o, *sbuf, *mt, *kt, *mq, *kq, *tok_seq, *tok_pos, *rows;
+    int8_t *x8, *q8;
+    int32_t *pval, *pidx, *logits_int;
+    int npart;
+    int32_t* status = nullptr;
+    int use_graph = 1;
+    std::map<std::string, GraphEntry> graphs;
+    int32_t* pinned = nullptr;       // host staging for small copies
+    size_t pinned_elems = 0;
+    cudaEvent_t pinned_done = nullptr;
+};
+
+// Copy host int32 arrays to device through pinned staging, asynchronously on
+// s; the staging area is reused only after the previous copies completed.
+static int stage_copies(detint_model* m, cudaStream_t s,
+                        const std::vector<std::pair<int32_t*, std::vector<int32_t>*>>& jobs) {
+    size_t total = 0;
+    for (auto& j : jobs) total += j.second->size();
+    if (m->pinned_done) CK(cudaEventSynchronize(m->pinned_done));
+    if (total > m->pinned_elems) {
+        if (m->pinned) cudaFreeHost(m->pinned);
+        m->pinned = nullptr;
+        size_t n = std::max(total, (size_t)4096);
+        CK(cudaMallocHost(&m->pinned, n * 4));
+        m->pinned_elems = n;
+    }
+    if (!m->pinned_done) CK(cudaEventCreateWithFlags(&m->pinned_done, cudaEventDisableTiming));
+    size_t off = 0;
+    for (auto& j : jobs) {
+        memcpy(m->pinned + off, j.second->data(), j.second->size() * 4);
+        CK(cudaMemcpyAsync(j.first, m->pinned + off, j.second->size() * 4, cudaMemcpyHostToDevice, s));
+        off += j.second->size();
+    }
+    CK(cudaEventRecord(m->pinned_done, s));
+    return DETINT_OK;
+}
+
+static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+static int ilog2i(int n) { int l = 0; while ((1 << l) < n) ++l; return l; }
+
+static void free_graphs(detint_model* m) {
+    for (auto& kv : m->graphs) {
+        if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+        if (kv.second.seq_dev) cudaFree(kv.second.seq_dev);
+    }
+    m->graphs.clear();
+}
+
+// (Re)allocate token scratch for T tokens; synchronises the device when it grows.
+static int ensure_scratch(detint_model* m, int T) {
+    if (T <= m->Tcap) return DETINT_OK;
+    int Tn = T < 64 ? 64 : T;
+    CK(cudaDeviceSynchronize());
+    free_graphs(m);
+    if (m->scratch) cudaFree(m->scratch);
+    m->scratch = nullptr;
+    const int nqkv = (m->nq + 2 * m->nkv) * m->d;
+    const int wmax = std::max(std::max(m->H, m->nq * m->d), m->F);
+    const int rows_out = m->max_batch;   // logits rows: one per sequence
+    m->npart = (m->V + 15) / 16;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = al256(off + bytes); return o; };
+    size_t o_h = take((size_t)Tn * m->H * 4), o_qkv = take((size_t)Tn * nqkv * 4),
+           o_o = take((size_t)Tn * m->nq * m->d * 4), o_s = take((size_t)Tn * m->F * 4),
+           o_mt = take((size_t)Tn * 4), o_kt = take((size_t)Tn * 4),
+           o_mq = take((size_t)Tn * m->nq * 4), o_kq = take((size_t)Tn * m->nq * 4),
+           o_ts = take((size_t)Tn * 4), o_tp = take((size_t)Tn * 4), o_rows = take((size_t)Tn * 4),
+           o_x8 = take((size_t)Tn * wmax), o_q8 = take((size_t)Tn * m->nq * m->d),
+           o_pv = take((size_t)rows_out * m->npart * 4), o_pi = take((size_t)rows_out * m->npart * 4),
+           o_lg = take((size_t)rows_out * m->V * 4);
+    cudaError_t e = cudaMalloc(&m->scratch, off);
+    if (e != cudaSuccess) { m->scratch = nullptr; m->Tcap = 0; return fail(DETINT_E_OOM, "scratch allocation failed"); }
+    unsigned char* b = m->scratch;
+    m->h = (int32_t*)(b + o_h); m->qkv = (int32_t*)(b + o_qkv); m->o = (int32_t*)(b + o_o);
+    m->sbuf = (int32_t*)(b + o_s); m->mt = (int32_t*)(b + o_mt); m->kt = (int32_t*)(b + o_kt);
+    m->mq = (int32_t*)(b + o_mq); m->kq = (int32_t*)(b + o_kq); m->tok_seq = (int32_t*)(b + o_ts);
+    m->tok_pos = (int32_t*)(b + o_tp); m->rows = (int32_t*)(b + o_rows);
+    m->x8 = (int8_t*)(b + o_x8); m->q8 = (int8_t*)(b + o_q8);
+    m->pval = (int32_t*)(b + o_pv); m->pidx = (int32_t*)(b + o_pi); m->logits_int = (int32_t*)(b + o_lg);
+    m->Tcap = Tn;
+    return DETINT_OK;
+}
+
+// GEMM of X[M][K] by W[N][K] with an epilogue; small M streams the weights
+// once per 32 tokens through the GEMV kernel, larger M uses the tiled GEMM.
+static cudaError_t gemm_epi(const int8_t* X, const int8_t* W, int M, int N, int K, int mode,
+                            const Epi& ep, cudaStream_t s) {
+    if (M <= 32) return launch_gemv(W, X, M, N, K, mode, ep, s);
+    return launch_gemm(X, W, M, N, K, mode, ep, s);
+}
+
+// The forward pass of T tokens whose (sequence, position) are in tok_seq /
+// tok_pos on the device (decode: positions are read from seq_len_dev by the
+// embedding kernel). Produces logits and argmax for the R rows listed in
+// m->rows (prefill) or for every token (decode, rows == nullptr).
+static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode, int R,
+                       const int32_t* rows, int32_t* logits, int32_t* next_tok, cudaStream_t s) {
+    const int H = m->H, d = m->d, nq = m->nq, nkv = m->nkv, F = m->F;
+    const int nqkv = (nq + 2 * nkv) * d;
+    CK(launch_embed(tokens, T, m->tok_seq, m->tok_pos, m->seq_len_dev, decode, m->max_ctx,
+                    m->embed, m->embed_m, H, m->V, m->h, m->status, s));
+    for (int l = 0; l < m->L; ++l) {
+        const LayerW& w = m->layers[l];
+        int8_t* kc = m->kcache + (size_t)l * m->kv_layer_elems;
+        int8_t* vc = m->vcache + (size_t)l * m->kv_layer_elems;
+        CK(launch_normquant(m->h, nullptr, T, H, w.attn_gamma, m->eps_h, m->x8, m->mt, m->kt, s));
+        Epi e{};
+        e.status = m->status;
+        e.mt = m->mt; e.kt = m->kt;
+        e.out = m->qkv; e.ldo = nqkv; e.mc = w.m_qkv; e.fout = 12;
+        CK(gemm_epi(m->x8, w.w_qkv, T, nqkv, H, EPI_QKV, e, s));
+        QkvPostArgs qa{};
+        qa.qkv = m->qkv; qa.q_gamma = w.q_gamma; qa.k_gamma = w.k_gamma; qa.qk_norm = m->qk_norm;
+        qa.eps_qk = m->eps_qk; qa.rope_cos = m->rope_cos; qa.rope_sin = m->rope_sin; qa.kvp = w.kvp;
+        qa.tok_seq = m->tok_seq; qa.tok_pos = m->tok_pos; qa.block_table = m->block_table;
+        qa.mbs = m->mbs; qa.q8 = m->q8; qa.mq = m->mq; qa.kq = m->kq; qa.kc = kc; qa.vc = vc;
+        qa.T = T; qa.nq = nq; qa.nkv = nkv; qa.d = d; qa.lg_grp = m->lg_grp;
+        CK(launch_qkv_post(qa, s));
+        AttnArgs aa{};
+        aa.q8 = m->q8; aa.mq = m->mq; aa.kq = m->kq; aa.kc = kc; aa.vc = vc;
+        aa.block_table = m->block_table; aa.mbs = m->mbs; aa.tok_seq = m->tok_seq;
+        aa.tok_pos = m->tok_pos; aa.kvp = w.kvp; aa.o = m->o; aa.T = T; aa.nq = nq; aa.nkv = nkv;
+        aa.d = d; aa.lg_grp = m->lg_grp; aa.ctx_cap = m->ctx_cap;
+        CK(launch_attention(aa, s));
+        CK(launch_actquant(m->o, T, nq * d, 12, m->x8, m->mt, m->kt, s));
+        e.out = m->h; e.ldo = H; e.mc = w.m_o; e.fout = 16;
+        CK(gemm_epi(m->x8, w.w_o, T, H, nq * d, EPI_RESADD, e, s));
+        CK(launch_normquant(m->h, nullptr, T, H, w.ffn_gamma, m->eps_h, m->x8, m->mt, m->kt, s));
+        e.out = m->sbuf; e.ldo = F; e.mc = w.m_gu; e.fout = 12;
+        CK(gemm_epi(m->x8, w.w_gu, T, 2 * F, H, EPI_SWIGLU, e, s));
+        CK(launch_actquant(m->sbuf, T, F, 10, m->x8, m->mt, m->kt, s));
+        e.out = m->h; e.ldo = H; e.mc = w.m_d; e.fout = 16;
+        CK(gemm_epi(m->x8, w.w_d, T, H, F, EPI_RESADD, e, s));
+    }
+    CK(launch_normquant(m->h, rows, R, H, m->final_gamma, m->eps_h, m->x8, m->mt, m->kt, s));
+    Epi e{};
+    e.status = m->status; e.mt = m->mt; e.kt = m->kt;
+    e.out = logits ? logits : m->logits_int; e.ldo = m->V; e.mc = m->embed_m; e.fout = 16;
+    e.pval = m->pval; e.pidx = m->pidx; e.npart = m->npart;
+    CK(gemm_epi(m->x8, m->embed, R, m->V, H, EPI_LOGITS, e, s));
+    CK(launch_argmax_final(m->pval, m->pidx, R, m->npart, next_tok, m->tok_seq,
+                           decode ? m->seq_len_dev : nullptr, s));
+    return DETINT_OK;
+}
+
+// ------------------------------------------------------------------ ABI
+extern "C" {
+
+const char* detint_strerror(int code) {
+    switch (code) {
+        case DETINT_OK: return "ok";
+        case DETINT_E_ARG: return "invalid argument";
+        case DETINT_E_SHAPE: return "unsupported shape";
+        case DETINT_E_TOKEN: return "token id outside the vocabulary";
+        case DETINT_E_CTX: return "context capacity exceeded";
+        case DETINT_E_ARTIFACT: return "unreadable or malformed artifact";
+        case DETINT_E_SHA: return "artifact sha256 mismatch";
+        case DETINT_E_CUDA: return "CUDA error";
+        case DETINT_E_OOM: return "device out of memory";
+        case DETINT_E_SEQ: return "bad sequence id";
+        case DETINT_E_SAT: return "saturation recorded";
+    }
+    return "unknown error";
+}
+
+const char* detint_last_error(void) { return g_last_error.c_str(); }
+
+void detint_free(detint_model* m) {
+    if (!m) return;
+    cudaDeviceSynchronize();
+    free_graphs(m);
+    if (m->scratch) cudaFree(m->scratch);
+    if (m->wblob) cudaFree(m->wblob);
+    if (m->kcache) cudaFree(m->kcache);
+    if (m->vcache) cudaFree(m->vcache);
+    if (m->block_table) cudaFree(m->block_table);
+    if (m->seq_len_dev) cudaFree(m->seq_len_dev);
+    if (m->status) cudaFree(m->status);
+    if (m->pinned) cudaFreeHost(m->pinned);
+    if (m->pinned_done) cudaEventDestroy(m->pinned_done);
+    delete m;
+}
+
+static int rd32(const unsigned char* p) { int32_t v; memcpy(&v, p, 4); return v; }
+
+int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t stream,
+                detint_model** out) {
+    if (!path || !out || max_batch < 1 || max_ctx < 1) return fail(DETINT_E_ARG, "detint_load: bad arguments");
+    *out = nullptr;
+    (void)stream;
+    FILE* f = fopen(path, "rb");
+    if (!f) return fail(DETINT_E_ARTIFACT, std::string("cannot open ") + path);
+    fseek(f, 0, SEEK_END);
+    long sz = ftell(f);
+    fseek(f, 0, SEEK_SET);
+    if (sz < 256) { fclose(f); return fail(DETINT_E_ARTIFACT, "artifact too small"); }
+    std::vector<unsigned char> blob((size_t)sz);
+    size_t got = fread(blob.data(), 1, blob.size(), f);
+    fclose(f);
+    if (got != blob.size()) return fail(DETINT_E_ARTIFACT, "short read");
+    // SHA-256 against the sidecar
+    std::string want;
+    {
+        FILE* g = fopen((std::string(path) + ".sha256").c_str(), "rb");
+        if (!g) return fail(DETINT_E_SHA, "missing .sha256 sidecar");
+        char buf[80] = {0};
+        size_t n = fread(buf, 1, 64, g);
+        fclose(g);
+        want.assign(buf, n);
+    }
+    Sha256 sh;
+    sh.update(blob.data(), blob.size());
+    if (sh.hex() != want) return fail(DETINT_E_SHA, "artifact sha256 mismatch");
+    const unsigned char* hd = blob.data();
+    if (memcmp(hd, "DETINT01", 8) != 0 || rd32(hd + 8) != 1) return fail(DETINT_E_ARTIFACT, "bad magic/version");
+    detint_model* m = new detint_model();
+    m->L = rd32(hd + 12); m->H = rd32(hd + 16); m->nq = rd32(hd + 20); m->nkv = rd32(hd + 24);
+    m->d = rd32(hd + 28); m->F = rd32(hd + 32); m->V = rd32(hd + 36); m->max_pos = rd32(hd + 40);
+    m->qk_norm = rd32(hd + 44); m->eps_h = rd32(hd + 48); m->eps_qk = rd32(hd + 52);
+    const int H = m->H, d = m->d, F = m->F, V = m->V, nq = m->nq, nkv = m->nkv;
+    auto bad_shape = [&](const char* why) { delete m; return fail(DETINT_E_SHAPE, why); };
+    if (m->L < 1 || H < 64 || (H & (H - 1)) || (d != 64 && d != 128) || nkv < 1 || nq % nkv)
+        return bad_shape("unsupported model shape");
+    const int grp = nq / nkv;
+    if (grp & (grp - 1) || grp > 8) return bad_shape("q heads per kv head must be a power of two <= 8");
+    if ((F & 63) || ((nq * d) & 63) || V < 1) return bad_shape("unsupported model shape");
+    if (max_ctx > m->max_pos) return bad_shape("max_ctx exceeds the RoPE table length");
+    m->lg_grp = ilog2i(grp);
+    m->max_batch = max_batch;
+    m->max_ctx = max_ctx;
+    m->mbs = (max_ctx + KV_BLK - 1) / KV_BLK;
+    m->ctx_cap = m->mbs * KV_BLK;
+    m->nblocks = m->mbs * max_batch;
+    if (attention_smem_bytes(grp, d, m->ctx_cap) > 220 * 1024) return bad_shape("max_ctx too large for the attention row");
+    // section walk (256-byte aligned, file order)
+    const int nqkv = (nq + 2 * nkv) * d;
+    size_t cur = 256;
+    bool ok = true;
+    auto take = [&](size_t bytes) -> const unsigned char* {
+        cur = (cur + 255) & ~(size_t)255;
+        if (cur + bytes > blob.size()) { ok = false; return blob.data(); }
+        const unsigned char* p = blob.data() + cur;
+        cur += bytes;
+        return p;
+    };
+    // device weight blob layout (same order, gate/up interleaved)
+    size_t dsz = 0;
+    auto dtake = [&](size_t bytes) { size_t o = dsz; dsz = al256(dsz + bytes); return o; };
+    struct Sec { const unsigned char* src; size_t bytes; size_t doff; int kind; };
+    std::vector<Sec> secs;
+    auto add = [&](size_t bytes, int kind = 0) {
+        const unsigned char* p = take(bytes);
+        secs.push_back({p, bytes, dtake(bytes), kind});
+        return secs.size() - 1;
+    };
+    size_t s_embed = add((size_t)V * H), s_em = add((size_t)V * 4), s_fg = add((size_t)H * 2),
+           s_rc = add((size_t)m->max_pos * (d / 2) * 2), s_rs = add((size_t)m->max_pos * (d / 2) * 2);
+    struct LS { size_t ag, fg, qg, kg, wqkv, mqkv, wo, mo, wg, mg, wu, mu, wd, md, kvp, wgu, mgu; };
+    std::vector<LS> ls(m->L);
+    for (int l = 0; l < m->L; ++l) {
+        LS& x = ls[l];
+        x.ag = add((size_t)H * 2); x.fg = add((size_t)H * 2); x.qg = add((size_t)d * 2);
+        x.kg = add((size_t)d * 2); x.wqkv = add((size_t)nqkv * H); x.mqkv = add((size_t)nqkv * 4);
+        x.wo = add((size_t)H * nq * d); x.mo = add((size_t)H * 4);
+        x.wg = secs.size(); secs.push_back({take((size_t)F * H), (size_t)F * H, 0, 1});
+        x.mg = secs.size(); secs.push_back({take((size_t)F * 4), (size_t)F * 4, 0, 1});
+        x.wu = secs.size(); secs.push_back({take((size_t)F * H), (size_t)F * H, 0, 1});
+        x.mu = secs.size(); secs.push_back({take((size_t)F * 4), (size_t)F * 4, 0, 1});
+        x.wgu = dtake((size_t)2 * F * H);
+        x.mgu = dtake((size_t)2 * F * 4);
+        x.wd = add((size_t)H * F); x.md = add((size_t)H * 4);
+        x.kvp = add((size_t)nkv * (8 + d / 2) * 4);
+    }
+    if (!ok) { delete m; return fail(DETINT_E_ARTIFACT, "artifact truncated"); }
+    cudaError_t ce = cudaMalloc(&m->wblob, dsz);
+    if (ce != cudaSuccess) { m->wblob = nullptr; detint_free(m); return fail(DETINT_E_OOM, "weight allocation failed"); }
+    for (const Sec& sc : secs)
+        if (sc.kind == 0) {
+            ce = cudaMemcpy(m->wblob + sc.doff, sc.src, sc.bytes, cudaMemcpyHostToDevice);
+            if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
+        }
+    // gate/up interleaved as rows (gate_i, up_i) so one CTA holds both of a channel
+    std::vector<int8_t> gu((size_t)2 * F * H);
+    std::vector<int32_t> mgu((size_t)2 * F);
+    m->layers.resize(m->L);
+    for (int l = 0; l < m->L; ++l) {
+        const LS& x = ls[l];
+        const int8_t* wg = (const int8_t*)secs[x.wg].src;
+        const int8_t* wu = (const int8_t*)secs[x.wu].src;
+        const int32_t* mg = (const int32_t*)secs[x.mg].src;
+        const int32_t* mu = (const int32_t*)secs[x.mu].src;
+        for (int i = 0; i < F; ++i) {
+            memcpy(&gu[(size_t)(2 * i) * H], wg + (size_t)i * H, H);
+            memcpy(&gu[(size_t)(2 * i + 1) * H], wu + (size_t)i * H, H);
+            int32_t a, b;
+            memcpy(&a, mg + i, 4); memcpy(&b, mu + i, 4);
+            mgu[2 * i] = a; mgu[2 * i + 1] = b;
+        }
+        ce = cudaMemcpy(m->wblob + x.wgu, gu.data(), gu.size(), cudaMemcpyHostToDevice);
+        if (ce == cudaSuccess) ce = cudaMemcpy(m->wblob + x.mgu, mgu.data(), mgu.size() * 4, cudaMemcpyHostToDevice);
+        if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
+        LayerW& w = m->layers[l];
+        auto P = [&](size_t si) { return m->wblob + secs[si].doff; };
+        w.attn_gamma = (int16_t*)P(x.ag); w.ffn_gamma = (int16_t*)P(x.fg);
+        w.q_gamma = (int16_t*)P(x.qg); w.k_gamma = (int16_t*)P(x.kg);
+        w.w_qkv = (int8_t*)P(x.wqkv); w.m_qkv = (int32_t*)P(x.mqkv);
+        w.w_o = (int8_t*)P(x.wo); w.m_o = (int32_t*)P(x.mo);
+        w.w_gu = (int8_t*)(m->wblob + x.wgu); w.m_gu = (int32_t*)(m->wblob + x.mgu);
+        w.w_d = (int8_t*)P(x.wd); w.m_d = (int32_t*)P(x.md);
+        w.kvp = (int32_t*)P(x.kvp);
+    }
+    m->embed = (int8_t*)(m->wblob + secs[s_embed].doff);
+    m->embed_m = (int32_t*)(m->wblob + secs[s_em].doff);
+    m->final_gamma = (int16_t*)(m->wblob + secs[s_fg].doff);
+    m->rope_cos = (int16_t*)(m->wblob + secs[s_rc].doff);
+    m->rope_sin = (int16_t*)(m->wblob + secs[s_rs].doff);
+    // paged int8 KV cache: K [L][NB][nkv][64][d], V [L][NB][nkv][d][64]
+    m->kv_layer_elems = (size_t)m->nblocks * nkv * KV_BLK * d;
+    if (cudaMalloc(&m->kcache, m->kv_layer_elems * m->L) != cudaSuccess ||
+        cudaMalloc(&m->vcache, m->kv_layer_elems * m->L) != cudaSuccess) {
+        detint_free(m);
+        return fail(DETINT_E_OOM, "KV cache allocation failed");
+    }
+    std::vector<int32_t> bt((size_t)max_batch * m->mbs);
+    for (size_t i = 0; i < bt.size(); ++i) bt[i] = (int32_t)i;   // sequence s owns blocks [s*mbs, (s+1)*mbs)
+    if (cudaMalloc(&m->block_table, bt.size() * 4) != cudaSuccess ||
+        cudaMalloc(&m->seq_len_dev, (size_t)max_batch * 4) != cudaSuccess ||
+        cudaMalloc(&m->status, ST_N * 4) != cudaSuccess) {
+        detint_free(m);
+        return fail(DETINT_E_OOM, "allocation failed");
+    }
+    ce = cudaMemcpy(m->block_table, bt.data(), bt.size() * 4, cudaMemcpyHostToDevice);
+    if (ce == cudaSuccess) ce = cudaMemset(m->seq_len_dev, 0, (size_t)max_batch * 4);
+    if (ce == cudaSuccess) ce = cudaMemset(m->status, 0, ST_N * 4);
+    if (ce == cudaSuccess) ce = cudaMemset(m->kcache, 0, m->kv_layer_elems * m->L);
+    if (ce == cudaSuccess) ce = cudaMemset(m->vcache, 0, m->kv_layer_elems * m->L);
+    if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
+    m->seq_len.assign(max_batch, 0);
+    int rc = ensure_scratch(m, std::max(64, max_batch));
+    if (rc != DETINT_OK) { detint_free(m); return rc; }
+    ce = kernels_init();
+    if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
+    ce = cudaDeviceSynchronize();
+    if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
+    *out = m;
+    return DETINT_OK;
+}
+
+static int check_seqs(detint_model* m, int n_seq, const int32_t* seq_ids) {
+    if (n_seq < 1 || !seq_ids) return fail(DETINT_E_ARG, "no sequences");
+    std::vector<char> seen(m->max_batch, 0);
+    for (int i = 0; i < n_seq; ++i) {
+        const int s = seq_ids[i];
+        if (s < 0 || s >= m->max_batch || seen[s]) return fail(DETINT_E_SEQ, "sequence id out of range or repeated");
+        seen[s] = 1;
+    }
+    return DETINT_OK;
+}
+
+int detint_prefill(detint_model* m, int n_seq, const int32_t* seq_ids, const int32_t* cu_lens,
+                   const int32_t* tokens, int32_t* logits, int32_t* next_tok, detint_stream_t sp) {
+    if (!m || !cu_lens || !tokens || !next_tok) return fail(DETINT_E_ARG, "detint_prefill: null pointer");
+    int rc = check_seqs(m, n_seq, seq_ids);
+    if (rc) return rc;
+    if (cu_lens[0] != 0) return fail(DETINT_E_ARG, "cu_lens[0] must be 0");
+    for (int i = 0; i < n_seq; ++i) {
+        const int len = cu_lens[i + 1] - cu_lens[i];
+        if (len < 1) return fail(DETINT_E_ARG, "empty prompt");
+        if (m->seq_len[seq_ids[i]] + len > m->max_ctx) return fail(DETINT_E_CTX, "prompt exceeds max_ctx");
+    }
+    const int T = cu_lens[n_seq];
+    cudaStream_t s = (cudaStream_t)sp;
+    rc = ensure_scratch(m, std::max(T, n_seq));
+    if (rc) return rc;
+    std::vector<int32_t> ts(T), tp(T), rows(n_seq);
+    for (int i = 0; i < n_seq; ++i) {
+        const int sid = seq_ids[i];
+        for (int j = cu_lens[i]; j < cu_lens[i + 1]; ++j) {
+            ts[j] = sid;
+            tp[j] = m->seq_len[sid] + (j - cu_lens[i]);
+        }
+        rows[i] = cu_lens[i + 1] - 1;
+    }
+    std::vector<int32_t> newlen(m->seq_len.begin(), m->seq_len.end());
+    for (int i = 0; i < n_seq; ++i) newlen[seq_ids[i]] += cu_lens[i + 1] - cu_lens[i];
+    rc = stage_copies(m, s, {{m->tok_seq, &ts}, {m->tok_pos, &tp}, {m->rows, &rows}});
+    if (rc) return rc;
+    rc = run_forward(m, T, tokens, 0, n_seq, m->rows, logits, next_tok, s);
+    if (rc) return rc;
+    rc = stage_copies(m, s, {{m->seq_len_dev, &newlen}});
+    if (rc) return rc;
+    for (int i = 0; i < m->max_batch; ++i) m->seq_len[i] = newlen[i];
+    return DETINT_OK;
+}
+
+int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const int32_t* tok,
+                       int32_t* logits, int32_t* next_tok, detint_stream_t sp) {
+    if (!m || !tok || !next_tok) return fail(DETINT_E_ARG, "detint_decode_step: null pointer");
+    int rc = check_seqs(m, n_seq, seq_ids);
+    if (rc) return rc;
+    for (int i = 0; i < n_seq; ++i)
+        if (m->seq_len[seq_ids[i]] + 1 > m->max_ctx) return fail(DETINT_E_CTX, "decode exceeds max_ctx");
+    cudaStream_t s = (cudaStream_t)sp;
+    rc = ensure_scratch(m, n_seq);
+    if (rc) return rc;
+    const bool graph = m->use_graph && s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread;
+    if (!graph) {
+        std::vector<int32_t> ids(seq_ids, seq_ids + n_seq);
+        rc = stage_copies(m, s, {{m->tok_seq, &ids}});
+        if (rc) return rc;
+        rc = run_forward(m, n_seq, tok, 1, n_seq, nullptr, logits, next_tok, s);
+        if (rc) return rc;
+    } else {
+        char key[128];
+        snprintf(key, sizeof key, "%d|%p|%p|%p|", n_seq, (const void*)tok, (void*)logits, (void*)next_tok);
+        std::string k(key);
+        for (int i = 0; i < n_seq; ++i) k += std::to_string(seq_ids[i]) + ",";
+        auto it = m->graphs.find(k);
+        if (it == m->graphs.end()) {
+            GraphEntry ge;
+            CK(cudaMalloc(&ge.seq_dev, (size_t)n_seq * 4));
+            CK(cudaMemcpy(ge.seq_dev, seq_ids, (size_t)n_seq * 4, cudaMemcpyHostToDevice));
+            int32_t* saved = m->tok_seq;
+            m->tok_seq = ge.seq_dev;
+            cudaGraph_t gph;
+            CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+            rc = run_forward(m, n_seq, tok, 1, n_seq, nullptr, logits, next_tok, s);
+            cudaError_t ce = cudaStreamEndCapture(s, &gph);
+            m->tok_seq = saved;
+            if (rc) { cudaFree(ge.seq_dev); return rc; }
+            if (ce != cudaSuccess) { cudaFree(ge.seq_dev); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
+            ce = cudaGraphInstantiate(&ge.exec, gph, 0);
+            cudaGraphDestroy(gph);
+            if (ce != cudaSuccess) { cudaFree(ge.seq_dev); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
+            it = m->graphs.emplace(k, ge).first;
+        }
+        CK(cudaGraphLaunch(it->second.exec, s));
+    }
+    for (int i = 0; i < n_seq; ++i) m->seq_len[seq_ids[i]] += 1;
+    return DETINT_OK;
+}
+
+int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, int K,
+                   detint_stream_t sp) {
+    if (!A || !B || !C || M < 1 || N < 1 || K < 1) return fail(DETINT_E_ARG, "detint_gemm_i8: bad arguments");
+    if (K % 16) return fail(DETINT_E_SHAPE, "detint_gemm_i8: K must be a multiple of 16");
+    if (((uintptr_t)A & 15) || ((uintptr_t)B & 15)) return fail(DETINT_E_ARG, "detint_gemm_i8: A and B must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)sp;
+    Epi e{};
+    e.out = C; e.ldo = N;
+    if (M <= 32 && (K % 64) == 0) { CK(launch_gemv(B, A, M, N, K, EPI_RAW, e, s)); }
+    else { CK(launch_gemm(A, B, M, N, K, EPI_RAW, e, s)); }
+    return DETINT_OK;
+}
+
+int detint_reset_seq(detint_model* m, int seq_id) {
+    if (!m) return fail(DETINT_E_ARG, "null model");
+    if (seq_id < 0 || seq_id >= m->max_batch) return fail(DETINT_E_SEQ, "sequence id out of range");
+    CK(cudaDeviceSynchronize());
+    m->seq_len[seq_id] = 0;
+    const int32_t z = 0;
+    CK(cudaMemcpy(m->seq_len_dev + seq_id, &z, 4, cudaMemcpyHostToDevice));
+    return DETINT_OK;
+}
+
+int detint_seq_len(detint_model* m, int seq_id, int32_t* len) {
+    if (!m || !len) return fail(DETINT_E_ARG, "null pointer");
+    if (seq_id < 0 || seq_id >= m->max_batch) return fail(DETINT_E_SEQ, "sequence id out of range");
+    *len = m->seq_len[seq_id];
+    return DETINT_OK;
+}
+
+int detint_status(detint_model* m, int32_t* flags, detint_stream_t sp) {
+    if (!m) return fail(DETINT_E_ARG, "null model");
+    int32_t st[ST_N];
+    CK(cudaStreamSynchronize((cudaStream_t)sp));
+    CK(cudaMemcpy(st, m->status, sizeof st, cudaMemcpyDeviceToHost));
+    CK(cudaMemset(m->status, 0, sizeof st));
+    if (flags) memcpy(flags, st, sizeof st);
+    if (st[ST_TOKEN]) return DETINT_E_TOKEN;
+    if (st[ST_CTX]) return DETINT_E_CTX;
+    return DETINT_OK;
+}
+
+int detint_set_graph(detint_model* m, int enable) {
+    if (!m || (enable != 0 && enable != 1)) return fail(DETINT_E_ARG, "bad argument");
+    m->use_graph = enable;
+    return DETINT_OK;
+}
+
+int detint_model_info(detint_model* m, int32_t* info) {
+    if (!m || !info) return fail(DETINT_E_ARG, "null pointer");
+    int32_t v[11] = {m->L, m->H, m->nq, m->nkv, m->d, m->F, m->V, m->max_pos, m->qk_norm,
+                     m->max_batch, m->max_ctx};
+    memcpy(info, v, sizeof v);
+    return DETINT_OK;
+}
+
+}  // extern "C"

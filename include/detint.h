@@ -1,0 +1,128 @@
+/*
+ * detint — C ABI of the GB300 (sm_103a) integer-only LLM decoder.
+ *
+ * The library runs the integer-only decoder forward pass of a Qwen3- or
+ * Llama-shaped model: every operation from input ids to int32 logits is
+ * exact integer arithmetic, so logits and greedy tokens are bit-identical
+ * across batch composition, prefill vs decode and backends ("DetLLM — Fully
+ * Deterministic LLM Inference", intro; DetLLM blog "Eliminating
+ * Nondeterminism in LLM Inference with Integer-Only Arithmetic", section
+ * "DetLLM"). The user-level API of the pages is
+ * `IntQwen3(path, backend).generate(ids, max_new, use_graph)` (README,
+ * "Usage"); its C counterpart is detint_load + detint_prefill +
+ * detint_decode_step.
+ *
+ * Conventions
+ *  - Streams are `cudaStream_t` values passed as `detint_stream_t`. All
+ *    compute calls are stream-ordered and asynchronous; they return after
+ *    enqueueing work. The legacy default stream (NULL) is accepted but CUDA
+ *    graphs are only used on a non-default stream.
+ *  - Device pointers are owned by the caller unless stated. The model owns
+ *    its weights, KV cache and scratch, released by detint_free.
+ *  - Every call returns 0 (DETINT_OK) or a positive DETINT_E_* code; nothing
+ *    aborts. detint_strerror names a code; detint_last_error gives the
+ *    detail of the last failure in this process.
+ *  - Conditions only the device can see (a token id >= vocab, a saturated
+ *    residual/logit) are recorded in a status word read by detint_status.
+ */
+#ifndef DETINT_H
+#define DETINT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct detint_model detint_model;
+typedef struct CUstream_st* detint_stream_t;   /* == cudaStream_t */
+
+enum {
+    DETINT_OK = 0,
+    DETINT_E_ARG = 1,       /* null pointer, bad count or option */
+    DETINT_E_SHAPE = 2,     /* unsupported sizes (e.g. K not a multiple of 16) */
+    DETINT_E_TOKEN = 3,     /* status: a token id outside [0, vocab) */
+    DETINT_E_CTX = 4,       /* a sequence would exceed max_ctx */
+    DETINT_E_ARTIFACT = 5,  /* unreadable or malformed artifact file */
+    DETINT_E_SHA = 6,       /* artifact SHA-256 differs from its .sha256 file */
+    DETINT_E_CUDA = 7,      /* a CUDA call failed */
+    DETINT_E_OOM = 8,       /* device allocation failed */
+    DETINT_E_SEQ = 9,       /* sequence id outside [0, max_batch) or repeated */
+    DETINT_E_SAT = 10       /* status: a saturation was recorded */
+};
+
+/* Load an artifact (format: the artifact section of the arithmetic
+ * specification; header, int8 weights, dyadic channel scales, int16 gammas,
+ * int16 Q14 RoPE tables, per-kv-head fixed K/V scales) after checking its
+ * SHA-256 against `<path>.sha256` (README, "Demo": comparisons are valid only
+ * for the same artifact hash). Allocates the weights, a paged int8 KV cache
+ * for `max_batch` sequences of up to `max_ctx` positions, and scratch.
+ * `max_ctx` <= the artifact's RoPE table length. Synchronous.
+ * Errors: ARG, ARTIFACT, SHA, OOM, CUDA, SHAPE. */
+int detint_load(const char* artifact_path, int max_batch, int max_ctx, detint_stream_t s,
+                detint_model** out);
+
+/* Prefill: append a ragged batch of prompts to the KV caches of `n_seq`
+ * distinct sequences and return the logits of each sequence's last new
+ * position (DetLLM blog, "DetLLM": prefill and decode see the same cached
+ * bits). seq_ids: host int32[n_seq], each in [0, max_batch), distinct.
+ * cu_lens: host int32[n_seq + 1], cu_lens[0] = 0, non-decreasing, each
+ * length >= 1; tokens of sequence i are tokens[cu_lens[i] .. cu_lens[i+1]).
+ * tokens: device int32[cu_lens[n_seq]]. logits: device int32[n_seq][vocab]
+ * or NULL. next_tok: device int32[n_seq] (argmax, ties to the lowest id).
+ * Positions continue from each sequence's current length, so a prompt may
+ * be split across calls (split prefill) with identical results.
+ * Errors: ARG, SEQ, CTX, CUDA, OOM. */
+int detint_prefill(detint_model* m, int n_seq, const int32_t* seq_ids, const int32_t* cu_lens,
+                   const int32_t* tokens, int32_t* logits, int32_t* next_tok, detint_stream_t s);
+
+/* One greedy decode step: one new token per sequence. seq_ids: host
+ * int32[n_seq]; tok: device int32[n_seq]; logits: device int32[n_seq][vocab]
+ * or NULL; next_tok: device int32[n_seq] (may alias tok). With graphs
+ * enabled (default) the step is one CUDA-graph launch, re-captured when the
+ * sequence set or a pointer changes. Errors: ARG, SEQ, CTX, CUDA. */
+int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const int32_t* tok,
+                       int32_t* logits, int32_t* next_tok, detint_stream_t s);
+
+/* Exact int8 x int8 -> int32 GEMM: C[m][n] = sum_k A[m][k] * B[n][k].
+ * A: device int8 [M][K] row-major; B: device int8 [N][K] row-major (the
+ * weight layout); C: device int32 [M][N]. M, N >= 1; K >= 16 and a multiple
+ * of 16; A, B 16-byte aligned. The integer GEMM is the one operation the
+ * pages dispatch per device (README, "Layout": int_gemm). Errors: ARG,
+ * SHAPE, CUDA. */
+int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, int K,
+                   detint_stream_t s);
+
+/* Forget a sequence's cached context (length back to 0). Synchronises the
+ * device first. Errors: ARG, SEQ, CUDA. */
+int detint_reset_seq(detint_model* m, int seq_id);
+
+/* Current length of a sequence (host-side bookkeeping). */
+int detint_seq_len(detint_model* m, int seq_id, int32_t* len);
+
+/* Read and clear the device status word after synchronising `s`.
+ * flags: host int32[8] or NULL; slots 0 token id out of range, 1 context
+ * clamp, 2 residual saturation, 3 gate/up saturation, 4 logit saturation,
+ * 5 q/k/v saturation. Returns DETINT_E_TOKEN if slot 0 is set, else
+ * DETINT_E_CTX if slot 1 is set, else DETINT_OK. */
+int detint_status(detint_model* m, int32_t* flags, detint_stream_t s);
+
+/* Enable (1, default) or disable (0) CUDA-graph replay of decode steps
+ * (README, "Usage": use_graph). */
+int detint_set_graph(detint_model* m, int enable);
+
+/* Shape of the loaded model: info[0..9] = n_layers, hidden, n_q, n_kv,
+ * head_dim, ffn, vocab, max_pos, qk_norm, max_batch; info[10] = max_ctx. */
+int detint_model_info(detint_model* m, int32_t* info);
+
+/* Release everything the model owns. NULL is a no-op. */
+void detint_free(detint_model* m);
+
+const char* detint_strerror(int code);
+const char* detint_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DETINT_H */

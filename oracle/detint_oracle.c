@@ -567,7 +567,10 @@ static void forward_token(or_model* m, or_seq* s, int32_t tok, int32_t* logits, 
             int E = 0;
             for (int i = 0; i < half; i++) if (kvp[8 + i] > E) E = kvp[8 + i];
             if (m->qk_norm) or_qknorm(qkv + hq * d, d, ly->q_gamma, m->eps_qk, y);
-            else for (int i = 0; i < d; i++) y[i] = qkv[hq * d + i] * 4;
+            else for (int i = 0; i < d; i++) {
+                CHECK(qkv[hq * d + i] < (1 << 29) && qkv[hq * d + i] > -(1 << 29));
+                y[i] = qkv[hq * d + i] * 4;
+            }
             or_rope(y, d, cr, sr);
             for (int c = 0; c < d; c++) {
                 i64 v = (i64)y[c] * P2(E - kvp[8 + (c % half)]);
@@ -583,7 +586,10 @@ static void forward_token(or_model* m, or_seq* s, int32_t tok, int32_t* logits, 
             int8_t* Kd = s->K + (((size_t)l * nkv + g2) * s->max_ctx + pos) * d;
             int8_t* Vd = s->V + (((size_t)l * nkv + g2) * s->max_ctx + pos) * d;
             if (m->qk_norm) or_qknorm(kin, d, ly->k_gamma, m->eps_qk, y);
-            else for (int i = 0; i < d; i++) y[i] = kin[i] * 4;
+            else for (int i = 0; i < d; i++) {
+                CHECK(kin[i] < (1 << 29) && kin[i] > -(1 << 29));
+                y[i] = kin[i] * 4;
+            }
             or_rope(y, d, cr, sr);
             for (int c = 0; c < d; c++) {
                 i64 v = (i64)y[c] * P2(kvp[8 + (c % half)]);

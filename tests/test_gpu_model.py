@@ -1,0 +1,156 @@
+"""GPU parity of the whole integer forward pass against the CPU oracle at
+tolerance 0 (logits of every step, tokens, chain hashes), plus the pages'
+invariances on the GPU itself: batch composition, split prefill, graph vs no
+graph, repeats (DetLLM README, "Demo"; DetLLM blog footnote on the
+zero-tolerance suite)."""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import deterministic_integer_only_gb300 as pkg
+    pkg.lib()
+    return torch
+
+
+def _oracle_run(path, prompt, steps, max_ctx):
+    import oracle
+    m = oracle.Model(path)
+    s = m.new_seq(max_ctx)
+    am, lg = s.feed(prompt)
+    toks, rows = [am], [lg]
+    for _ in range(steps - 1):
+        am, lg = s.feed([toks[-1]])
+        toks.append(am)
+        rows.append(lg)
+    return np.array(toks, np.int32), rows
+
+
+def _load(path, max_batch, max_ctx):
+    import deterministic_integer_only_gb300 as pkg
+    return pkg.Model(path, max_batch=max_batch, max_ctx=max_ctx)
+
+
+def test_tiny_matches_oracle_every_step(torch_cuda, tiny_artifact):
+    prompt = synth.prompt_ids(0, 0, 16, 1024)
+    ot, orows = _oracle_run(tiny_artifact, prompt, 16, 64)
+    for graph in (True, False):
+        m = _load(tiny_artifact, 2, 64)
+        m.set_graph(graph)
+        toks, rows = m.generate([prompt], 16)
+        assert np.array_equal(toks[0], ot)
+        for s in range(16):
+            assert np.array_equal(rows[s][0], orows[s]), f"step {s} graph={graph}"
+        assert not m.status().any()
+        m.close()
+
+
+def test_tiny_golden_hash(torch_cuda, tiny_artifact):
+    import json
+    import os
+    import deterministic_integer_only_gb300 as pkg
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "oracle_tiny_seed0.json")))
+    prompt = synth.prompt_ids(g["seed"], 0, g["prompt_len"], 1024)
+    m = _load(tiny_artifact, 1, 64)
+    toks, rows = m.generate([prompt], g["steps"])
+    assert toks[0].tolist() == g["tokens"]
+    assert pkg.chain_hash([r[0] for r in rows]).hex()[:12] == g["logits_hash12"]
+
+
+def test_tiny_batch_composition_and_split_prefill(torch_cuda, tiny_artifact):
+    prompt = synth.prompt_ids(0, 0, 16, 1024)
+    ot, orows = _oracle_run(tiny_artifact, prompt, 12, 128)
+    lens = synth.coprompt_lengths(0, 7, 16, 100)
+    cos = [synth.prompt_ids(0, 100 + i, int(n), 1024) for i, n in enumerate(lens)]
+    m = _load(tiny_artifact, 8, 128)
+    toks, rows = m.generate([prompt] + cos, 12)
+    assert np.array_equal(toks[0], ot)
+    for s in range(12):
+        assert np.array_equal(rows[s][0], orows[s])
+    # a co-prompt row matches the oracle too
+    ot3, orows3 = _oracle_run(tiny_artifact, cos[3], 12, 128)
+    assert np.array_equal(toks[4], ot3)
+    assert all(np.array_equal(rows[s][4], orows3[s]) for s in range(12))
+    m.close()
+    # split prefill: 7 tokens at once, the rest one by one, then decode
+    torch = torch_cuda
+    m = _load(tiny_artifact, 1, 128)
+    dev = torch.device("cuda")
+    lg = torch.empty((1, 1024), dtype=torch.int32, device=dev)
+    tok = torch.empty(1, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(m.stream):
+        m.prefill([0], torch.tensor(prompt[:7], device=dev), [0, 7], lg, tok)
+        for t in prompt[7:]:
+            m.decode_step([0], torch.tensor([t], dtype=torch.int32, device=dev), lg, tok)
+        out = [int(tok.item())]
+        rows2 = [lg.cpu().numpy()[0]]
+        for _ in range(11):
+            m.decode_step([0], tok, lg, tok)
+            out.append(int(tok.item()))
+            rows2.append(lg.cpu().numpy()[0])
+    assert out == ot.tolist()
+    assert all(np.array_equal(a, b) for a, b in zip(rows2, orows))
+    m.close()
+
+
+def test_tiny_repeats_and_reset(torch_cuda, tiny_artifact):
+    prompt = synth.prompt_ids(0, 5, 20, 1024)
+    m = _load(tiny_artifact, 1, 64)
+    ref = None
+    for _ in range(3):
+        toks, rows = m.generate([prompt], 8, keep_logits="hash")
+        if ref is None:
+            ref = (toks, rows)
+        assert np.array_equal(toks, ref[0]) and rows == ref[1]
+        m.reset_seq(0)
+    m.close()
+
+
+def test_bad_inputs_are_reported(torch_cuda, tiny_artifact):
+    import deterministic_integer_only_gb300 as pkg
+    torch = torch_cuda
+    m = _load(tiny_artifact, 2, 32)
+    dev = torch.device("cuda")
+    with pytest.raises(pkg.DetintError) as e:
+        m.prefill([5], torch.zeros(4, dtype=torch.int32, device=dev), [0, 4])
+    assert e.value.code == 9
+    with pytest.raises(pkg.DetintError) as e:
+        m.prefill([0], torch.zeros(40, dtype=torch.int32, device=dev), [0, 40])
+    assert e.value.code == 4
+    with torch.cuda.stream(m.stream):
+        m.prefill([1], torch.tensor([3, 2000, 7], dtype=torch.int32, device=dev), [0, 3])
+    flags = m.status()
+    assert flags[0] == 1
+    m.close()
+
+
+def test_qwen_shape_matches_oracle(torch_cuda, qwen_artifact):
+    prompt = synth.prompt_ids(0, 0, 64, 151936)
+    ot, orows = _oracle_run(qwen_artifact, prompt, 6, 128)
+    m = _load(qwen_artifact, 8, 1024)
+    toks, rows = m.generate([prompt], 6)
+    assert np.array_equal(toks[0], ot)
+    for s in range(6):
+        assert np.array_equal(rows[s][0], orows[s]), f"step {s}"
+    assert not m.status().any()
+    m.close()
+
+
+def test_qwen_batch8_row0_equals_batch1(torch_cuda, qwen_artifact):
+    prompt = synth.prompt_ids(0, 0, 64, 151936)
+    lens = synth.coprompt_lengths(0, 7)
+    cos = [synth.prompt_ids(0, 100 + i, int(n), 151936) for i, n in enumerate(lens)]
+    m = _load(qwen_artifact, 8, 1024)
+    t1, h1 = m.generate([prompt], 24, keep_logits="hash")
+    m.reset_seq(0)
+    t8, h8 = m.generate([prompt] + cos, 24, keep_logits="hash")
+    assert np.array_equal(t8[0], t1[0]) and h8[0] == h1[0]
+    m.close()
