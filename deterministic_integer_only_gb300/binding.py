@@ -25,6 +25,7 @@ ERRORS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "token id o
 # every entry point of include/detint.h
 SYMBOLS = ["detint_load", "detint_prefill", "detint_decode_step", "detint_gemm_i8",
            "detint_reset_seq", "detint_seq_len", "detint_status", "detint_set_graph",
+           "detint_set_option",
            "detint_model_info", "detint_free", "detint_strerror", "detint_last_error"]
 
 
@@ -52,6 +53,7 @@ def lib():
         L.detint_seq_len.argtypes = [vp, C.c_int, i32p]
         L.detint_status.argtypes = [vp, i32p, vp]
         L.detint_set_graph.argtypes = [vp, C.c_int]
+        L.detint_set_option.argtypes = [vp, C.c_int, C.c_int]
         L.detint_model_info.argtypes = [vp, i32p]
         L.detint_free.argtypes = [vp]
         L.detint_free.restype = None
@@ -130,6 +132,9 @@ class Model:
 
     def set_graph(self, enable: bool):
         _check(lib().detint_set_graph(self._h, int(bool(enable))), "detint_set_graph")
+
+    def set_fused_decode(self, enable: bool):
+        _check(lib().detint_set_option(self._h, 1, int(bool(enable))), "detint_set_option")
 
     def reset_seq(self, seq_id: int):
         _check(lib().detint_reset_seq(self._h, int(seq_id)), "detint_reset_seq")

@@ -117,4 +117,64 @@ __device__ __forceinline__ int swiglu_dev(int g, int u) {
     return sat32(rshr(silu * (i64)u, 14));
 }
 
+// ------------------------------------------------ warp-cooperative forms
+// The 32 lanes of a warp call these with identical arguments; each round
+// tests 32 candidates for the next 5 result bits at once and keeps the
+// largest that still satisfies the defining inequality (exact results,
+// identical to the bit-serial forms above).
+
+// floor(n / d), d >= 1, n < 2^62
+__device__ __forceinline__ u64 warp_udiv64(u64 n, u64 d) {
+    if (n < d) return 0;
+    const u64 lane = threadIdx.x & 31;
+    const int qb = bitlen_u64(n) - bitlen_u64(d) + 1;     // quotient < 2^qb
+    u64 q = 0;
+    for (int sh = qb - 5;; sh -= 5) {
+        const int s = sh < 0 ? 0 : sh;
+        const int nb = sh < 0 ? 5 + sh : 5;
+        const u64 cand = q + (lane << s);
+        const bool ok = lane < (1ull << nb) && cand * d <= n;   // cand*d < 2^(bitlen(n)+1)
+        const unsigned bal = __ballot_sync(0xffffffffu, ok);
+        q += (u64)(31 - __clz((int)bal)) << s;
+        if (sh <= 0) break;
+    }
+    return q;
+}
+
+// floor(sqrt(n)), n < 2^62
+__device__ __forceinline__ u64 warp_isqrt64(u64 n) {
+    if (n == 0) return 0;
+    const u64 lane = threadIdx.x & 31;
+    const int rb = (bitlen_u64(n) + 1) >> 1;              // root < 2^rb
+    u64 r = 0;
+    for (int sh = rb - 5;; sh -= 5) {
+        const int s = sh < 0 ? 0 : sh;
+        const int nb = sh < 0 ? 5 + sh : 5;
+        const u64 cand = r + (lane << s);
+        const bool ok = lane < (1ull << nb) && cand * cand <= n;
+        const unsigned bal = __ballot_sync(0xffffffffu, ok);
+        r += (u64)(31 - __clz((int)bal)) << s;
+        if (sh <= 0) break;
+    }
+    return r;
+}
+
+// dyadic(N, D) computed by a warp
+__device__ __forceinline__ void warp_dyadic(u64 N, u64 D, int* m_out, int* k_out) {
+    int k = 14 + bitlen_u64(D) - bitlen_u64(N);
+    for (int it = 0; it < 4; ++it) {
+        u64 lhs, lo;
+        if (k >= 0) { lhs = N << k; lo = D << 14; }
+        else { lhs = N; lo = D << (14 - k); }
+        if (lhs < lo) { ++k; continue; }
+        if (lhs >= (lo << 1)) { --k; continue; }
+        break;
+    }
+    u64 num, den;
+    if (k >= 0) { num = (N << (k + 1)) + D; den = D << 1; }
+    else { num = (N << 1) + (D << (-k)); den = D << (1 - k); }
+    *m_out = (int)warp_udiv64(num, den);
+    *k_out = k;
+}
+
 }  // namespace detint

@@ -8,8 +8,10 @@
 // shape (DetLLM README, intro and "Layout"; DetLLM blog, section "DetLLM").
 // Integer sums are exact in any order, so no kernel here needs a fixed
 // reduction order; none uses atomics or floating point.
+#pragma once
 #include "kernels.h"
 #include "int_device.cuh"
+#include "ptx.cuh"
 
 namespace detint {
 
@@ -212,13 +214,13 @@ __device__ void qk_norm_warp(i64 (&y)[EPL], const int16_t* gamma, int lane, int 
     for (int j = 0; j < EPL; ++j) y[j] = rshr(xp[j] * (i64)gamma[lane + 32 * j] * Rr, sh);
 }
 
+// one warp: q head `slot` (< nq; q8 to q_dst, scale to mq_dst/kq_dst) or kv
+// head `slot - nq` (K/V written into the paged cache) of token t
 template <int EPL>
-__global__ void __launch_bounds__(128) k_qkv_post(QkvPostArgs a) {
+__device__ void qkv_head(const QkvPostArgs& a, int t, int slot, int8_t* q_dst, int32_t* mq_dst,
+                         int32_t* kq_dst) {
     const int lane = threadIdx.x & 31;
-    const int slot = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int t = blockIdx.y;
     const int nq = a.nq, nkv = a.nkv, d = a.d, dh2 = d >> 1;
-    if (slot >= nq + nkv) return;
     const int lg_d = (EPL == 4) ? 7 : 6;
     const int nqkv = (nq + 2 * nkv) * d;
     const int pos = a.tok_pos[t];
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(128) k_qkv_post(QkvPostArgs a) {
 #pragma unroll
         for (int j = 0; j < EPL; ++j) y[j] *= 4;
     }
-    // RoPE, rotate-dh2 pairing
+    // RoPE, rotate-half pairing
 #pragma unroll
     for (int j = 0; j < EPL / 2; ++j) {
         const int i = lane + 32 * j;
@@ -260,11 +262,11 @@ __global__ void __launch_bounds__(128) k_qkv_post(QkvPostArgs a) {
             am = umax64(am, absu(y[j]));
         }
         am = warp_max_u64(am);
-        int8_t* qo = a.q8 + ((size_t)t * nq + slot) * d;
+        int8_t* qo = q_dst;
         if (am == 0) {
 #pragma unroll
             for (int j = 0; j < EPL; ++j) qo[lane + 32 * j] = 0;
-            if (lane == 0) { a.mq[t * nq + slot] = 0; a.kq[t * nq + slot] = 0; }
+            if (lane == 0) { *mq_dst = 0; *kq_dst = 0; }
             return;
         }
         i64 R = 0, e = 0;
@@ -274,8 +276,8 @@ __global__ void __launch_bounds__(128) k_qkv_post(QkvPostArgs a) {
             e = ee;
             int m, k;
             dyadic_dev(am, 127ull, &m, &k);
-            a.mq[t * nq + slot] = m;
-            a.kq[t * nq + slot] = k + 14;
+            *mq_dst = m;
+            *kq_dst = k + 14;
         }
         R = warp_bcast_i64(R);
         e = warp_bcast_i64(e);
@@ -301,6 +303,15 @@ __global__ void __launch_bounds__(128) k_qkv_post(QkvPostArgs a) {
     }
 }
 
+template <int EPL>
+__global__ void __launch_bounds__(128) k_qkv_post(QkvPostArgs a) {
+    const int slot = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int t = blockIdx.y;
+    if (slot >= a.nq + a.nkv) return;
+    const size_t qi = (size_t)t * a.nq + (slot < a.nq ? slot : 0);
+    qkv_head<EPL>(a, t, slot, a.q8 + qi * a.d, a.mq + qi, a.kq + qi);
+}
+
 // --------------------------------------------------------------- attention
 // a5: one CTA per (token, kv head) serving its group of q heads. Scores
 // S = q8 . k8 (dp4a), base-2 logits, exact row max, 15-bit E_j by the
@@ -321,14 +332,15 @@ size_t attention_smem_bytes(int grp, int d, int ctx_cap) {
            2 * 256 * (size_t)MAXG * 4 + 256;
 }
 
-__global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
-    extern __shared__ __align__(16) unsigned char sm[];
-    const int t = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+// attention of token t's q heads of kv group g; qs [G][d], mqs/kqs [G] in
+// shared memory, sm the dynamic shared memory (score row, E bytes, partials)
+__device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs,
+                               const int32_t* mqs, const int32_t* kqs, unsigned char* sm) {
+    const int tid = threadIdx.x;
     const int d = a.d, G = 1 << a.lg_grp, nkv = a.nkv, cap = a.ctx_cap;
     const int seq = a.tok_seq[t];
     const int ctx = a.tok_pos[t] + 1;
     const int ctx16 = (ctx + 15) & ~15;
-    int8_t* qs = (int8_t*)sm;                                   // [G][d]
     int32_t* S = (int32_t*)(sm + ((G * d + 15) & ~15));        // [G][cap]
     unsigned char* Elo = (unsigned char*)(S + (size_t)G * cap); // [G][cap]
     unsigned char* Ehi = Elo + (size_t)G * cap;                 // [G][cap]
@@ -340,10 +352,6 @@ __global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
     const i64 CSTM = kvp[6], MV = kvp[4];
     const int CSTK = kvp[7], KVS = kvp[5];
     const int* bt = a.block_table + (size_t)seq * a.mbs;
-
-    for (int i = tid; i < G * d; i += 256)
-        qs[i] = a.q8[((size_t)t * a.nq + (g << a.lg_grp)) * d + i];
-    __syncthreads();
 
     // phase 1: scores and per-head maxima
     int smax[MAXG];
@@ -387,8 +395,8 @@ __global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
         if (tid < G) {
             i64 v = red[tid];
             for (int w2 = 1; w2 < 8; ++w2) v = v > red[w2 * MAXG + tid] ? v : red[w2 * MAXG + tid];
-            const i64 mq = a.mq[(size_t)t * a.nq + (g << a.lg_grp) + tid];
-            const int kq = a.kq[(size_t)t * a.nq + (g << a.lg_grp) + tid];
+            const i64 mq = mqs[tid];
+            const int kq = kqs[tid];
             umax_s[tid] = rshr(v * mq * CSTM, kq + CSTK - 10);
         }
         __syncthreads();
@@ -404,8 +412,8 @@ __global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
                 if (hh < G) {
                     int E = 0;
                     if (j < ctx) {
-                        const i64 mq = a.mq[(size_t)t * a.nq + (g << a.lg_grp) + hh];
-                        const int kq = a.kq[(size_t)t * a.nq + (g << a.lg_grp) + hh];
+                        const i64 mq = mqs[hh];
+                        const int kq = kqs[hh];
                         const i64 u = rshr((i64)S[hh * cap + j] * mq * CSTM, kq + CSTK - 10);
                         E = min(32767, exp2q_dev(u - umax_s[hh]));
                     }
@@ -484,6 +492,40 @@ __global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
             a.o[(size_t)t * a.nq * d + ((g << a.lg_grp) + hh) * d + cc] = (int32_t)ov;
         }
     }
+}
+
+// prefill: queries already quantised by k_qkv_post
+__global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
+    extern __shared__ __align__(16) unsigned char sm[];
+    __shared__ int32_t mqs[MAXG], kqs[MAXG];
+    const int t = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+    const int G = 1 << a.lg_grp, d = a.d;
+    int8_t* qs = (int8_t*)sm;
+    for (int i = tid; i < G * d; i += 256) qs[i] = a.q8[((size_t)t * a.nq + (g << a.lg_grp)) * d + i];
+    if (tid < G) {
+        mqs[tid] = a.mq[(size_t)t * a.nq + (g << a.lg_grp) + tid];
+        kqs[tid] = a.kq[(size_t)t * a.nq + (g << a.lg_grp) + tid];
+    }
+    __syncthreads();
+    attention_core(a, t, g, qs, mqs, kqs, sm);
+}
+
+// decode: one new token per sequence, so this CTA alone produces the K/V of
+// (sequence, position) it then attends to; QK-norm/RoPE/quantisation of its
+// G q heads and its kv head run first, one warp per head.
+template <int EPL>
+__global__ void __launch_bounds__(256) k_attn_decode(AttnArgs a, QkvPostArgs qa) {
+    extern __shared__ __align__(16) unsigned char sm[];
+    __shared__ int32_t mqs[MAXG], kqs[MAXG];
+    const int t = blockIdx.x, g = blockIdx.y, w = threadIdx.x >> 5;
+    const int G = 1 << a.lg_grp;
+    int8_t* qs = (int8_t*)sm;
+    pdl_wait();
+    if (w < G) qkv_head<EPL>(qa, t, (g << a.lg_grp) + w, qs + w * a.d, &mqs[w], &kqs[w]);
+    else if (w == G) qkv_head<EPL>(qa, t, a.nq + g, nullptr, nullptr, nullptr);
+    __syncthreads();
+    pdl_launch();
+    attention_core(a, t, g, qs, mqs, kqs, sm);
 }
 
 // ------------------------------------------------------------- GEMV (M<=32)
@@ -663,62 +705,9 @@ __global__ void __launch_bounds__(256) k_gemv(const int8_t* __restrict__ W,
     }
 }
 
-static size_t gemv_smem_bytes(int NT, int K) {
-    return (size_t)8 * NT * (K + 64) + (size_t)8 * 16 * 8 * NT * 4;
-}
-constexpr size_t GEMV_SMEM_MAX = 200 * 1024;
-
-template <int NT, int MODE>
-static cudaError_t gemv_attr() {
-    return cudaFuncSetAttribute(k_gemv<NT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)GEMV_SMEM_MAX);
-}
-
-template <int NT, int MODE>
-static cudaError_t gemv_launch_t(const int8_t* W, const int8_t* X, int M, int N, int K,
-                                 const Epi& ep, cudaStream_t s) {
-    const size_t smem = gemv_smem_bytes(NT, K);
-    const int grid = (N + 15) / 16;
-    k_gemv<NT, MODE><<<grid, 256, smem, s>>>(W, X, M, N, K, ep);
-    return cudaGetLastError();
-}
-
-// the Epi of rows m0.. of a larger launch
-static Epi epi_rows(const Epi& ep, int m0) {
-    Epi e = ep;
-    if (e.out) e.out += (size_t)m0 * ep.ldo;
-    if (e.mt) e.mt += m0;
-    if (e.kt) e.kt += m0;
-    if (e.pval) e.pval += (size_t)m0 * ep.npart;
-    if (e.pidx) e.pidx += (size_t)m0 * ep.npart;
-    return e;
-}
-
-template <int MODE>
-static cudaError_t gemv_nt(const int8_t* W, const int8_t* X, int M, int N, int K, const Epi& ep,
-                           cudaStream_t s) {
-    if (M <= 8) return gemv_launch_t<1, MODE>(W, X, M, N, K, ep, s);
-    if (M <= 16 || gemv_smem_bytes(4, K) > GEMV_SMEM_MAX) {
-        if (M <= 16) return gemv_launch_t<2, MODE>(W, X, M, N, K, ep, s);
-        cudaError_t e = gemv_launch_t<2, MODE>(W, X, 16, N, K, ep, s);
-        if (e != cudaSuccess) return e;
-        return gemv_nt<MODE>(W, X + (size_t)16 * K, M - 16, N, K, epi_rows(ep, 16), s);
-    }
-    return gemv_launch_t<4, MODE>(W, X, M, N, K, ep, s);
-}
-
-cudaError_t launch_gemv(const int8_t* W, const int8_t* X, int M, int N, int K, int mode,
-                        const Epi& ep, cudaStream_t s) {
-    if (M < 1 || M > 32 || N < 1 || (K & 63) || K < 64) return cudaErrorInvalidValue;
-    switch (mode) {
-        case EPI_RAW: return gemv_nt<EPI_RAW>(W, X, M, N, K, ep, s);
-        case EPI_QKV: return gemv_nt<EPI_QKV>(W, X, M, N, K, ep, s);
-        case EPI_RESADD: return gemv_nt<EPI_RESADD>(W, X, M, N, K, ep, s);
-        case EPI_SWIGLU: return gemv_nt<EPI_SWIGLU>(W, X, M, N, K, ep, s);
-        case EPI_LOGITS: return gemv_nt<EPI_LOGITS>(W, X, M, N, K, ep, s);
-    }
-    return cudaErrorInvalidValue;
-}
+}  // namespace detint
+#include "k_sgemv.cuh"
+namespace detint {
 
 // ----------------------------------------------------------- argmax (a11)
 // Final reduction of the per-CTA (max, lowest index) partials of one row;
@@ -733,6 +722,7 @@ __global__ void __launch_bounds__(256) k_argmax_final(const int32_t* __restrict_
                                                       int32_t* __restrict__ seq_len) {
     __shared__ int sv[8], si[8];
     const int r = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
     int bv = -2147483647 - 1, bi = 2147483647;
     for (int i = tid; i < npart; i += 256)
         better(bv, bi, pval[(size_t)r * npart + i], pidx[(size_t)r * npart + i]);
@@ -750,85 +740,6 @@ __global__ void __launch_bounds__(256) k_argmax_final(const int32_t* __restrict_
         next_tok[r] = bi;
         if (seq_len) seq_len[tok_seq[r]] += 1;
     }
-}
-
-// ------------------------------------------------------------- launchers
-cudaError_t launch_embed(const int32_t* tokens, int T, const int32_t* tok_seq, int32_t* tok_pos,
-                         const int32_t* seq_len, int decode, int max_pos, const int8_t* E,
-                         const int32_t* Em, int H, int V, int32_t* h, int32_t* status,
-                         cudaStream_t s) {
-    k_embed<<<T, 256, 0, s>>>(tokens, tok_seq, tok_pos, seq_len, decode, max_pos, E, Em, H, V, h,
-                              status);
-    return cudaGetLastError();
-}
-
-static int ilog2(int n) { int l = 0; while ((1 << l) < n) ++l; return l; }
-
-cudaError_t launch_normquant(const int32_t* x, const int32_t* rows, int R, int n,
-                             const int16_t* gamma, long long eps, int8_t* q, int32_t* mt,
-                             int32_t* kt, cudaStream_t s) {
-    k_normquant<<<R, 256, 0, s>>>(x, rows, n, ilog2(n), gamma, eps, q, mt, kt);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_actquant(const int32_t* x, int R, int n, int F, int8_t* q, int32_t* mt,
-                            int32_t* kt, cudaStream_t s) {
-    k_actquant<<<R, 256, 0, s>>>(x, n, F, q, mt, kt);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_qkv_post(const QkvPostArgs& a, cudaStream_t s) {
-    dim3 grid((a.nq + a.nkv + 3) / 4, a.T);
-    if (a.d == 128) k_qkv_post<4><<<grid, 128, 0, s>>>(a);
-    else if (a.d == 64) k_qkv_post<2><<<grid, 128, 0, s>>>(a);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
-}
-
-cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
-    const size_t smem = attention_smem_bytes(1 << a.lg_grp, a.d, a.ctx_cap);
-    dim3 grid(a.T, a.nkv);
-    k_attention<<<grid, 256, smem, s>>>(a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int rows, int npart,
-                                int32_t* next_tok, const int32_t* tok_seq, int32_t* seq_len,
-                                cudaStream_t s) {
-    k_argmax_final<<<rows, 256, 0, s>>>(pval, pidx, npart, next_tok, tok_seq, seq_len);
-    return cudaGetLastError();
-}
-
-// M > 32 without the tiled GEMM: the GEMV in 32-token chunks (each chunk
-// streams the weights again)
-cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, int mode,
-                        const Epi& ep, cudaStream_t s) {
-    if (K & 63) return cudaErrorInvalidValue;
-    for (int m0 = 0; m0 < M; m0 += 32) {
-        const int mc = M - m0 < 32 ? M - m0 : 32;
-        cudaError_t e = launch_gemv(W, A + (size_t)m0 * K, mc, N, K, mode, epi_rows(ep, m0), s);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
-}
-
-template <int MODE>
-static cudaError_t gemv_attr_all() {
-    cudaError_t e = gemv_attr<1, MODE>();
-    if (e == cudaSuccess) e = gemv_attr<2, MODE>();
-    if (e == cudaSuccess) e = gemv_attr<4, MODE>();
-    return e;
-}
-
-cudaError_t kernels_init() {
-    cudaError_t e = gemv_attr_all<EPI_RAW>();
-    if (e == cudaSuccess) e = gemv_attr_all<EPI_QKV>();
-    if (e == cudaSuccess) e = gemv_attr_all<EPI_RESADD>();
-    if (e == cudaSuccess) e = gemv_attr_all<EPI_SWIGLU>();
-    if (e == cudaSuccess) e = gemv_attr_all<EPI_LOGITS>();
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    return e;
 }
 
 }  // namespace detint

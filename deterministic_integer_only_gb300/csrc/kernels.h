@@ -13,6 +13,7 @@ enum {
     ST_SAT_GU = 3,    // a gate/up output saturated at 2^24
     ST_SAT_LOGIT = 4, // a logit saturated
     ST_SAT_QKV = 5,   // a q/k/v output saturated
+    ST_TIMEOUT = 6,   // a bounded pipeline wait gave up (results invalid)
     ST_N = 8
 };
 
@@ -94,9 +95,19 @@ struct AttnArgs {
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 size_t attention_smem_bytes(int grp, int d, int ctx_cap);
 
+// streaming decode GEMV (M <= 8) with a fused quantisation prologue:
+// pro 1 = NormQuant(xin rows, gamma, eps), 2 = ActQuant(xin rows, F).
+// Returns cudaErrorNotSupported when the shape does not fit (the caller
+// then uses the separate row kernels and launch_gemv).
+cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xin,
+                         const int32_t* rows, const int16_t* gamma, long long eps, int F, int pro,
+                         int mode, const Epi& ep, cudaStream_t s);
+// decode attention fused with the QKV post-processing (one token per sequence)
+cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s);
+
 cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int rows, int npart,
                                 int32_t* next_tok, const int32_t* tok_seq, int32_t* seq_len,
-                                cudaStream_t s);
+                                cudaStream_t s, bool pdl = false);
 
 cudaError_t kernels_init();
 

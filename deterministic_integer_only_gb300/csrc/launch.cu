@@ -1,0 +1,219 @@
+// Host launchers of the detint kernels: grid sizing, shared-memory
+// attributes, programmatic dependent launch. Kernel code lives in the
+// .cuh files.
+#include "kernels.cuh"
+
+namespace detint {
+
+static size_t gemv_smem_bytes(int NT, int K) {
+    return (size_t)8 * NT * (K + 64) + (size_t)8 * 16 * 8 * NT * 4;
+}
+constexpr size_t GEMV_SMEM_MAX = 200 * 1024;
+
+template <int NT, int MODE>
+static cudaError_t gemv_attr() {
+    return cudaFuncSetAttribute(k_gemv<NT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)GEMV_SMEM_MAX);
+}
+
+template <int NT, int MODE>
+static cudaError_t gemv_launch_t(const int8_t* W, const int8_t* X, int M, int N, int K,
+                                 const Epi& ep, cudaStream_t s) {
+    const size_t smem = gemv_smem_bytes(NT, K);
+    const int grid = (N + 15) / 16;
+    k_gemv<NT, MODE><<<grid, 256, smem, s>>>(W, X, M, N, K, ep);
+    return cudaGetLastError();
+}
+
+// the Epi of rows m0.. of a larger launch
+static Epi epi_rows(const Epi& ep, int m0) {
+    Epi e = ep;
+    if (e.out) e.out += (size_t)m0 * ep.ldo;
+    if (e.mt) e.mt += m0;
+    if (e.kt) e.kt += m0;
+    if (e.pval) e.pval += (size_t)m0 * ep.npart;
+    if (e.pidx) e.pidx += (size_t)m0 * ep.npart;
+    return e;
+}
+
+template <int MODE>
+static cudaError_t gemv_nt(const int8_t* W, const int8_t* X, int M, int N, int K, const Epi& ep,
+                           cudaStream_t s) {
+    if (M <= 8) return gemv_launch_t<1, MODE>(W, X, M, N, K, ep, s);
+    if (M <= 16 || gemv_smem_bytes(4, K) > GEMV_SMEM_MAX) {
+        if (M <= 16) return gemv_launch_t<2, MODE>(W, X, M, N, K, ep, s);
+        cudaError_t e = gemv_launch_t<2, MODE>(W, X, 16, N, K, ep, s);
+        if (e != cudaSuccess) return e;
+        return gemv_nt<MODE>(W, X + (size_t)16 * K, M - 16, N, K, epi_rows(ep, 16), s);
+    }
+    return gemv_launch_t<4, MODE>(W, X, M, N, K, ep, s);
+}
+
+cudaError_t launch_gemv(const int8_t* W, const int8_t* X, int M, int N, int K, int mode,
+                        const Epi& ep, cudaStream_t s) {
+    if (M < 1 || M > 32 || N < 1 || (K & 63) || K < 64) return cudaErrorInvalidValue;
+    switch (mode) {
+        case EPI_RAW: return gemv_nt<EPI_RAW>(W, X, M, N, K, ep, s);
+        case EPI_QKV: return gemv_nt<EPI_QKV>(W, X, M, N, K, ep, s);
+        case EPI_RESADD: return gemv_nt<EPI_RESADD>(W, X, M, N, K, ep, s);
+        case EPI_SWIGLU: return gemv_nt<EPI_SWIGLU>(W, X, M, N, K, ep, s);
+        case EPI_LOGITS: return gemv_nt<EPI_LOGITS>(W, X, M, N, K, ep, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+
+// ------------------------------------------------------------- launchers
+cudaError_t launch_embed(const int32_t* tokens, int T, const int32_t* tok_seq, int32_t* tok_pos,
+                         const int32_t* seq_len, int decode, int max_pos, const int8_t* E,
+                         const int32_t* Em, int H, int V, int32_t* h, int32_t* status,
+                         cudaStream_t s) {
+    k_embed<<<T, 256, 0, s>>>(tokens, tok_seq, tok_pos, seq_len, decode, max_pos, E, Em, H, V, h,
+                              status);
+    return cudaGetLastError();
+}
+
+static int ilog2(int n) { int l = 0; while ((1 << l) < n) ++l; return l; }
+
+cudaError_t launch_normquant(const int32_t* x, const int32_t* rows, int R, int n,
+                             const int16_t* gamma, long long eps, int8_t* q, int32_t* mt,
+                             int32_t* kt, cudaStream_t s) {
+    k_normquant<<<R, 256, 0, s>>>(x, rows, n, ilog2(n), gamma, eps, q, mt, kt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_actquant(const int32_t* x, int R, int n, int F, int8_t* q, int32_t* mt,
+                            int32_t* kt, cudaStream_t s) {
+    k_actquant<<<R, 256, 0, s>>>(x, n, F, q, mt, kt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qkv_post(const QkvPostArgs& a, cudaStream_t s) {
+    dim3 grid((a.nq + a.nkv + 3) / 4, a.T);
+    if (a.d == 128) k_qkv_post<4><<<grid, 128, 0, s>>>(a);
+    else if (a.d == 64) k_qkv_post<2><<<grid, 128, 0, s>>>(a);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
+    const size_t smem = attention_smem_bytes(1 << a.lg_grp, a.d, a.ctx_cap);
+    dim3 grid(a.T, a.nkv);
+    k_attention<<<grid, 256, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+// launch with programmatic stream serialization: the kernel may start while
+// its predecessor drains and must griddepcontrol.wait before reading its output
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int rows, int npart,
+                                int32_t* next_tok, const int32_t* tok_seq, int32_t* seq_len,
+                                cudaStream_t s, bool pdl) {
+    if (pdl) return launch_pdl(k_argmax_final, dim3(rows), dim3(256), 0, s, pval, pidx, npart,
+                               next_tok, tok_seq, seq_len);
+    k_argmax_final<<<rows, 256, 0, s>>>(pval, pidx, npart, next_tok, tok_seq, seq_len);
+    return cudaGetLastError();
+}
+
+static int g_num_sms = 0;
+
+static size_t sgemv_smem(int K, int KC) {
+    return (size_t)SG_STAGES * 16 * (KC + 64) + (size_t)8 * (K + 64) + 8 * 16 * 8 * 4;
+}
+constexpr size_t SG_SMEM_MAX = 160 * 1024;
+
+cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xin,
+                         const int32_t* rows, const int16_t* gamma, long long eps, int F, int pro,
+                         int mode, const Epi& ep, cudaStream_t s) {
+    if (M < 1 || M > 8 || N < 1 || K < 64 || (K & 63)) return cudaErrorNotSupported;
+    const int KC = K <= 1024 ? K : 1024;
+    if (K % KC) return cudaErrorNotSupported;
+    if (pro == PRO_NORMQUANT && (K & (K - 1))) return cudaErrorNotSupported;
+    const size_t smem = sgemv_smem(K, KC);
+    if (smem > SG_SMEM_MAX) return cudaErrorNotSupported;
+    SgArgs a{};
+    a.W = W; a.N = N; a.K = K; a.KC = KC; a.nkc = K / KC; a.M = M; a.xin = xin; a.rows = rows;
+    a.gamma = gamma; a.eps = eps; a.F = F; a.pro = pro; a.ep = ep;
+    int lg = 0;
+    while ((1 << lg) < K) ++lg;
+    a.lg_k = lg;
+    const int G = (N + 15) / 16;
+    const int ncta = G < g_num_sms ? G : g_num_sms;
+    a.rg_q = G / ncta;
+    a.rg_r = G % ncta;
+    const dim3 grid(ncta), block(SG_THREADS);
+    if (pro == PRO_NORMQUANT && mode == EPI_QKV) return launch_pdl(k_sgemv<PRO_NORMQUANT, EPI_QKV>, grid, block, smem, s, a);
+    if (pro == PRO_ACTQUANT && mode == EPI_RESADD) return launch_pdl(k_sgemv<PRO_ACTQUANT, EPI_RESADD>, grid, block, smem, s, a);
+    if (pro == PRO_NORMQUANT && mode == EPI_SWIGLU) return launch_pdl(k_sgemv<PRO_NORMQUANT, EPI_SWIGLU>, grid, block, smem, s, a);
+    if (pro == PRO_NORMQUANT && mode == EPI_LOGITS) return launch_pdl(k_sgemv<PRO_NORMQUANT, EPI_LOGITS>, grid, block, smem, s, a);
+    return cudaErrorNotSupported;
+}
+
+cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s) {
+    const size_t smem = attention_smem_bytes(1 << a.lg_grp, a.d, a.ctx_cap);
+    const dim3 grid(a.T, a.nkv);
+    if (a.d == 128) return launch_pdl(k_attn_decode<4>, grid, dim3(256), smem, s, a, qa);
+    if (a.d == 64) return launch_pdl(k_attn_decode<2>, grid, dim3(256), smem, s, a, qa);
+    return cudaErrorInvalidValue;
+}
+
+// M > 32 without the tiled GEMM: the GEMV in 32-token chunks (each chunk
+// streams the weights again)
+cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, int mode,
+                        const Epi& ep, cudaStream_t s) {
+    if (K & 63) return cudaErrorInvalidValue;
+    for (int m0 = 0; m0 < M; m0 += 32) {
+        const int mc = M - m0 < 32 ? M - m0 : 32;
+        cudaError_t e = launch_gemv(W, A + (size_t)m0 * K, mc, N, K, mode, epi_rows(ep, m0), s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <int MODE>
+static cudaError_t gemv_attr_all() {
+    cudaError_t e = gemv_attr<1, MODE>();
+    if (e == cudaSuccess) e = gemv_attr<2, MODE>();
+    if (e == cudaSuccess) e = gemv_attr<4, MODE>();
+    return e;
+}
+
+cudaError_t kernels_init() {
+    cudaError_t e = gemv_attr_all<EPI_RAW>();
+    if (e == cudaSuccess) e = gemv_attr_all<EPI_QKV>();
+    if (e == cudaSuccess) e = gemv_attr_all<EPI_RESADD>();
+    if (e == cudaSuccess) e = gemv_attr_all<EPI_SWIGLU>();
+    if (e == cudaSuccess) e = gemv_attr_all<EPI_LOGITS>();
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn_decode<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn_decode<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    const int sgm = (int)SG_SMEM_MAX;
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_NORMQUANT, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_ACTQUANT, EPI_RESADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_NORMQUANT, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_NORMQUANT, EPI_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
+    int dev = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    return e;
+}
+
+}  // namespace detint

@@ -136,6 +136,7 @@ struct detint_model {
     int npart;
     int32_t* status = nullptr;
     int use_graph = 1;
+    int fused_decode = 1;    // 0: decode through the separate row kernels (tests compare both)
     std::map<std::string, GraphEntry> graphs;
     int32_t* pinned = nullptr;       // host staging for small copies
     size_t pinned_elems = 0;
@@ -225,10 +226,69 @@ static cudaError_t gemm_epi(const int8_t* X, const int8_t* W, int M, int N, int 
 // tok_pos on the device (decode: positions are read from seq_len_dev by the
 // embedding kernel). Produces logits and argmax for the R rows listed in
 // m->rows (prefill) or for every token (decode, rows == nullptr).
+// Decode with at most 8 sequences: 5 kernels per layer chained by
+// programmatic dependent launch (weights stream ahead of the dependency).
+static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32_t* logits,
+                            int32_t* next_tok, cudaStream_t s) {
+    const int H = m->H, d = m->d, nq = m->nq, nkv = m->nkv, F = m->F;
+    const int nqkv = (nq + 2 * nkv) * d;
+    CK(launch_embed(tokens, T, m->tok_seq, m->tok_pos, m->seq_len_dev, 1, m->max_ctx,
+                    m->embed, m->embed_m, H, m->V, m->h, m->status, s));
+    for (int l = 0; l < m->L; ++l) {
+        const LayerW& w = m->layers[l];
+        Epi e{};
+        e.status = m->status;
+        e.out = m->qkv; e.ldo = nqkv; e.mc = w.m_qkv; e.fout = 12;
+        CK(launch_sgemv(w.w_qkv, nqkv, H, T, m->h, nullptr, w.attn_gamma, m->eps_h, 0, 1, EPI_QKV, e, s));
+        QkvPostArgs qa{};
+        qa.qkv = m->qkv; qa.q_gamma = w.q_gamma; qa.k_gamma = w.k_gamma; qa.qk_norm = m->qk_norm;
+        qa.eps_qk = m->eps_qk; qa.rope_cos = m->rope_cos; qa.rope_sin = m->rope_sin; qa.kvp = w.kvp;
+        qa.tok_seq = m->tok_seq; qa.tok_pos = m->tok_pos; qa.block_table = m->block_table;
+        qa.mbs = m->mbs; qa.kc = m->kcache + (size_t)l * m->kv_layer_elems;
+        qa.vc = m->vcache + (size_t)l * m->kv_layer_elems;
+        qa.T = T; qa.nq = nq; qa.nkv = nkv; qa.d = d; qa.lg_grp = m->lg_grp;
+        AttnArgs aa{};
+        aa.kc = qa.kc; aa.vc = qa.vc; aa.block_table = m->block_table; aa.mbs = m->mbs;
+        aa.tok_seq = m->tok_seq; aa.tok_pos = m->tok_pos; aa.kvp = w.kvp; aa.o = m->o; aa.T = T;
+        aa.nq = nq; aa.nkv = nkv; aa.d = d; aa.lg_grp = m->lg_grp; aa.ctx_cap = m->ctx_cap;
+        CK(launch_attn_decode(aa, qa, s));
+        e.out = m->h; e.ldo = H; e.mc = w.m_o; e.fout = 16;
+        CK(launch_sgemv(w.w_o, H, nq * d, T, m->o, nullptr, nullptr, 0, 12, 2, EPI_RESADD, e, s));
+        e.out = m->sbuf; e.ldo = F; e.mc = w.m_gu; e.fout = 12;
+        CK(launch_sgemv(w.w_gu, 2 * F, H, T, m->h, nullptr, w.ffn_gamma, m->eps_h, 0, 1, EPI_SWIGLU, e, s));
+        e.out = m->h; e.ldo = H; e.mc = w.m_d; e.fout = 16;
+        CK(launch_sgemv(w.w_d, H, F, T, m->sbuf, nullptr, nullptr, 0, 10, 2, EPI_RESADD, e, s));
+    }
+    Epi e{};
+    e.status = m->status;
+    e.out = logits ? logits : m->logits_int; e.ldo = m->V; e.mc = m->embed_m; e.fout = 16;
+    e.pval = m->pval; e.pidx = m->pidx; e.npart = m->npart;
+    CK(launch_sgemv(m->embed, m->V, H, T, m->h, nullptr, m->final_gamma, m->eps_h, 0, 1, EPI_LOGITS, e, s));
+    CK(launch_argmax_final(m->pval, m->pidx, T, m->npart, next_tok, m->tok_seq, m->seq_len_dev, s, true));
+    return DETINT_OK;
+}
+
+// every shape the fused decode path supports
+static bool decode_fusable(const detint_model* m, int T) {
+    if (T > 8 || m->fused_decode == 0) return false;
+    const int d = m->d, nq = m->nq, nkv = m->nkv;
+    const int Ks[4] = {m->H, nq * d, m->H, m->F};
+    for (int K : Ks) {
+        if (K & 63) return false;
+        const int KC = K <= 1024 ? K : 1024;
+        if (K % KC) return false;
+        const size_t smem = (size_t)4 * 16 * (KC + 64) + (size_t)8 * (K + 64) + 4096;
+        if (smem > 160 * 1024) return false;
+    }
+    // one warp per q head of a kv group plus one for the K/V head
+    return ((m->H & (m->H - 1)) == 0) && nkv >= 1 && (1 << m->lg_grp) < 8;
+}
+
 static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode, int R,
                        const int32_t* rows, int32_t* logits, int32_t* next_tok, cudaStream_t s) {
     const int H = m->H, d = m->d, nq = m->nq, nkv = m->nkv, F = m->F;
     const int nqkv = (nq + 2 * nkv) * d;
+    if (decode && decode_fusable(m, T)) return run_decode_fused(m, T, tokens, logits, next_tok, s);
     CK(launch_embed(tokens, T, m->tok_seq, m->tok_pos, m->seq_len_dev, decode, m->max_ctx,
                     m->embed, m->embed_m, H, m->V, m->h, m->status, s));
     for (int l = 0; l < m->L; ++l) {
@@ -578,6 +638,14 @@ int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, i
     if (K % 16) return fail(DETINT_E_SHAPE, "detint_gemm_i8: K must be a multiple of 16");
     if (((uintptr_t)A & 15) || ((uintptr_t)B & 15)) return fail(DETINT_E_ARG, "detint_gemm_i8: A and B must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)sp;
+    {
+        static std::mutex mu;
+        static int inited_dev = -1;
+        int dev = 0;
+        CK(cudaGetDevice(&dev));
+        std::lock_guard<std::mutex> lk(mu);
+        if (inited_dev != dev) { CK(kernels_init()); inited_dev = dev; }
+    }
     Epi e{};
     e.out = C; e.ldo = N;
     if (M <= 32 && (K % 64) == 0) { CK(launch_gemv(B, A, M, N, K, EPI_RAW, e, s)); }
@@ -617,6 +685,14 @@ int detint_status(detint_model* m, int32_t* flags, detint_stream_t sp) {
 int detint_set_graph(detint_model* m, int enable) {
     if (!m || (enable != 0 && enable != 1)) return fail(DETINT_E_ARG, "bad argument");
     m->use_graph = enable;
+    return DETINT_OK;
+}
+
+int detint_set_option(detint_model* m, int option, int value) {
+    if (!m || (value != 0 && value != 1)) return fail(DETINT_E_ARG, "bad argument");
+    if (option == DETINT_OPT_GRAPH) m->use_graph = value;
+    else if (option == DETINT_OPT_FUSED_DECODE) { m->fused_decode = value; free_graphs(m); }
+    else return fail(DETINT_E_ARG, "unknown option");
     return DETINT_OK;
 }
 

@@ -111,6 +111,14 @@ int detint_status(detint_model* m, int32_t* flags, detint_stream_t s);
  * (README, "Usage": use_graph). */
 int detint_set_graph(detint_model* m, int enable);
 
+/* Options: DETINT_OPT_GRAPH (1 = replay decode steps as CUDA graphs, the
+ * default; same as detint_set_graph) and DETINT_OPT_FUSED_DECODE (1 = decode
+ * batches of up to 8 sequences through the fused streaming kernels, the
+ * default; 0 = through the separate row kernels). Both settings give
+ * bit-identical results. Errors: ARG. */
+enum { DETINT_OPT_GRAPH = 0, DETINT_OPT_FUSED_DECODE = 1 };
+int detint_set_option(detint_model* m, int option, int value);
+
 /* Shape of the loaded model: info[0..9] = n_layers, hidden, n_q, n_kv,
  * head_dim, ffn, vocab, max_pos, qk_norm, max_batch; info[10] = max_ctx. */
 int detint_model_info(detint_model* m, int32_t* info);

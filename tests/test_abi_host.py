@@ -80,8 +80,12 @@ _FLOAT_LIT = re.compile(r"(?<![\w.])\d+\.\d*(?:[eE][-+]?\d+)?f?\b|(?<![\w.])\d+[
 
 
 def _kernel_sources():
-    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".cu", ".cuh"))
-            and f != "runtime.cu"]
+    """Device code: every .cuh file (host launchers and the runtime are .cu)."""
+    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith(".cuh")]
+
+
+def _all_sources():
+    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".cu", ".cuh"))]
 
 
 def _code_only(src):
@@ -90,8 +94,8 @@ def _code_only(src):
     return re.sub(r'"(?:\\.|[^"\\])*"', '""', src)
 
 
-def test_kernel_sources_have_no_floating_point():
-    for path in _kernel_sources():
+def test_sources_have_no_floating_point():
+    for path in _all_sources():
         code = _code_only(open(path).read())
         assert not _FLOAT.search(code), (path, _FLOAT.search(code).group(0))
         assert not _FLOAT_LIT.search(code), (path, _FLOAT_LIT.search(code).group(0))

@@ -39,12 +39,14 @@ def _load(path, max_batch, max_ctx):
     return pkg.Model(path, max_batch=max_batch, max_ctx=max_ctx)
 
 
-def test_tiny_matches_oracle_every_step(torch_cuda, tiny_artifact):
+@pytest.mark.parametrize("graph,fused", [(True, True), (False, True), (True, False), (False, False)])
+def test_tiny_matches_oracle_every_step(torch_cuda, tiny_artifact, graph, fused):
     prompt = synth.prompt_ids(0, 0, 16, 1024)
     ot, orows = _oracle_run(tiny_artifact, prompt, 16, 64)
-    for graph in (True, False):
+    if True:
         m = _load(tiny_artifact, 2, 64)
         m.set_graph(graph)
+        m.set_fused_decode(fused)
         toks, rows = m.generate([prompt], 16)
         assert np.array_equal(toks[0], ot)
         for s in range(16):
@@ -132,10 +134,12 @@ def test_bad_inputs_are_reported(torch_cuda, tiny_artifact):
     m.close()
 
 
-def test_qwen_shape_matches_oracle(torch_cuda, qwen_artifact):
+@pytest.mark.parametrize("fused", [True, False])
+def test_qwen_shape_matches_oracle(torch_cuda, qwen_artifact, fused):
     prompt = synth.prompt_ids(0, 0, 64, 151936)
     ot, orows = _oracle_run(qwen_artifact, prompt, 6, 128)
     m = _load(qwen_artifact, 8, 1024)
+    m.set_fused_decode(fused)
     toks, rows = m.generate([prompt], 6)
     assert np.array_equal(toks[0], ot)
     for s in range(6):
