@@ -707,6 +707,7 @@ __global__ void __launch_bounds__(256) k_gemv(const int8_t* __restrict__ W,
 
 }  // namespace detint
 #include "k_sgemv.cuh"
+#include "k_gemm.cuh"
 namespace detint {
 
 // ----------------------------------------------------------- argmax (a11)

@@ -1,6 +1,8 @@
 // Host launchers of the detint kernels: grid sizing, shared-memory
 // attributes, programmatic dependent launch. Kernel code lives in the
 // .cuh files.
+#include <cudaTypedefs.h>
+
 #include "kernels.cuh"
 
 namespace detint {
@@ -172,17 +174,54 @@ cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStr
     return cudaErrorInvalidValue;
 }
 
-// M > 32 without the tiled GEMM: the GEMV in 32-token chunks (each chunk
-// streams the weights again)
+// ------------------------------------------------------------ tiled GEMM
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static cudaError_t get_encode() {
+    if (g_encode) return cudaSuccess;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    return cudaSuccess;
+}
+
+// int8 matrix [rows][K] (K % 16 == 0), 128 x 128-byte boxes, 128-byte swizzle,
+// zero fill outside the matrix
+static cudaError_t make_map(CUtensorMap* map, const void* base, int rows, int K) {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {(cuuint32_t)GM_BK, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, int mode,
                         const Epi& ep, cudaStream_t s) {
-    if (K & 63) return cudaErrorInvalidValue;
-    for (int m0 = 0; m0 < M; m0 += 32) {
-        const int mc = M - m0 < 32 ? M - m0 : 32;
-        cudaError_t e = launch_gemv(W, A + (size_t)m0 * K, mc, N, K, mode, epi_rows(ep, m0), s);
-        if (e != cudaSuccess) return e;
+    if ((K & 15) || K < 16 || M < 1 || N < 1) return cudaErrorInvalidValue;
+    if (((uintptr_t)A & 15) || ((uintptr_t)W & 15)) return cudaErrorInvalidValue;
+    cudaError_t e = get_encode();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mw;
+    e = make_map(&ma, A, M, K);
+    if (e == cudaSuccess) e = make_map(&mw, W, N, K);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((N + GM_BN - 1) / GM_BN, (M + GM_BM - 1) / GM_BM);
+    switch (mode) {
+        case EPI_RAW: k_gemm_tma<EPI_RAW><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep); break;
+        case EPI_QKV: k_gemm_tma<EPI_QKV><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep); break;
+        case EPI_RESADD: k_gemm_tma<EPI_RESADD><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep); break;
+        case EPI_SWIGLU: k_gemm_tma<EPI_SWIGLU><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep); break;
+        default: return cudaErrorInvalidValue;
     }
-    return cudaSuccess;
+    return cudaGetLastError();
 }
 
 template <int MODE>
@@ -210,6 +249,10 @@ cudaError_t kernels_init() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_ACTQUANT, EPI_RESADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_NORMQUANT, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_NORMQUANT, EPI_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RESADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     int dev = 0;
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);

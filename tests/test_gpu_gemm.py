@@ -31,7 +31,10 @@ def _run(torch, A, B):
 @pytest.mark.parametrize("M,N,K", [(1, 1, 64), (1, 17, 128), (3, 40, 256), (8, 4096, 1024),
                                    (9, 100, 192), (17, 1000, 320), (31, 333, 640),
                                    (32, 64, 8192), (33, 517, 640), (100, 250, 2048),
-                                   (257, 129, 1024)])
+                                   (257, 129, 1024),
+                                   # K a multiple of 16 only, ragged M/N tails of the 128 tiles
+                                   (1, 1000, 80), (5, 33, 48), (40, 70, 16), (130, 200, 1040),
+                                   (300, 389, 272)])
 def test_gemm_small_exact(torch_cuda, M, N, K):
     rng = np.random.default_rng(M * 1000 + N + K)
     A = rng.integers(-127, 128, (M, K)).astype(np.int8)
