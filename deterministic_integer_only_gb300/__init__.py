@@ -3,7 +3,8 @@
 The compute path is libdetint (hand-written CUDA kernels behind the C ABI in
 include/detint.h); this package only marshals arguments to it.
 """
-from .binding import (Model, DetintError, chain_hash, detint_gemm_i8, lib, LIB_PATH,
-                      SYMBOLS)
+from .binding import (Model, DetintError, chain_hash, detint_gemm_i8, detint_argmax_noalloc,
+                      lib, LIB_PATH, SYMBOLS)
 
-__all__ = ["Model", "DetintError", "chain_hash", "detint_gemm_i8", "lib", "LIB_PATH", "SYMBOLS"]
+__all__ = ["Model", "DetintError", "chain_hash", "detint_gemm_i8", "detint_argmax_noalloc", "lib",
+           "LIB_PATH", "SYMBOLS"]

@@ -25,7 +25,7 @@ ERRORS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "token id o
 # every entry point of include/detint.h
 SYMBOLS = ["detint_load", "detint_prefill", "detint_decode_step", "detint_gemm_i8",
            "detint_reset_seq", "detint_seq_len", "detint_status", "detint_set_graph",
-           "detint_set_option",
+           "detint_set_option", "detint_argmax_noalloc",
            "detint_model_info", "detint_free", "detint_strerror", "detint_last_error"]
 
 
@@ -54,6 +54,7 @@ def lib():
         L.detint_status.argtypes = [vp, i32p, vp]
         L.detint_set_graph.argtypes = [vp, C.c_int]
         L.detint_set_option.argtypes = [vp, C.c_int, C.c_int]
+        L.detint_argmax_noalloc.argtypes = [vp, C.c_int, C.c_int, vp, vp]
         L.detint_model_info.argtypes = [vp, i32p]
         L.detint_free.argtypes = [vp]
         L.detint_free.restype = None
@@ -91,6 +92,15 @@ def detint_gemm_i8(A, B, C_out, stream=None):
     _check(lib().detint_gemm_i8(_ptr(A), _ptr(B), _ptr(C_out), M, N, K, _stream(stream)),
            "detint_gemm_i8")
     return C_out
+
+
+def detint_argmax_noalloc(logits, out, stream=None):
+    """out[r] = tie-low argmax of logits[r] (int32 cuda tensors), computed
+    without any device allocation (partials in a fixed device array)."""
+    rows, n = logits.shape
+    _check(lib().detint_argmax_noalloc(_ptr(logits), rows, n, _ptr(out), _stream(stream)),
+           "detint_argmax_noalloc")
+    return out
 
 
 def chain_hash(rows, prev: bytes | None = None) -> bytes:

@@ -93,6 +93,27 @@ int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const
 int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, int K,
                    detint_stream_t s);
 
+/* Tie-low argmax of `rows` int32 rows of length `n` (device, row-major) into
+ * out[rows] (device int32), for callers that cannot allocate device memory:
+ * code running inside a stream capture that must stay allocation-free, in a
+ * host callback, or under an application that owns every allocation. This
+ * entry point calls no cudaMalloc/cudaFree or allocating library routine;
+ * its per-block partial results live in one fixed device array of 128 KB
+ * that every GPU loading this library holds until the process exits.
+ * Limits: rows <= DETINT_ARGMAX_NOALLOC_MAX_ROWS, n <=
+ * DETINT_ARGMAX_NOALLOC_MAX_COLS; larger sizes return DETINT_E_SHAPE.
+ * The first call on a device looks up that array's device address (with the
+ * device current), so make it before any stream capture. All calls share the
+ * one array: calls that overlap on the GPU (different streams, no ordering)
+ * race and give wrong results; calls ordered on one stream are safe. Each
+ * call writes every partial slot it reads, so no clearing is needed.
+ * Ties go to the lowest column, as in the decode steps' token choice. The
+ * pages have no counterpart to this entry point.
+ * Errors: ARG, SHAPE, CUDA. */
+#define DETINT_ARGMAX_NOALLOC_MAX_ROWS 64
+#define DETINT_ARGMAX_NOALLOC_MAX_COLS 1048576
+int detint_argmax_noalloc(const int32_t* logits, int rows, int n, int32_t* out, detint_stream_t s);
+
 /* Forget a sequence's cached context (length back to 0). Synchronises the
  * device first. Errors: ARG, SEQ, CUDA. */
 int detint_reset_seq(detint_model* m, int seq_id);
