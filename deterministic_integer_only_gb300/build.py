@@ -30,13 +30,15 @@ def _deps():
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and os.path.exists(OUT) and os.path.getmtime(OUT) >= _deps():
+    """DETINT_NVCC_FLAGS (space-separated) adds compiler flags."""
+    extra = os.environ.get("DETINT_NVCC_FLAGS", "").split()
+    if not force and not extra and os.path.exists(OUT) and os.path.getmtime(OUT) >= _deps():
         return OUT
     os.makedirs(BUILD, exist_ok=True)
 
     def compile_one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc(), *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")

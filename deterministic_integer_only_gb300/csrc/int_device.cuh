@@ -102,15 +102,19 @@ __device__ __forceinline__ int swiglu_dev(int g, int u) {
     i64 ag = g < 0 ? -(i64)g : (i64)g;
     i64 z = rshr(ag * 47274LL, 17);
     int Ez = exp2q_dev(-z);
-    unsigned D = 32768u + (unsigned)Ez;                  // [2^15, 2^16]
-    // round(2^30 / D) = floor((2^31 + D) / 2D): quotient < 2^16
-    u64 num = 0x80000000ull + D, dd = (u64)D << 16;  // 2D * 2^15
-    unsigned q = 0;
+    const unsigned D = 32768u + (unsigned)Ez;            // [2^15, 2^16]
+    // round(2^30 / D) = floor((2^31 + D) / 2D) <= 2^15, and = 2^15 only for
+    // D = 2^15; otherwise 15 quotient bits by restoring division in 32 bits
+    unsigned q = 32768u;
+    if (D != 32768u) {
+        unsigned num = 0x80000000u + D, dd = D << 15;   // 2D * 2^14 < 2^32
+        q = 0;
 #pragma unroll
-    for (int i = 15; i >= 0; --i) {
-        q <<= 1;
-        if (num >= dd) { num -= dd; q |= 1u; }
-        dd >>= 1;
+        for (int i = 14; i >= 0; --i) {
+            q <<= 1;
+            if (num >= dd) { num -= dd; q |= 1u; }
+            dd >>= 1;
+        }
     }
     i64 sg = g >= 0 ? (i64)q : 32768LL - (i64)q;
     i64 silu = rshr((i64)g * sg, 15);

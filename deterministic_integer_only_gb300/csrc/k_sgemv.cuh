@@ -22,7 +22,9 @@ namespace detint {
 constexpr int SG_STAGES = 4;
 constexpr int SG_THREADS = 288;      // 8 compute warps + 1 producer warp
 
-enum { PRO_NORMQUANT = 1, PRO_ACTQUANT = 2 };
+enum { PRO_NONE = 0, PRO_NORMQUANT = 1, PRO_ACTQUANT = 2 };
+
+constexpr int SG_GB = 4;             // row groups whose partial sums are reduced together
 
 struct SgArgs {
     const int8_t* W;          // weights [N][K]
@@ -34,7 +36,11 @@ struct SgArgs {
     long long eps;
     int lg_k;                 // log2 K (NormQuant mean)
     int F;                    // PRO_ACTQUANT fixed point
-    int pro;
+    int pro;                  // PRO_NORMQUANT, PRO_ACTQUANT or PRO_NONE
+    const int8_t* x8;         // PRO_NONE: quantised rows [M][K]
+    const int32_t* mt_in;     // PRO_NONE: token scales [M]
+    const int32_t* kt_in;
+    int mode;                 // EPI_QKV, EPI_RESADD, EPI_SWIGLU or EPI_LOGITS
     int rg_q, rg_r;           // CTA c owns rg_q + (c < rg_r) row groups
     Epi ep;
 };
@@ -43,17 +49,33 @@ struct SgShared {
     unsigned long long full[SG_STAGES];
     unsigned long long empty[SG_STAGES];
     int mt[8], kt[8];
-    long long red64[8][2];     // prologue group reductions (per warp)
-    long long bc[8][4];        // per-row broadcast of R, shift, sigma, flag
+    long long red64[8][3];     // prologue group reductions (per warp)
+    long long bc[8][2];        // per-row quantisation multiplier and shift
 };
 
 __device__ __forceinline__ size_t sg_ring_bytes(int KC) { return (size_t)SG_STAGES * 16 * (KC + 64); }
 
-// ---- prologue: one group of (8 / Mp) warps per token row
-template <int PRO>
-__device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP) {
+// ---- prologue: one group of (8 / Mp) warps per token row quantises it into
+// the int8 tile. The row is read once; up to SG_NV 16-byte vectors per thread
+// stay in registers for the later passes. The integer square root and the
+// two divisions run on different warps of the group where it has more than
+// one.
+constexpr int SG_NV = 6;
+
+__device__ __forceinline__ int4 sg_vec(const int4 (&v)[SG_NV], const int32_t* xr, int j, int i) {
+    // vector j of this thread (element offset i): from registers when held
+    int4 r = make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int q = 0; q < SG_NV; ++q)
+        if (q == j) r = v[q];
+    if (j >= SG_NV) r = *(const int4*)(xr + i);
+    return r;
+}
+
+__device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, const int16_t* gam) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int M = a.M, K = a.K;
+    const bool norm = a.pro == PRO_NORMQUANT;
     const int lgw = M > 4 ? 0 : (M > 2 ? 1 : (M > 1 ? 2 : 3));   // log2 warps per row
     const int wpr = 1 << lgw;
     const int r = warp >> lgw;              // row of this warp's group
@@ -61,6 +83,7 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP) {
     const int gt = gw * 32 + lane;          // thread index in its group
     const int gn = wpr * 32;
     const int bar = 2 + r;
+    const int w0 = r << lgw;                // first warp of the group
     int8_t* qr = xs + (size_t)r * XP;
     if (r >= M) {
         for (int i = gt * 16; i < K; i += gn * 16) *(int4*)(qr + i) = make_int4(0, 0, 0, 0);
@@ -68,108 +91,216 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP) {
     }
     const int src = a.rows ? a.rows[r] : r;
     const int32_t* xr = a.xin + (size_t)src * K;
+    const int nvec = K >> 2;                                  // 16-byte vectors in the row
+    const int nv = (nvec + gn - 1) >> (5 + lgw);              // per thread (the last may be empty)
+    int4 v[SG_NV];
+#pragma unroll
+    for (int j = 0; j < SG_NV; ++j)
+        v[j] = (j < nv && gt + j * gn < nvec) ? *(const int4*)(xr + (gt + j * gn) * 4)
+                                              : make_int4(0, 0, 0, 0);
     // pass 1: max |x|
     u64 ax = 0;
-    for (int i = gt * 4; i < K; i += gn * 4) {
-        const int4 v = *(const int4*)(xr + i);
-        ax = umax64(ax, umax64(umax64(absu(v.x), absu(v.y)), umax64(absu(v.z), absu(v.w))));
+    for (int j = 0; j < nv; ++j) {
+        if (gt + j * gn >= nvec) break;
+        const int4 w = sg_vec(v, xr, j, (gt + j * gn) * 4);
+        ax = umax64(ax, umax64(umax64(absu(w.x), absu(w.y)), umax64(absu(w.z), absu(w.w))));
     }
     ax = warp_max_u64(ax);
     if (lane == 0) sh.red64[warp][0] = (long long)ax;
     bar_named(bar, gn);
     ax = 0;
-    for (int w = 0; w < wpr; ++w) ax = umax64(ax, (u64)sh.red64[(r << lgw) + w][0]);
-    bar_named(bar, gn);
+    for (int w = 0; w < wpr; ++w) ax = umax64(ax, (u64)sh.red64[w0 + w][0]);
     if (ax == 0) {
         for (int i = gt * 16; i < K; i += gn * 16) *(int4*)(qr + i) = make_int4(0, 0, 0, 0);
         if (gt == 0) { sh.mt[r] = 0; sh.kt[r] = 0; }
         return;
     }
     int sig = 0;
-    u64 amax = ax;
-    if (PRO == PRO_NORMQUANT) {
+    if (norm) {
         sig = bitlen_u64(ax) - 24;
         // pass 2: sum of squares of the 24-bit row and max |x' gamma|
         i64 ss = 0;
         u64 az = 0;
-        for (int i = gt * 4; i < K; i += gn * 4) {
-            const int4 v = *(const int4*)(xr + i);
-            const int xv[4] = {v.x, v.y, v.z, v.w};
+        for (int j = 0; j < nv; ++j) {
+            if (gt + j * gn >= nvec) break;
+            const int i = (gt + j * gn) * 4;
+            const int4 w = sg_vec(v, xr, j, i);
+            const short4 gm = *(const short4*)(gam + i);
+            const int xv[4] = {w.x, w.y, w.z, w.w};
+            const int gv[4] = {gm.x, gm.y, gm.z, gm.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const i64 xp = norm24(xv[j], sig);
+            for (int q = 0; q < 4; ++q) {
+                const i64 xp = norm24(xv[q], sig);
                 ss += xp * xp;
-                az = umax64(az, absu(xp * (i64)a.gamma[i + j]));
+                az = umax64(az, absu(xp * (i64)gv[q]));
             }
         }
         ss = warp_sum_i64(ss);
         az = warp_max_u64(az);
-        if (lane == 0) { sh.red64[warp][0] = ss; sh.red64[warp][1] = (long long)az; }
+        if (lane == 0) { sh.red64[warp][1] = ss; sh.red64[warp][2] = (long long)az; }
         bar_named(bar, gn);
         ss = 0;
         az = 0;
         for (int w = 0; w < wpr; ++w) {
-            ss += sh.red64[(r << lgw) + w][0];
-            az = umax64(az, (u64)sh.red64[(r << lgw) + w][1]);
+            ss += sh.red64[w0 + w][1];
+            az = umax64(az, (u64)sh.red64[w0 + w][2]);
         }
-        amax = az;
+        const int e = bitlen_u64(az);
         if (gw == 0) {
             i64 eps_s;
             if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (a.eps >> (2 * sig));
             else eps_s = a.eps * (1LL << (-2 * sig));
             const u64 rr = warp_isqrt64((u64)((ss >> a.lg_k) + eps_s));
-            const int e = bitlen_u64(az);
-            const u64 R = warp_udiv64(127ull << (e + 16), az);
             int m, k;
             warp_dyadic(az, 127ull * rr, &m, &k);
-            if (lane == 0) {
-                sh.bc[r][0] = (long long)R;
-                sh.bc[r][1] = e + 16;
-                sh.mt[r] = m;
-                sh.kt[r] = k + 12;
-            }
+            if (lane == 0) { sh.mt[r] = m; sh.kt[r] = k + 12; }
+        }
+        if (gw == (wpr > 1 ? 1 : 0)) {
+            const u64 R = warp_udiv64(127ull << (e + 16), az);
+            if (lane == 0) { sh.bc[r][0] = (long long)R; sh.bc[r][1] = e + 16; }
         }
     } else {
+        const int e = bitlen_u64(ax);
         if (gw == 0) {
-            const int e = bitlen_u64(ax);
             const u64 R = warp_udiv64(127ull << (e + 16), ax);
+            if (lane == 0) { sh.bc[r][0] = (long long)R; sh.bc[r][1] = e + 16; }
+        }
+        if (gw == (wpr > 1 ? 1 : 0)) {
             int m, k;
             warp_dyadic(ax, 127ull, &m, &k);
-            if (lane == 0) {
-                sh.bc[r][0] = (long long)R;
-                sh.bc[r][1] = e + 16;
-                sh.mt[r] = m;
-                sh.kt[r] = k + a.F;
-            }
+            if (lane == 0) { sh.mt[r] = m; sh.kt[r] = k + a.F; }
         }
     }
-    (void)amax;
     bar_named(bar, gn);
     const i64 R = sh.bc[r][0];
     const int shq = (int)sh.bc[r][1];
     // pass 3: quantise
-    for (int i = gt * 4; i < K; i += gn * 4) {
-        const int4 v = *(const int4*)(xr + i);
-        const int xv[4] = {v.x, v.y, v.z, v.w};
-        char4 q;
+    for (int j = 0; j < nv; ++j) {
+        if (gt + j * gn >= nvec) break;
+        const int i = (gt + j * gn) * 4;
+        const int4 w = sg_vec(v, xr, j, i);
+        const int xv[4] = {w.x, w.y, w.z, w.w};
         i64 z[4];
+        if (norm) {
+            const short4 gm = *(const short4*)(gam + i);
+            const int gv[4] = {gm.x, gm.y, gm.z, gm.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            z[j] = (PRO == PRO_NORMQUANT) ? norm24(xv[j], sig) * (i64)a.gamma[i + j] : (i64)xv[j];
-        q.x = (signed char)rshr(z[0] * R, shq);
-        q.y = (signed char)rshr(z[1] * R, shq);
-        q.z = (signed char)rshr(z[2] * R, shq);
-        q.w = (signed char)rshr(z[3] * R, shq);
-        *(char4*)(qr + i) = q;
+            for (int q = 0; q < 4; ++q) z[q] = norm24(xv[q], sig) * (i64)gv[q];
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) z[q] = xv[q];
+        }
+        char4 c4;
+        c4.x = (signed char)rshr(z[0] * R, shq);
+        c4.y = (signed char)rshr(z[1] * R, shq);
+        c4.z = (signed char)rshr(z[2] * R, shq);
+        c4.w = (signed char)rshr(z[3] * R, shq);
+        *(char4*)(qr + i) = c4;
     }
 }
 
-__device__ __forceinline__ i64 sg_requant(int acc, const SgShared& sh, const Epi& ep, int tk, int n) {
-    const i64 M = (i64)sh.mt[tk] * (i64)ep.mc[n];
+// PRO_NONE: the rows were quantised by a row kernel; load the int8 tile and
+// the token scales
+__device__ void sg_load_x8(const SgArgs& a, SgShared& sh, int8_t* xs, int XP) {
+    const int tid = threadIdx.x;
+    const int kv = a.K >> 4;
+    for (int r = 0; r < 8; ++r)
+        for (int v = tid; v < kv; v += 256) {
+            int4 val = make_int4(0, 0, 0, 0);
+            if (r < a.M) val = *(const int4*)(a.x8 + (size_t)r * a.K + v * 16);
+            *(int4*)(xs + (size_t)r * XP + v * 16) = val;
+        }
+    if (tid < 8) {
+        sh.mt[tid] = tid < a.M ? a.mt_in[tid] : 0;
+        sh.kt[tid] = tid < a.M ? a.kt_in[tid] : 0;
+    }
+}
+
+// weight-channel scale of output row n: from the CTA's shared-memory copy when
+// it was staged (mcs, rows from nbase), else from global memory
+__device__ __forceinline__ i64 sg_requant(int acc, const SgShared& sh, const Epi& ep, int tk, int n,
+                                          const int32_t* mcs, int nbase) {
+    const i64 mc = mcs ? mcs[n - nbase] : ep.mc[n];
+    const i64 M = (i64)sh.mt[tk] * mc;
     return rshr((i64)acc * M, sh.kt[tk] + 22 - ep.fout);
 }
 
-template <int PRO, int MODE>
+// epilogue of nb row groups starting at group gb, from the per-warp partial
+// tiles red[b][warp][16 rows][8 tokens]
+__device__ void sg_epilogue(const SgArgs& a, const SgShared& sh, int32_t* red, int gb, int nb,
+                            const int32_t* hold, int g0, const int32_t* mcs) {
+    const int nbase = g0 * 16;
+    const int tid = threadIdx.x;
+    const Epi& ep = a.ep;
+    if (a.mode == EPI_SWIGLU) {
+        for (int it = tid; it < nb * 64; it += 256) {
+            const int b = it >> 6, p = (it >> 3) & 7, tk = it & 7;
+            const int32_t* rb = red + b * 1024;
+            int sg = 0, su = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                sg += rb[w * 128 + (2 * p) * 8 + tk];
+                su += rb[w * 128 + (2 * p + 1) * 8 + tk];
+            }
+            const int n = (gb + b) * 16 + 2 * p;
+            if (tk < a.M && n < a.N) {
+                i64 yg = sg_requant(sg, sh, ep, tk, n, mcs, nbase), yu = sg_requant(su, sh, ep, tk, n + 1, mcs, nbase);
+                if (yg > (1 << 24) || yg < -(1 << 24) || yu > (1 << 24) || yu < -(1 << 24))
+                    ep.status[ST_SAT_GU] = 1;
+                yg = sat_b(yg, 1 << 24);
+                yu = sat_b(yu, 1 << 24);
+                ep.out[(size_t)tk * ep.ldo + (n >> 1)] = swiglu_dev((int)yg, (int)yu);
+            }
+        }
+        return;
+    }
+    for (int it = tid; it < nb * 128; it += 256) {
+        const int b = it >> 7, rr = (it >> 3) & 15, tk = it & 7;
+        const int32_t* rb = red + b * 1024;
+        int sum = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) sum += rb[w * 128 + (it & 127)];
+        const int n = (gb + b) * 16 + rr;
+        int outv = -2147483647;
+        if (tk < a.M && n < a.N) {
+            const i64 y = sg_requant(sum, sh, ep, tk, n, mcs, nbase);
+            if (a.mode == EPI_QKV) {
+                if (y > 2147483647LL || y < -2147483647LL) ep.status[ST_SAT_QKV] = 1;
+                ep.out[(size_t)tk * ep.ldo + n] = sat32(y);
+            } else if (a.mode == EPI_RESADD) {
+                int32_t* hp = ep.out + (size_t)tk * ep.ldo + n;
+                const int li = ((gb + b - g0) * 16 + rr) * 8 + tk;      // preloaded slot
+                const i64 hv = hold ? hold[li] : *hp;
+                const i64 s2 = hv + (i64)sat32(y);
+                if (s2 > 2147483647LL || s2 < -2147483647LL) ep.status[ST_SAT_RES] = 1;
+                *hp = sat32(s2);
+            } else {
+                if (y > 2147483647LL || y < -2147483647LL) ep.status[ST_SAT_LOGIT] = 1;
+                outv = sat32(y);
+                ep.out[(size_t)tk * ep.ldo + n] = outv;
+            }
+        }
+        if (a.mode == EPI_LOGITS) red[b * 1024 + (it & 127)] = outv;   // warp 0's slot, summed already
+    }
+    if (a.mode == EPI_LOGITS) {
+        bar_named(1, 256);
+        // per (group, token): the largest logit of the 16 rows, lowest row on ties
+        for (int it = tid; it < nb * 8; it += 256) {
+            const int b = it >> 3, tk = it & 7;
+            if (tk >= a.M) continue;
+            const int n0 = (gb + b) * 16;
+            const int32_t* lg = red + b * 1024;
+            int bv = lg[tk], bi = n0;
+            for (int q = 1; q < 16; ++q) {
+                const int v = lg[q * 8 + tk];
+                if (v > bv && n0 + q < a.N) { bv = v; bi = n0 + q; }
+            }
+            ep.pval[(size_t)tk * ep.npart + gb + b] = bv;
+            ep.pidx[(size_t)tk * ep.npart + gb + b] = bi;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ SgShared sh;
@@ -178,7 +309,7 @@ __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
     const int XP = a.K + 64;                      // activation row pitch
     unsigned char* ring = smem;
     int8_t* xs = (int8_t*)(smem + sg_ring_bytes(a.KC));
-    int32_t* red = (int32_t*)(xs + (size_t)8 * XP);     // [8 warps][16][8]
+    int32_t* red = (int32_t*)(xs + (size_t)8 * XP);     // [SG_GB][8 warps][16][8]
     const int c = blockIdx.x;
     const int g0 = c * a.rg_q + min(c, a.rg_r);
     const int g1 = g0 + a.rg_q + (c < a.rg_r ? 1 : 0);
@@ -220,99 +351,62 @@ __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
         return;
     }
 
-    // compute warps
+    // compute warps: copy the (immutable) RMSNorm gamma and this CTA's weight
+    // channel scales before the wait
+    int16_t* gam = (int16_t*)(red + SG_GB * 1024);
+    if (a.pro == PRO_NORMQUANT)
+        for (int i = tid * 8; i < a.K; i += 256 * 8) *(int4*)(gam + i) = *(const int4*)(a.gamma + i);
+    int32_t* hold = (int32_t*)(gam + a.K);
+    int32_t* mcs = hold + 256;
+    const bool mc_pre = (g1 - g0) * 16 <= 256;
+    if (mc_pre && tid < (g1 - g0) * 16) mcs[tid] = a.ep.mc[min(g0 * 16 + tid, a.N - 1)];
     pdl_wait();
-    sg_prologue<PRO>(a, sh, xs, XP);
+    // residual add: issue the loads of this CTA's old residual values now so
+    // they overlap the quantisation prologue
+    const bool pre = a.mode == EPI_RESADD && (g1 - g0) * 128 <= 256;
+    int hv = 0;
+    if (pre && tid < (g1 - g0) * 128) {
+        const int tk = tid & 7, n = g0 * 16 + (tid >> 3);
+        if (tk < a.M && n < a.N) hv = a.ep.out[(size_t)tk * a.ep.ldo + n];
+    }
+    if (a.pro == PRO_NONE) sg_load_x8(a, sh, xs, XP);
+    else sg_prologue(a, sh, xs, XP, gam);
+    if (pre && tid < (g1 - g0) * 128) hold[tid] = hv;
     bar_named(1, 256);
 
     const int g = lane >> 2, tq = lane & 3;
     const int nch = a.KC >> 6;
     int u = 0;
-    for (int grp = g0; grp < g1; ++grp) {
-        int acc[4] = {0, 0, 0, 0};
-        for (int kc = 0; kc < a.nkc; ++kc, ++u) {
-            const int s = u & (SG_STAGES - 1);
-            if (!mbar_wait(smem_u32(&sh.full[s]), (u >> 2) & 1)) a.ep.status[ST_TIMEOUT] = 1;
-            const int8_t* st = (const int8_t*)ring + (size_t)s * 16 * P;
-            const int8_t* wlo = st + g * P + 16 * tq;
-            const int8_t* whi = wlo + 8 * P;
-            const int8_t* xb = xs + g * XP + kc * a.KC + 16 * tq;
-            for (int ch = warp; ch < nch; ch += 8) {
-                const int4 al = *(const int4*)(wlo + ch * 64);
-                const int4 ah = *(const int4*)(whi + ch * 64);
-                const int4 b = *(const int4*)(xb + ch * 64);
-                mma_s8(acc, al.x, ah.x, al.y, ah.y, b.x, b.y);
-                mma_s8(acc, al.z, ah.z, al.w, ah.w, b.z, b.w);
+    for (int gb = g0; gb < g1; gb += SG_GB) {
+        const int nb = min(SG_GB, g1 - gb);
+        for (int b = 0; b < nb; ++b) {
+            int acc[4] = {0, 0, 0, 0};
+            for (int kc = 0; kc < a.nkc; ++kc, ++u) {
+                const int s = u & (SG_STAGES - 1);
+                if (!mbar_wait(smem_u32(&sh.full[s]), (u >> 2) & 1)) a.ep.status[ST_TIMEOUT] = 1;
+                const int8_t* st = (const int8_t*)ring + (size_t)s * 16 * P;
+                const int8_t* wlo = st + g * P + 16 * tq;
+                const int8_t* whi = wlo + 8 * P;
+                const int8_t* xb = xs + g * XP + kc * a.KC + 16 * tq;
+                for (int ch = warp; ch < nch; ch += 8) {
+                    const int4 al = *(const int4*)(wlo + ch * 64);
+                    const int4 ah = *(const int4*)(whi + ch * 64);
+                    const int4 bx = *(const int4*)(xb + ch * 64);
+                    mma_s8(acc, al.x, ah.x, al.y, ah.y, bx.x, bx.y);
+                    mma_s8(acc, al.z, ah.z, al.w, ah.w, bx.z, bx.w);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
+            // accumulator fragment: c0 (row g, tok 2tq), c1, c2 (row g+8), c3
+            int32_t* rw = red + b * 1024 + warp * 128;
+            rw[g * 8 + 2 * tq] = acc[0];
+            rw[g * 8 + 2 * tq + 1] = acc[1];
+            rw[(g + 8) * 8 + 2 * tq] = acc[2];
+            rw[(g + 8) * 8 + 2 * tq + 1] = acc[3];
         }
-        int32_t* rw = red + warp * 128;
-        rw[g * 8 + 2 * tq] = acc[0];
-        rw[g * 8 + 2 * tq + 1] = acc[1];
-        rw[(g + 8) * 8 + 2 * tq] = acc[2];
-        rw[(g + 8) * 8 + 2 * tq + 1] = acc[3];
         bar_named(1, 256);
-        const int n0 = grp * 16;
-        const Epi& ep = a.ep;
-        if (MODE == EPI_SWIGLU) {
-            if (tid < 64) {
-                const int p = tid >> 3, tk = tid & 7;
-                int sg = 0, su = 0;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    sg += red[w * 128 + (2 * p) * 8 + tk];
-                    su += red[w * 128 + (2 * p + 1) * 8 + tk];
-                }
-                const int n = n0 + 2 * p;
-                if (tk < a.M && n < a.N) {
-                    i64 yg = sg_requant(sg, sh, ep, tk, n), yu = sg_requant(su, sh, ep, tk, n + 1);
-                    if (yg > (1 << 24) || yg < -(1 << 24) || yu > (1 << 24) || yu < -(1 << 24))
-                        ep.status[ST_SAT_GU] = 1;
-                    yg = sat_b(yg, 1 << 24);
-                    yu = sat_b(yu, 1 << 24);
-                    ep.out[(size_t)tk * ep.ldo + (n >> 1)] = swiglu_dev((int)yg, (int)yu);
-                }
-            }
-        } else if (tid < 128) {
-            const int rr = tid >> 3, tk = tid & 7;
-            int sum = 0;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) sum += red[w * 128 + tid];
-            const int n = n0 + rr;
-            int outv = -2147483647;
-            if (tk < a.M && n < a.N) {
-                const i64 y = sg_requant(sum, sh, ep, tk, n);
-                if (MODE == EPI_QKV) {
-                    if (y > 2147483647LL || y < -2147483647LL) ep.status[ST_SAT_QKV] = 1;
-                    ep.out[(size_t)tk * ep.ldo + n] = sat32(y);
-                } else if (MODE == EPI_RESADD) {
-                    int32_t* hp = ep.out + (size_t)tk * ep.ldo + n;
-                    const i64 s2 = (i64)*hp + (i64)sat32(y);
-                    if (s2 > 2147483647LL || s2 < -2147483647LL) ep.status[ST_SAT_RES] = 1;
-                    *hp = sat32(s2);
-                } else if (MODE == EPI_LOGITS) {
-                    if (y > 2147483647LL || y < -2147483647LL) ep.status[ST_SAT_LOGIT] = 1;
-                    outv = sat32(y);
-                    ep.out[(size_t)tk * ep.ldo + n] = outv;
-                }
-            }
-            if (MODE == EPI_LOGITS) {
-                // per-token (max, lowest row) of this row group, via the red tile
-                bar_named(2, 128);
-                red[tid] = outv;          // warp 0's slot is free again after the sums
-                bar_named(2, 128);
-                if (tid < a.M) {
-                    int bv = red[tid], bi = n0;
-                    for (int q = 1; q < 16; ++q) {
-                        const int v = red[q * 8 + tid];
-                        if (v > bv && n0 + q < a.N) { bv = v; bi = n0 + q; }
-                    }
-                    ep.pval[(size_t)tid * ep.npart + grp] = bv;
-                    ep.pidx[(size_t)tid * ep.npart + grp] = bi;
-                }
-            }
-        }
+        sg_epilogue(a, sh, red, gb, nb, pre ? hold : nullptr, g0, mc_pre ? mcs : nullptr);
         bar_named(1, 256);
     }
     // every issued copy has completed before the CTA exits (bounded wait;

@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(256) k_normquant(const int32_t* __restrict__ x
     __shared__ u64 redu[8];
     __shared__ i64 bc[2];
     const int r = blockIdx.x, tid = threadIdx.x;
+    pdl_launch();
+    pdl_wait();
     const int src = rows ? rows[r] : r;
     const int32_t* xr = x + (size_t)src * n;
     int8_t* qr = q + (size_t)r * n;
@@ -117,20 +119,18 @@ __global__ void __launch_bounds__(256) k_normquant(const int32_t* __restrict__ x
     }
     ss = block_sum_i64(ss, (i64*)redu);
     az = block_max_u64(az, redu);
-    if (tid == 0) {
+    if (tid < 32) {
         i64 eps_s;
         if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (eps >> (2 * sig));
         else eps_s = eps * (1LL << (-2 * sig));
-        u64 ms = (u64)((ss >> lg_n) + eps_s);
-        u64 rr = isqrt_u64(ms);
-        int e;
-        u64 R = quant_mult(az, &e);
+        const u64 rr = warp_isqrt64((u64)((ss >> lg_n) + eps_s));
         int m, k;
-        dyadic_dev(az, 127ull * rr, &m, &k);
-        mt[r] = m;
-        kt[r] = k + 12;
-        bc[0] = (i64)R;
-        bc[1] = e;
+        warp_dyadic(az, 127ull * rr, &m, &k);
+        if (tid == 0) { mt[r] = m; kt[r] = k + 12; }
+    } else if (tid < 64) {
+        const int e = bitlen_u64(az);
+        const u64 R = warp_udiv64(127ull << (e + 16), az);
+        if (tid == 32) { bc[0] = (i64)R; bc[1] = e; }
     }
     __syncthreads();
     const i64 R = bc[0];
@@ -150,6 +150,8 @@ __global__ void __launch_bounds__(256) k_actquant(const int32_t* __restrict__ x,
     __shared__ u64 redu[8];
     __shared__ i64 bc[2];
     const int r = blockIdx.x, tid = threadIdx.x;
+    pdl_launch();
+    pdl_wait();
     const int32_t* xr = x + (size_t)r * n;
     int8_t* qr = q + (size_t)r * n;
     u64 a = 0;
@@ -160,15 +162,14 @@ __global__ void __launch_bounds__(256) k_actquant(const int32_t* __restrict__ x,
         if (tid == 0) { mt[r] = 0; kt[r] = 0; }
         return;
     }
-    if (tid == 0) {
-        int e;
-        u64 R = quant_mult(a, &e);
+    if (tid < 32) {
+        const int e = bitlen_u64(a);
+        const u64 R = warp_udiv64(127ull << (e + 16), a);
+        if (tid == 0) { bc[0] = (i64)R; bc[1] = e; }
+    } else if (tid < 64) {
         int m, k;
-        dyadic_dev(a, 127ull, &m, &k);
-        mt[r] = m;
-        kt[r] = k + F;
-        bc[0] = (i64)R;
-        bc[1] = e;
+        warp_dyadic(a, 127ull, &m, &k);
+        if (tid == 32) { mt[r] = m; kt[r] = k + F; }
     }
     __syncthreads();
     const i64 R = bc[0];
@@ -199,45 +200,58 @@ __device__ void qk_norm_warp(i64 (&y)[EPL], const int16_t* gamma, int lane, int 
 #pragma unroll
     for (int j = 0; j < EPL; ++j) { xp[j] = norm24(y[j], sig); ss += xp[j] * xp[j]; }
     ss = warp_sum_i64(ss);
-    i64 rr = 0, Rr = 0;
-    if (lane == 0) {
-        i64 eps_s;
-        if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (eps >> (2 * sig));
-        else eps_s = eps * (1LL << (-2 * sig));
-        rr = (i64)isqrt_u64((u64)((ss >> lg_d) + eps_s));
-        Rr = (i64)udiv64(1ull << (bitlen_u64((u64)rr) + 23), (u64)rr);
-    }
-    rr = warp_bcast_i64(rr);
-    Rr = warp_bcast_i64(Rr);
+    i64 eps_s;
+    if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (eps >> (2 * sig));
+    else eps_s = eps * (1LL << (-2 * sig));
+    const i64 rr = (i64)warp_isqrt64((u64)((ss >> lg_d) + eps_s));
+    const i64 Rr = (i64)warp_udiv64(1ull << (bitlen_u64((u64)rr) + 23), (u64)rr);
     const int sh = bitlen_u64((u64)rr) + 21;
 #pragma unroll
     for (int j = 0; j < EPL; ++j) y[j] = rshr(xp[j] * (i64)gamma[lane + 32 * j] * Rr, sh);
 }
 
 // one warp: q head `slot` (< nq; q8 to q_dst, scale to mq_dst/kq_dst) or kv
-// head `slot - nq` (K/V written into the paged cache) of token t
+// head `slot - nq` (K/V written into the paged cache) of token t;
+// cr/sr: RoPE row of this token's position, kvp: its kv head's parameters,
+// gq/gk: QK-norm gammas (global or shared memory)
+template <int EPL>
+__device__ void qkv_head_p(const QkvPostArgs& a, int t, int slot, int8_t* q_dst, int32_t* mq_dst,
+                           int32_t* kq_dst, const int16_t* cr, const int16_t* sr,
+                           const int32_t* kvp, const int16_t* gq, const int16_t* gk);
+
 template <int EPL>
 __device__ void qkv_head(const QkvPostArgs& a, int t, int slot, int8_t* q_dst, int32_t* mq_dst,
                          int32_t* kq_dst) {
+    const int dh2 = a.d >> 1;
+    const int pos = a.tok_pos[t];
+    const int kvh = slot < a.nq ? (slot >> a.lg_grp) : (slot - a.nq);
+    qkv_head_p<EPL>(a, t, slot, q_dst, mq_dst, kq_dst, a.rope_cos + (size_t)pos * dh2,
+                    a.rope_sin + (size_t)pos * dh2, a.kvp + (size_t)kvh * (8 + dh2), a.q_gamma,
+                    a.k_gamma);
+}
+
+template <int EPL>
+__device__ void qkv_head_p(const QkvPostArgs& a, int t, int slot, int8_t* q_dst, int32_t* mq_dst,
+                           int32_t* kq_dst, const int16_t* cr, const int16_t* sr,
+                           const int32_t* kvp, const int16_t* gq, const int16_t* gk) {
     const int lane = threadIdx.x & 31;
     const int nq = a.nq, nkv = a.nkv, d = a.d, dh2 = d >> 1;
     const int lg_d = (EPL == 4) ? 7 : 6;
     const int nqkv = (nq + 2 * nkv) * d;
     const int pos = a.tok_pos[t];
-    const int16_t* cr = a.rope_cos + (size_t)pos * dh2;
-    const int16_t* sr = a.rope_sin + (size_t)pos * dh2;
     const int32_t* row = a.qkv + (size_t)t * nqkv;
     const int kvh = slot < nq ? (slot >> a.lg_grp) : (slot - nq);
-    const int32_t* kvp = a.kvp + (size_t)kvh * (8 + dh2);
     int E = 0;
-    for (int i = 0; i < dh2; ++i) E = max(E, kvp[8 + i]);
+    for (int i = lane; i < dh2; i += 32) E = max(E, kvp[8 + i]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) E = max(E, __shfl_xor_sync(0xffffffffu, E, o));
 
     i64 y[EPL];
     const int base = slot < nq ? slot * d : (nq + kvh) * d;
 #pragma unroll
     for (int j = 0; j < EPL; ++j) y[j] = row[base + lane + 32 * j];
     if (a.qk_norm) {
-        qk_norm_warp<EPL>(y, slot < nq ? a.q_gamma : a.k_gamma, lane, lg_d, a.eps_qk);
+        qk_norm_warp<EPL>(y, slot < nq ? gq : gk, lane, lg_d, a.eps_qk);
     } else {
 #pragma unroll
         for (int j = 0; j < EPL; ++j) y[j] *= 4;
@@ -269,18 +283,14 @@ __device__ void qkv_head(const QkvPostArgs& a, int t, int slot, int8_t* q_dst, i
             if (lane == 0) { *mq_dst = 0; *kq_dst = 0; }
             return;
         }
-        i64 R = 0, e = 0;
+        const int e = bitlen_u64(am);
+        const i64 R = (i64)warp_udiv64(127ull << (e + 16), am);
+        int m, k;
+        warp_dyadic(am, 127ull, &m, &k);
         if (lane == 0) {
-            int ee;
-            R = (i64)quant_mult(am, &ee);
-            e = ee;
-            int m, k;
-            dyadic_dev(am, 127ull, &m, &k);
             *mq_dst = m;
             *kq_dst = k + 14;
         }
-        R = warp_bcast_i64(R);
-        e = warp_bcast_i64(e);
 #pragma unroll
         for (int j = 0; j < EPL; ++j) qo[lane + 32 * j] = (int8_t)rshr(y[j] * R, (int)e + 16);
     } else {
@@ -432,12 +442,13 @@ __device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs
             }
         }
         __syncthreads();
-        if (tid < G) {
+        if ((tid >> 5) < G) {
+            const int hh = tid >> 5;
             i64 v = 0;
-            for (int w2 = 0; w2 < 8; ++w2) v += red[w2 * MAXG + tid];
-            sig_s[tid] = v;
+            for (int w2 = 0; w2 < 8; ++w2) v += red[w2 * MAXG + hh];
             const int bl = bitlen_u64((u64)v);
-            rs_s[tid] = (i64)udiv64(1ull << (bl + 23), (u64)v);
+            const i64 rs = (i64)warp_udiv64(1ull << (bl + 23), (u64)v);
+            if ((tid & 31) == 0) { sig_s[hh] = v; rs_s[hh] = rs; }
         }
         __syncthreads();
     }
@@ -519,10 +530,46 @@ __global__ void __launch_bounds__(256) k_attn_decode(AttnArgs a, QkvPostArgs qa)
     __shared__ int32_t mqs[MAXG], kqs[MAXG];
     const int t = blockIdx.x, g = blockIdx.y, w = threadIdx.x >> 5;
     const int G = 1 << a.lg_grp;
+    const int dh2 = a.d >> 1;
     int8_t* qs = (int8_t*)sm;
+    // RoPE row, QK-norm gammas and this kv head's parameters never depend on
+    // the previous kernel: stage them in shared memory before the wait (the
+    // position is this sequence's length before the step)
+    __shared__ __align__(16) int16_t s_cos[64], s_sin[64], s_gq[128], s_gk[128];
+    __shared__ int32_t s_kvp[8 + 64];
+    {
+        const int p0 = a.seq_len[a.tok_seq[t]];
+        const int tid = threadIdx.x;
+        if (tid < dh2) {
+            s_cos[tid] = qa.rope_cos[(size_t)p0 * dh2 + tid];
+            s_sin[tid] = qa.rope_sin[(size_t)p0 * dh2 + tid];
+        }
+        if (tid < a.d) { s_gq[tid] = qa.q_gamma[tid]; s_gk[tid] = qa.k_gamma[tid]; }
+        if (tid < 8 + dh2) s_kvp[tid] = qa.kvp[(size_t)g * (8 + dh2) + tid];
+    }
+    {
+        // positions before this step's token were written by earlier steps
+        // (earlier graph launches), so their cache blocks can be pulled into
+        // L2 before the wait; the sequence length is read from the same
+        // completed state
+        const int seq = a.tok_seq[t];
+        const int ctx = a.seq_len[seq];
+        const int nb = (ctx + KV_BLK) >> 6;
+        const size_t blk_bytes = (size_t)KV_BLK * a.d;
+        for (int b = threadIdx.x; b < nb; b += 256) {
+            const int blk = a.block_table[(size_t)seq * a.mbs + b];
+            const size_t off = ((size_t)blk * a.nkv + g) * blk_bytes;
+            prefetch_l2(a.kc + off, (uint32_t)blk_bytes);
+            prefetch_l2(a.vc + off, (uint32_t)blk_bytes);
+        }
+    }
     pdl_wait();
-    if (w < G) qkv_head<EPL>(qa, t, (g << a.lg_grp) + w, qs + w * a.d, &mqs[w], &kqs[w]);
-    else if (w == G) qkv_head<EPL>(qa, t, a.nq + g, nullptr, nullptr, nullptr);
+    __syncthreads();
+    if (w < G)
+        qkv_head_p<EPL>(qa, t, (g << a.lg_grp) + w, qs + w * a.d, &mqs[w], &kqs[w], s_cos, s_sin,
+                        s_kvp, s_gq, s_gk);
+    else if (w == G)
+        qkv_head_p<EPL>(qa, t, a.nq + g, nullptr, nullptr, nullptr, s_cos, s_sin, s_kvp, s_gq, s_gk);
     __syncthreads();
     pdl_launch();
     attention_core(a, t, g, qs, mqs, kqs, sm);

@@ -50,10 +50,10 @@ cudaError_t launch_embed(const int32_t* tokens, int T, const int32_t* tok_seq, i
 
 cudaError_t launch_normquant(const int32_t* x, const int32_t* rows, int R, int n,
                              const int16_t* gamma, long long eps, int8_t* q, int32_t* mt,
-                             int32_t* kt, cudaStream_t s);
+                             int32_t* kt, cudaStream_t s, bool pdl = false);
 
 cudaError_t launch_actquant(const int32_t* x, int R, int n, int F, int8_t* q, int32_t* mt,
-                            int32_t* kt, cudaStream_t s);
+                            int32_t* kt, cudaStream_t s, bool pdl = false);
 
 struct QkvPostArgs {
     const int32_t* qkv;      // [T][(nq + 2 nkv) d] Q12
@@ -91,17 +91,20 @@ struct AttnArgs {
     int32_t* o;              // [T][nq d] Q12
     int T, nq, nkv, d, lg_grp;
     int ctx_cap;             // keys that fit the shared-memory row
+    const int32_t* seq_len;  // decode: lengths before this step (L2 prefetch only)
 };
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 size_t attention_smem_bytes(int grp, int d, int ctx_cap);
 
 // streaming decode GEMV (M <= 8) with a fused quantisation prologue:
-// pro 1 = NormQuant(xin rows, gamma, eps), 2 = ActQuant(xin rows, F).
+// pro 1 = NormQuant(xin rows, gamma, eps), 2 = ActQuant(xin rows, F),
+// 0 = rows already quantised (x8 [M][K] with scales mt/kt).
 // Returns cudaErrorNotSupported when the shape does not fit (the caller
 // then uses the separate row kernels and launch_gemv).
 cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xin,
                          const int32_t* rows, const int16_t* gamma, long long eps, int F, int pro,
-                         int mode, const Epi& ep, cudaStream_t s);
+                         int mode, const Epi& ep, cudaStream_t s, const int8_t* x8 = nullptr,
+                         const int32_t* mt = nullptr, const int32_t* kt = nullptr);
 // decode attention fused with the QKV post-processing (one token per sequence)
 cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s);
 

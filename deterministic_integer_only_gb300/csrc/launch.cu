@@ -77,15 +77,22 @@ cudaError_t launch_embed(const int32_t* tokens, int T, const int32_t* tok_seq, i
 
 static int ilog2(int n) { int l = 0; while ((1 << l) < n) ++l; return l; }
 
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args);
+
 cudaError_t launch_normquant(const int32_t* x, const int32_t* rows, int R, int n,
                              const int16_t* gamma, long long eps, int8_t* q, int32_t* mt,
-                             int32_t* kt, cudaStream_t s) {
+                             int32_t* kt, cudaStream_t s, bool pdl) {
+    if (pdl) return launch_pdl(k_normquant, dim3(R), dim3(256), 0, s, x, rows, n, ilog2(n), gamma,
+                               (i64)eps, q, mt, kt);
     k_normquant<<<R, 256, 0, s>>>(x, rows, n, ilog2(n), gamma, eps, q, mt, kt);
     return cudaGetLastError();
 }
 
 cudaError_t launch_actquant(const int32_t* x, int R, int n, int F, int8_t* q, int32_t* mt,
-                            int32_t* kt, cudaStream_t s) {
+                            int32_t* kt, cudaStream_t s, bool pdl) {
+    if (pdl) return launch_pdl(k_actquant, dim3(R), dim3(256), 0, s, x, n, F, q, mt, kt);
     k_actquant<<<R, 256, 0, s>>>(x, n, F, q, mt, kt);
     return cudaGetLastError();
 }
@@ -110,6 +117,10 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t s, Args... args) {
+#ifdef DETINT_NO_PDL
+    kern<<<grid, block, smem, s>>>(args...);
+    return cudaGetLastError();
+#endif
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -135,13 +146,17 @@ cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int ro
 static int g_num_sms = 0;
 
 static size_t sgemv_smem(int K, int KC) {
-    return (size_t)SG_STAGES * 16 * (KC + 64) + (size_t)8 * (K + 64) + 8 * 16 * 8 * 4;
+    // ring + int8 activation tile + partial tiles + gamma copy + preloaded
+    // residual (256 int32) + weight-channel scales (256 int32)
+    return (size_t)SG_STAGES * 16 * (KC + 64) + (size_t)8 * (K + 64) + (size_t)SG_GB * 8 * 16 * 8 * 4 +
+           (size_t)2 * K + 2048;
 }
-constexpr size_t SG_SMEM_MAX = 160 * 1024;
+constexpr size_t SG_SMEM_MAX = 176 * 1024;
 
 cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xin,
                          const int32_t* rows, const int16_t* gamma, long long eps, int F, int pro,
-                         int mode, const Epi& ep, cudaStream_t s) {
+                         int mode, const Epi& ep, cudaStream_t s, const int8_t* x8,
+                         const int32_t* mt, const int32_t* kt) {
     if (M < 1 || M > 8 || N < 1 || K < 64 || (K & 63)) return cudaErrorNotSupported;
     const int KC = K <= 1024 ? K : 1024;
     if (K % KC) return cudaErrorNotSupported;
@@ -150,7 +165,8 @@ cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xi
     if (smem > SG_SMEM_MAX) return cudaErrorNotSupported;
     SgArgs a{};
     a.W = W; a.N = N; a.K = K; a.KC = KC; a.nkc = K / KC; a.M = M; a.xin = xin; a.rows = rows;
-    a.gamma = gamma; a.eps = eps; a.F = F; a.pro = pro; a.ep = ep;
+    a.gamma = gamma; a.eps = eps; a.F = F; a.pro = pro; a.mode = mode; a.ep = ep;
+    a.x8 = x8; a.mt_in = mt; a.kt_in = kt;
     int lg = 0;
     while ((1 << lg) < K) ++lg;
     a.lg_k = lg;
@@ -158,12 +174,10 @@ cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xi
     const int ncta = G < g_num_sms ? G : g_num_sms;
     a.rg_q = G / ncta;
     a.rg_r = G % ncta;
-    const dim3 grid(ncta), block(SG_THREADS);
-    if (pro == PRO_NORMQUANT && mode == EPI_QKV) return launch_pdl(k_sgemv<PRO_NORMQUANT, EPI_QKV>, grid, block, smem, s, a);
-    if (pro == PRO_ACTQUANT && mode == EPI_RESADD) return launch_pdl(k_sgemv<PRO_ACTQUANT, EPI_RESADD>, grid, block, smem, s, a);
-    if (pro == PRO_NORMQUANT && mode == EPI_SWIGLU) return launch_pdl(k_sgemv<PRO_NORMQUANT, EPI_SWIGLU>, grid, block, smem, s, a);
-    if (pro == PRO_NORMQUANT && mode == EPI_LOGITS) return launch_pdl(k_sgemv<PRO_NORMQUANT, EPI_LOGITS>, grid, block, smem, s, a);
-    return cudaErrorNotSupported;
+    if (pro != PRO_NORMQUANT && pro != PRO_ACTQUANT && pro != PRO_NONE) return cudaErrorNotSupported;
+    if (mode != EPI_QKV && mode != EPI_RESADD && mode != EPI_SWIGLU && mode != EPI_LOGITS)
+        return cudaErrorNotSupported;
+    return launch_pdl(k_sgemv, dim3(ncta), dim3(SG_THREADS), smem, s, a);
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s) {
@@ -245,10 +259,7 @@ cudaError_t kernels_init() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attn_decode<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     const int sgm = (int)SG_SMEM_MAX;
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_NORMQUANT, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_ACTQUANT, EPI_RESADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_NORMQUANT, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<PRO_NORMQUANT, EPI_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RESADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);

@@ -232,6 +232,20 @@ static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32
                             int32_t* next_tok, cudaStream_t s) {
     const int H = m->H, d = m->d, nq = m->nq, nkv = m->nkv, F = m->F;
     const int nqkv = (nq + 2 * nkv) * d;
+    // from 3 sequences on, each row is quantised once by a row kernel (one CTA
+    // per row) instead of redundantly by every GEMV CTA
+    const bool sep = T >= 3;
+    auto gemv = [&](const int8_t* W, int N, int K, const int32_t* xin, const int16_t* gamma, int F_in,
+                    int pro, int mode, const Epi& e) -> int {
+        if (sep) {
+            if (pro == 1) CK(launch_normquant(xin, nullptr, T, K, gamma, m->eps_h, m->x8, m->mt, m->kt, s, true));
+            else CK(launch_actquant(xin, T, K, F_in, m->x8, m->mt, m->kt, s, true));
+            CK(launch_sgemv(W, N, K, T, nullptr, nullptr, nullptr, 0, 0, 0, mode, e, s, m->x8, m->mt, m->kt));
+        } else {
+            CK(launch_sgemv(W, N, K, T, xin, nullptr, gamma, m->eps_h, F_in, pro, mode, e, s));
+        }
+        return DETINT_OK;
+    };
     CK(launch_embed(tokens, T, m->tok_seq, m->tok_pos, m->seq_len_dev, 1, m->max_ctx,
                     m->embed, m->embed_m, H, m->V, m->h, m->status, s));
     for (int l = 0; l < m->L; ++l) {
@@ -239,7 +253,8 @@ static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32
         Epi e{};
         e.status = m->status;
         e.out = m->qkv; e.ldo = nqkv; e.mc = w.m_qkv; e.fout = 12;
-        CK(launch_sgemv(w.w_qkv, nqkv, H, T, m->h, nullptr, w.attn_gamma, m->eps_h, 0, 1, EPI_QKV, e, s));
+        int rc = gemv(w.w_qkv, nqkv, H, m->h, w.attn_gamma, 0, 1, EPI_QKV, e);
+        if (rc) return rc;
         QkvPostArgs qa{};
         qa.qkv = m->qkv; qa.q_gamma = w.q_gamma; qa.k_gamma = w.k_gamma; qa.qk_norm = m->qk_norm;
         qa.eps_qk = m->eps_qk; qa.rope_cos = m->rope_cos; qa.rope_sin = m->rope_sin; qa.kvp = w.kvp;
@@ -251,19 +266,21 @@ static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32
         aa.kc = qa.kc; aa.vc = qa.vc; aa.block_table = m->block_table; aa.mbs = m->mbs;
         aa.tok_seq = m->tok_seq; aa.tok_pos = m->tok_pos; aa.kvp = w.kvp; aa.o = m->o; aa.T = T;
         aa.nq = nq; aa.nkv = nkv; aa.d = d; aa.lg_grp = m->lg_grp; aa.ctx_cap = m->ctx_cap;
+        aa.seq_len = m->seq_len_dev;
         CK(launch_attn_decode(aa, qa, s));
         e.out = m->h; e.ldo = H; e.mc = w.m_o; e.fout = 16;
-        CK(launch_sgemv(w.w_o, H, nq * d, T, m->o, nullptr, nullptr, 0, 12, 2, EPI_RESADD, e, s));
+        if ((rc = gemv(w.w_o, H, nq * d, m->o, nullptr, 12, 2, EPI_RESADD, e))) return rc;
         e.out = m->sbuf; e.ldo = F; e.mc = w.m_gu; e.fout = 12;
-        CK(launch_sgemv(w.w_gu, 2 * F, H, T, m->h, nullptr, w.ffn_gamma, m->eps_h, 0, 1, EPI_SWIGLU, e, s));
+        if ((rc = gemv(w.w_gu, 2 * F, H, m->h, w.ffn_gamma, 0, 1, EPI_SWIGLU, e))) return rc;
         e.out = m->h; e.ldo = H; e.mc = w.m_d; e.fout = 16;
-        CK(launch_sgemv(w.w_d, H, F, T, m->sbuf, nullptr, nullptr, 0, 10, 2, EPI_RESADD, e, s));
+        if ((rc = gemv(w.w_d, H, F, m->sbuf, nullptr, 10, 2, EPI_RESADD, e))) return rc;
     }
     Epi e{};
     e.status = m->status;
     e.out = logits ? logits : m->logits_int; e.ldo = m->V; e.mc = m->embed_m; e.fout = 16;
     e.pval = m->pval; e.pidx = m->pidx; e.npart = m->npart;
-    CK(launch_sgemv(m->embed, m->V, H, T, m->h, nullptr, m->final_gamma, m->eps_h, 0, 1, EPI_LOGITS, e, s));
+    int rc = gemv(m->embed, m->V, H, m->h, m->final_gamma, 0, 1, EPI_LOGITS, e);
+    if (rc) return rc;
     CK(launch_argmax_final(m->pval, m->pidx, T, m->npart, next_tok, m->tok_seq, m->seq_len_dev, s, true));
     return DETINT_OK;
 }
@@ -277,8 +294,8 @@ static bool decode_fusable(const detint_model* m, int T) {
         if (K & 63) return false;
         const int KC = K <= 1024 ? K : 1024;
         if (K % KC) return false;
-        const size_t smem = (size_t)4 * 16 * (KC + 64) + (size_t)8 * (K + 64) + 4096;
-        if (smem > 160 * 1024) return false;
+        const size_t smem = (size_t)4 * 16 * (KC + 64) + (size_t)8 * (K + 64) + 16384 + 2 * K + 2048;
+        if (smem > 176 * 1024) return false;
     }
     // one warp per q head of a kv group plus one for the K/V head
     return ((m->H & (m->H - 1)) == 0) && nkv >= 1 && (1 << m->lg_grp) < 8;

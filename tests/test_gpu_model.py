@@ -158,3 +158,17 @@ def test_qwen_batch8_row0_equals_batch1(torch_cuda, qwen_artifact):
     t8, h8 = m.generate([prompt] + cos, 24, keep_logits="hash")
     assert np.array_equal(t8[0], t1[0]) and h8[0] == h1[0]
     m.close()
+
+
+@pytest.mark.parametrize("B", [2, 3, 5])
+def test_tiny_batch_sizes_match_oracle(torch_cuda, tiny_artifact, B):
+    """Decode batches of 2 (quantisation fused into the GEMV prologue) and of
+    3 or 5 (rows quantised by the row kernels) agree with the oracle."""
+    prompts = [synth.prompt_ids(7, i, 10 + 4 * i, 1024) for i in range(B)]
+    m = _load(tiny_artifact, B, 64)
+    toks, rows = m.generate(prompts, 6)
+    for b in (0, B - 1):
+        ot, orows = _oracle_run(tiny_artifact, prompts[b], 6, 64)
+        assert np.array_equal(toks[b], ot)
+        assert all(np.array_equal(rows[s][b], orows[s]) for s in range(6))
+    m.close()
