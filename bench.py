@@ -151,6 +151,122 @@ def cpu_baseline(seconds: float = 12.0):
                       f"(~{seconds:.0f} s of CPU work)"}
 
 
+# int8 tensor-pipe peak of this GPU: mma.sync m16n8k32 s8, measured with a
+# register-only issue loop on a GB300 (measurement)
+MMA_S8_PEAK_TOPS = 150.3
+
+
+def run_prefill(args):
+    """Prefill throughput: 4 sequences x 4096 seeded tokens on the Qwen3-0.6B
+    shape in one detint_prefill call (last-position logits per sequence)."""
+    import torch
+    import synth
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+    B, L = 4, 4096
+    path = synth.ensure_artifact(SHAPE, SEED)
+    model = pkg.Model(path, max_batch=B, max_ctx=L)
+    dev = torch.device("cuda")
+    prompts = [synth.prompt_ids(SEED, 200 + i, L, model.vocab) for i in range(B)]
+    flat = torch.tensor(np.concatenate(prompts), dtype=torch.int32, device=dev)
+    cu = np.arange(B + 1) * L
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    s = model.stream
+    times = []
+    for it in range(args.warmup + args.steps):
+        for sid in range(B):
+            model.reset_seq(sid)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            model.prefill(list(range(B)), flat, cu, None, tok)
+            e1.record(s)
+        s.synchronize()
+        if it >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    ms = float(np.median(times))
+    H, F, nq, nkv, d, Lyr = model.hidden, model.ffn, model.n_q, model.n_kv, model.head_dim, model.n_layers
+    gemm_ops = 2.0 * B * L * Lyr * ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F)
+    attn_ops = 2.0 * B * Lyr * nq * d * (L * (L + 1) / 2) * 3    # QK^T + two E.V limbs, causal
+    line = {"metric": "prefill tok/s (Qwen3-0.6B shape, 4 x 4096)", "value": B * L / (ms / 1e3),
+            "unit": "tok/s", "ms": ms, "steps": args.steps, "warmup": args.warmup,
+            "gemm_tops": gemm_ops / (ms / 1e3) / 1e12, "attn_ops_T": attn_ops / 1e12,
+            "gemm_ops_T": gemm_ops / 1e12, "dtype": "int8/int32", "data": "synthetic"}
+    print(json.dumps(line), flush=True)
+    model.close()
+
+
+def _graph_time(fn, stream, n):
+    """Milliseconds per call of fn (a CUDA launch on `stream`), timed as one
+    CUDA-graph replay of n captured calls so host overhead cannot leak in."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(n):
+            fn()
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def run_lmhead(args):
+    """The dominant decode kernel alone (streaming GEMV at the lm_head shape,
+    151936 x 1024, M = --batch), for profiler captures."""
+    import torch
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+    dev = torch.device("cuda")
+    W = torch.randint(-127, 128, (151936, 1024), dtype=torch.int8, device=dev)
+    X = torch.randint(-127, 128, (args.batch, 1024), dtype=torch.int8, device=dev)
+    C = torch.empty((args.batch, 151936), dtype=torch.int32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        pkg.detint_gemm_i8(X, W, C)
+    torch.cuda.synchronize()
+    print(json.dumps({"workload": "lmhead", "launches": args.warmup + args.steps}), flush=True)
+
+
+def run_gemm_sweep(args):
+    """Exact int8 GEMM (detint_gemm_i8) over M x (N, K) of the Llama-3.2-1B
+    projections: TOPS = 2MNK/t and bytes = MK + NK + 4MN per launch."""
+    import torch
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+    peak_gbs, _ = _peaks()
+    dev = torch.device("cuda")
+    s = torch.cuda.Stream()
+    rows = []
+    for (N, K) in [(2048, 2048), (512, 2048), (3072, 2048), (16384, 2048), (2048, 8192), (128256, 2048)]:
+        W = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev)
+        for M in [1, 8, 64, 512, 4096]:
+            A = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev)
+            C = torch.empty((M, N), dtype=torch.int32, device=dev)
+            n = max(3, min(50, int(2e9 / max(1, M * N * K))))
+            t = _graph_time(lambda: pkg.detint_gemm_i8(A, W, C, stream=s), s, n) / 1e3
+            ops = 2.0 * M * N * K
+            byt = M * K + N * K + 4 * M * N
+            rows.append({"M": M, "N": N, "K": K, "us": t * 1e6, "tops": ops / t / 1e12,
+                         "gbs": byt / t / 1e9, "hbm_frac": byt / t / 1e9 / peak_gbs})
+            del A, C
+        del W
+    print(json.dumps({"metric": "int8 GEMM sweep (Llama-3.2-1B shapes)", "unit": "TOPS",
+                      "mma_s8_peak_tops": MMA_S8_PEAK_TOPS, "hbm_peak_gbs": peak_gbs,
+                      "sweep": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -159,9 +275,18 @@ def main():
     ap.add_argument("--impl", default="detint", choices=["detint", "reference"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "gemm", "lmhead"],
+                    help="decode (the headline line), prefill (4 x 4096 prompt throughput) or "
+                         "gemm (exact int8 GEMM sweep over the Llama-3.2-1B projection shapes)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "prefill":
+        return run_prefill(args)
+    if args.workload == "gemm":
+        return run_gemm_sweep(args)
+    if args.workload == "lmhead":
+        return run_lmhead(args)
 
     import torch
     import synth
@@ -250,21 +375,10 @@ def main():
     wmat = torch.randint(-127, 128, (V, H), dtype=torch.int8, device=dev)
     xmat = torch.randint(-127, 128, (B, H), dtype=torch.int8, device=dev)
     cmat = torch.empty((B, V), dtype=torch.int32, device=dev)
-    with torch.cuda.stream(s):
-        for _ in range(3):
-            pkg.detint_gemm_i8(xmat, wmat, cmat, stream=s)
-        r0 = torch.cuda.Event(enable_timing=True)
-        r1 = torch.cuda.Event(enable_timing=True)
-        nrep = 50
-        r0.record(s)
-        for _ in range(nrep):
-            pkg.detint_gemm_i8(xmat, wmat, cmat, stream=s)
-        r1.record(s)
-    s.synchronize()
-    kms = r0.elapsed_time(r1) / nrep
+    kms = _graph_time(lambda: pkg.detint_gemm_i8(xmat, wmat, cmat, stream=s), s, 50)
     kbytes = V * H + B * H + 4 * B * V
     achieved = kbytes / (kms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "k_gemv<1,EPI_RAW> (lm_head shape 151936x1024, B=%d)" % B,
+    roofline = {"bound": "hbm", "kernel": "k_sgemv (decode streaming GEMV), lm_head shape 151936x1024, M=%d" % B,
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": kbytes,
                 "us_per_launch": kms * 1e3}

@@ -19,7 +19,7 @@
 
 namespace detint {
 
-constexpr int SG_STAGES = 4;
+constexpr int SG_STAGES = 8;           // most ring stages (the launch picks 4 or 8)
 constexpr int SG_THREADS = 288;      // 8 compute warps + 1 producer warp
 
 enum { PRO_NONE = 0, PRO_NORMQUANT = 1, PRO_ACTQUANT = 2 };
@@ -42,6 +42,7 @@ struct SgArgs {
     const int32_t* kt_in;
     int mode;                 // EPI_QKV, EPI_RESADD, EPI_SWIGLU or EPI_LOGITS
     int rg_q, rg_r;           // CTA c owns rg_q + (c < rg_r) row groups
+    int lg_ns;                // log2 of the ring stages used (2 or 3)
     Epi ep;
 };
 
@@ -53,7 +54,7 @@ struct SgShared {
     long long bc[8][2];        // per-row quantisation multiplier and shift
 };
 
-__device__ __forceinline__ size_t sg_ring_bytes(int KC) { return (size_t)SG_STAGES * 16 * (KC + 64); }
+__device__ __forceinline__ size_t sg_ring_bytes(int KC, int ns) { return (size_t)ns * 16 * (KC + 64); }
 
 // ---- prologue: one group of (8 / Mp) warps per token row quantises it into
 // the int8 tile. The row is read once; up to SG_NV 16-byte vectors per thread
@@ -211,8 +212,8 @@ __device__ void sg_load_x8(const SgArgs& a, SgShared& sh, int8_t* xs, int XP) {
             *(int4*)(xs + (size_t)r * XP + v * 16) = val;
         }
     if (tid < 8) {
-        sh.mt[tid] = tid < a.M ? a.mt_in[tid] : 0;
-        sh.kt[tid] = tid < a.M ? a.kt_in[tid] : 0;
+        sh.mt[tid] = (tid < a.M && a.mt_in) ? a.mt_in[tid] : 0;
+        sh.kt[tid] = (tid < a.M && a.kt_in) ? a.kt_in[tid] : 0;
     }
 }
 
@@ -227,8 +228,9 @@ __device__ __forceinline__ i64 sg_requant(int acc, const SgShared& sh, const Epi
 
 // epilogue of nb row groups starting at group gb, from the per-warp partial
 // tiles red[b][warp][16 rows][8 tokens]
+// nw: partial tiles per group to add (8 for the mma path, 1 for dp4a)
 __device__ void sg_epilogue(const SgArgs& a, const SgShared& sh, int32_t* red, int gb, int nb,
-                            const int32_t* hold, int g0, const int32_t* mcs) {
+                            const int32_t* hold, int g0, const int32_t* mcs, int nw) {
     const int nbase = g0 * 16;
     const int tid = threadIdx.x;
     const Epi& ep = a.ep;
@@ -237,8 +239,7 @@ __device__ void sg_epilogue(const SgArgs& a, const SgShared& sh, int32_t* red, i
             const int b = it >> 6, p = (it >> 3) & 7, tk = it & 7;
             const int32_t* rb = red + b * 1024;
             int sg = 0, su = 0;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
+            for (int w = 0; w < nw; ++w) {
                 sg += rb[w * 128 + (2 * p) * 8 + tk];
                 su += rb[w * 128 + (2 * p + 1) * 8 + tk];
             }
@@ -258,10 +259,13 @@ __device__ void sg_epilogue(const SgArgs& a, const SgShared& sh, int32_t* red, i
         const int b = it >> 7, rr = (it >> 3) & 15, tk = it & 7;
         const int32_t* rb = red + b * 1024;
         int sum = 0;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) sum += rb[w * 128 + (it & 127)];
+        for (int w = 0; w < nw; ++w) sum += rb[w * 128 + (it & 127)];
         const int n = (gb + b) * 16 + rr;
         int outv = -2147483647;
+        if (a.mode == EPI_RAW) {
+            if (tk < a.M && n < a.N) ep.out[(size_t)tk * ep.ldo + n] = sum;
+            continue;
+        }
         if (tk < a.M && n < a.N) {
             const i64 y = sg_requant(sum, sh, ep, tk, n, mcs, nbase);
             if (a.mode == EPI_QKV) {
@@ -305,10 +309,14 @@ __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ SgShared sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int P = a.KC + 64;                      // ring row pitch (bank-conflict-free pairs)
+    // ring row pitch: a whole 16-row group arrives in one bulk copy when the
+    // rows are not chunked (pitch K); chunked rows get a 64-byte pad so
+    // fragment loads of neighbouring rows fall in different banks
+    const int P = a.nkc == 1 ? a.K : a.KC + 64;
     const int XP = a.K + 64;                      // activation row pitch
     unsigned char* ring = smem;
-    int8_t* xs = (int8_t*)(smem + sg_ring_bytes(a.KC));
+    const int NS = 1 << a.lg_ns;
+    int8_t* xs = (int8_t*)(smem + sg_ring_bytes(a.KC, NS));
     int32_t* red = (int32_t*)(xs + (size_t)8 * XP);     // [SG_GB][8 warps][16][8]
     const int c = blockIdx.x;
     const int g0 = c * a.rg_q + min(c, a.rg_r);
@@ -316,7 +324,7 @@ __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
     const int units = (g1 - g0) * a.nkc;
 
     if (tid == 0) {
-        for (int s = 0; s < SG_STAGES; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
             mbar_init(smem_u32(&sh.empty[s]), 8);
         }
@@ -330,21 +338,32 @@ __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
         int u = 0;
         for (int g = g0; g < g1; ++g) {
             for (int kc = 0; kc < a.nkc; ++kc, ++u) {
-                const int s = u & (SG_STAGES - 1);
-                if (u >= SG_STAGES && lane == 0) {
+                const int s = u & (NS - 1);
+                if (u >= NS && lane == 0) {
                     // bounded: on a timeout the status word records it and the
                     // stream continues (results are then invalid, nothing hangs)
-                    if (!mbar_wait(smem_u32(&sh.empty[s]), ((u >> 2) - 1) & 1))
+                    if (!mbar_wait(smem_u32(&sh.empty[s]), ((u >> a.lg_ns) - 1) & 1))
                         a.ep.status[ST_TIMEOUT] = 1;
                 }
                 __syncwarp();
                 const uint32_t fb = smem_u32(&sh.full[s]);
-                if (lane == 0) mbar_arrive_expect_tx(fb, 16u * a.KC);
-                __syncwarp();
-                if (lane < 16) {
-                    const int row = min(g * 16 + lane, a.N - 1);
-                    bulk_g2s(smem_u32(ring + ((size_t)s * 16 + lane) * P),
-                             a.W + (size_t)row * a.K + (size_t)kc * a.KC, a.KC, fb);
+                if (a.nkc == 1) {
+                    // the group's rows are contiguous: one copy (the last group
+                    // may hold fewer than 16 rows; its missing rows are never stored)
+                    const int rows = min(16, a.N - g * 16);
+                    const uint32_t bytes = (uint32_t)rows * (uint32_t)a.K;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(fb, bytes);
+                        bulk_g2s(smem_u32(ring + (size_t)s * 16 * P), a.W + (size_t)g * 16 * a.K, bytes, fb);
+                    }
+                } else {
+                    if (lane == 0) mbar_arrive_expect_tx(fb, 16u * a.KC);
+                    __syncwarp();
+                    if (lane < 16) {
+                        const int row = min(g * 16 + lane, a.N - 1);
+                        bulk_g2s(smem_u32(ring + ((size_t)s * 16 + lane) * P),
+                                 a.W + (size_t)row * a.K + (size_t)kc * a.KC, a.KC, fb);
+                    }
                 }
             }
         }
@@ -358,7 +377,7 @@ __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
         for (int i = tid * 8; i < a.K; i += 256 * 8) *(int4*)(gam + i) = *(const int4*)(a.gamma + i);
     int32_t* hold = (int32_t*)(gam + a.K);
     int32_t* mcs = hold + 256;
-    const bool mc_pre = (g1 - g0) * 16 <= 256;
+    const bool mc_pre = a.ep.mc && (g1 - g0) * 16 <= 256;
     if (mc_pre && tid < (g1 - g0) * 16) mcs[tid] = a.ep.mc[min(g0 * 16 + tid, a.N - 1)];
     pdl_wait();
     // residual add: issue the loads of this CTA's old residual values now so
@@ -376,14 +395,89 @@ __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
 
     const int g = lane >> 2, tq = lane & 3;
     const int nch = a.KC >> 6;
+    // up to 4 tokens: dp4a on the integer pipe (one multiply per weight per
+    // token); more: mma.sync m16n8k32 over 8 token columns. On sm_103a both
+    // run at the same int8 rate, so the m16n8 tile's unused columns would
+    // cost up to 8x the integer work at one token.
+    const bool dp = a.M <= 4;
     int u = 0;
     for (int gb = g0; gb < g1; gb += SG_GB) {
         const int nb = min(SG_GB, g1 - gb);
+        if (dp) {
+            // a half-warp per weight row: thread t of the half reads 16-byte
+            // chunks t, t+16, ... of the row's K-chunk and the same chunks of
+            // each token's activations; a 4-step shuffle sums the half. Each
+            // 32-bit word lane of a chunk has its own accumulator and the
+            // chunk loads are issued before any multiply, so the dp4a
+            // latencies overlap instead of forming one dependent chain.
+            const int r = tid >> 4, hl = tid & 15;
+            const int nc = a.KC >> 4;                 // 16-byte chunks per row chunk
+            for (int b = 0; b < nb; ++b) {
+                int acc[4][4];
+#pragma unroll
+                for (int tk = 0; tk < 4; ++tk) acc[tk][0] = acc[tk][1] = acc[tk][2] = acc[tk][3] = 0;
+                for (int kc = 0; kc < a.nkc; ++kc, ++u) {
+                    const int s = u & (NS - 1);
+                    if (!mbar_wait(smem_u32(&sh.full[s]), (u >> a.lg_ns) & 1)) a.ep.status[ST_TIMEOUT] = 1;
+                    const unsigned char* wr = ring + ((size_t)s * 16 + r) * P;
+                    const int8_t* xk = xs + (size_t)kc * a.KC;
+                    for (int c0 = hl; c0 < nc; c0 += 64) {
+                        int4 w[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            w[j] = (c0 + 16 * j < nc) ? *(const int4*)(wr + (c0 + 16 * j) * 16) : make_int4(0, 0, 0, 0);
+#pragma unroll
+                        for (int tk = 0; tk < 4; ++tk) {
+                            if (tk < a.M) {
+                                int4 xv[4];
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    xv[j] = (c0 + 16 * j < nc)
+                                                ? *(const int4*)(xk + (size_t)tk * XP + (c0 + 16 * j) * 16)
+                                                : make_int4(0, 0, 0, 0);
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    acc[tk][0] = __dp4a(w[j].x, xv[j].x, acc[tk][0]);
+                                    acc[tk][1] = __dp4a(w[j].y, xv[j].y, acc[tk][1]);
+                                    acc[tk][2] = __dp4a(w[j].z, xv[j].z, acc[tk][2]);
+                                    acc[tk][3] = __dp4a(w[j].w, xv[j].w, acc[tk][3]);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
+                }
+                int tot[4];
+#pragma unroll
+                for (int tk = 0; tk < 4; ++tk) {
+                    int v = (acc[tk][0] + acc[tk][1]) + (acc[tk][2] + acc[tk][3]);
+                    if (tk < a.M) {
+                        v += __shfl_xor_sync(0xffffffffu, v, 8);
+                        v += __shfl_xor_sync(0xffffffffu, v, 4);
+                        v += __shfl_xor_sync(0xffffffffu, v, 2);
+                        v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    }
+                    tot[tk] = v;
+                }
+                if (hl < 8) {
+                    int v = 0;
+#pragma unroll
+                    for (int tk = 0; tk < 4; ++tk)
+                        if (hl == tk && tk < a.M) v = tot[tk];
+                    red[b * 1024 + r * 8 + hl] = v;
+                }
+            }
+            bar_named(1, 256);
+            sg_epilogue(a, sh, red, gb, nb, pre ? hold : nullptr, g0, mc_pre ? mcs : nullptr, 1);
+            bar_named(1, 256);
+            continue;
+        }
         for (int b = 0; b < nb; ++b) {
-            int acc[4] = {0, 0, 0, 0};
+            int acc[4] = {0, 0, 0, 0}, acc2[4] = {0, 0, 0, 0};
             for (int kc = 0; kc < a.nkc; ++kc, ++u) {
-                const int s = u & (SG_STAGES - 1);
-                if (!mbar_wait(smem_u32(&sh.full[s]), (u >> 2) & 1)) a.ep.status[ST_TIMEOUT] = 1;
+                const int s = u & (NS - 1);
+                if (!mbar_wait(smem_u32(&sh.full[s]), (u >> a.lg_ns) & 1)) a.ep.status[ST_TIMEOUT] = 1;
                 const int8_t* st = (const int8_t*)ring + (size_t)s * 16 * P;
                 const int8_t* wlo = st + g * P + 16 * tq;
                 const int8_t* whi = wlo + 8 * P;
@@ -393,11 +487,13 @@ __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
                     const int4 ah = *(const int4*)(whi + ch * 64);
                     const int4 bx = *(const int4*)(xb + ch * 64);
                     mma_s8(acc, al.x, ah.x, al.y, ah.y, bx.x, bx.y);
-                    mma_s8(acc, al.z, ah.z, al.w, ah.w, bx.z, bx.w);
+                    mma_s8(acc2, al.z, ah.z, al.w, ah.w, bx.z, bx.w);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] += acc2[q];
             // accumulator fragment: c0 (row g, tok 2tq), c1, c2 (row g+8), c3
             int32_t* rw = red + b * 1024 + warp * 128;
             rw[g * 8 + 2 * tq] = acc[0];
@@ -406,15 +502,15 @@ __global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
             rw[(g + 8) * 8 + 2 * tq + 1] = acc[3];
         }
         bar_named(1, 256);
-        sg_epilogue(a, sh, red, gb, nb, pre ? hold : nullptr, g0, mc_pre ? mcs : nullptr);
+        sg_epilogue(a, sh, red, gb, nb, pre ? hold : nullptr, g0, mc_pre ? mcs : nullptr, 8);
         bar_named(1, 256);
     }
     // every issued copy has completed before the CTA exits (bounded wait;
     // normally these phases completed long ago)
     if (tid == 0) {
-        for (int s = 0; s < SG_STAGES && s < units; ++s) {
-            const int ul = s + ((units - 1 - s) >> 2) * SG_STAGES;   // last unit on stage s
-            if (!mbar_wait(smem_u32(&sh.full[s]), (ul >> 2) & 1)) a.ep.status[ST_TIMEOUT] = 1;
+        for (int s = 0; s < NS && s < units; ++s) {
+            const int ul = s + ((units - 1 - s) >> a.lg_ns) * NS;    // last unit on stage s
+            if (!mbar_wait(smem_u32(&sh.full[s]), (ul >> a.lg_ns) & 1)) a.ep.status[ST_TIMEOUT] = 1;
         }
     }
 }

@@ -23,6 +23,11 @@ __device__ __forceinline__ u64 warp_max_u64(u64 v) {
     for (int o = 16; o; o >>= 1) v = umax64(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
+__device__ __forceinline__ int warp_sum_i32(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
 __device__ __forceinline__ i64 warp_sum_i64(i64 v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -104,7 +104,8 @@ size_t attention_smem_bytes(int grp, int d, int ctx_cap);
 cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xin,
                          const int32_t* rows, const int16_t* gamma, long long eps, int F, int pro,
                          int mode, const Epi& ep, cudaStream_t s, const int8_t* x8 = nullptr,
-                         const int32_t* mt = nullptr, const int32_t* kt = nullptr);
+                         const int32_t* mt = nullptr, const int32_t* kt = nullptr,
+                         bool pdl = true);   // pdl: W is immutable (streamed before the wait)
 // decode attention fused with the QKV post-processing (one token per sequence)
 cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s);
 

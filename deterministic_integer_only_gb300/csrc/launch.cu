@@ -145,38 +145,55 @@ cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int ro
 
 static int g_num_sms = 0;
 
-static size_t sgemv_smem(int K, int KC) {
+static size_t sgemv_smem(int K, int KC, int ns) {
     // ring + int8 activation tile + partial tiles + gamma copy + preloaded
     // residual (256 int32) + weight-channel scales (256 int32)
-    return (size_t)SG_STAGES * 16 * (KC + 64) + (size_t)8 * (K + 64) + (size_t)SG_GB * 8 * 16 * 8 * 4 +
+    return (size_t)ns * 16 * (KC + 64) + (size_t)8 * (K + 64) + (size_t)SG_GB * 8 * 16 * 8 * 4 +
            (size_t)2 * K + 2048;
 }
-constexpr size_t SG_SMEM_MAX = 176 * 1024;
+constexpr size_t SG_SMEM_MAX = 200 * 1024;
 
 cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xin,
                          const int32_t* rows, const int16_t* gamma, long long eps, int F, int pro,
                          int mode, const Epi& ep, cudaStream_t s, const int8_t* x8,
-                         const int32_t* mt, const int32_t* kt) {
+                         const int32_t* mt, const int32_t* kt, bool pdl) {
     if (M < 1 || M > 8 || N < 1 || K < 64 || (K & 63)) return cudaErrorNotSupported;
     const int KC = K <= 1024 ? K : 1024;
     if (K % KC) return cudaErrorNotSupported;
     if (pro == PRO_NORMQUANT && (K & (K - 1))) return cudaErrorNotSupported;
-    const size_t smem = sgemv_smem(K, KC);
+    // long streams (many 16-row units per CTA): two CTAs per SM, each with a
+    // 4-stage ring, so one CTA's consumer latency overlaps the other's and
+    // twice the bytes are in flight; short ones: one CTA per SM (the next
+    // kernel's CTA takes the other slot while this one drains)
+    const int G0 = (N + 15) / 16;
+    const int units_per_cta = ((G0 + g_num_sms - 1) / g_num_sms) * (K / KC);
+    int lg_ns = 2, cta_per_sm = 1;
+    size_t smem = sgemv_smem(K, KC, 4);
+    if (units_per_cta > 4) {
+        if (smem <= 113 * 1024) cta_per_sm = 2;
+        else if (sgemv_smem(K, KC, 8) <= SG_SMEM_MAX) { lg_ns = 3; smem = sgemv_smem(K, KC, 8); }
+    }
     if (smem > SG_SMEM_MAX) return cudaErrorNotSupported;
     SgArgs a{};
     a.W = W; a.N = N; a.K = K; a.KC = KC; a.nkc = K / KC; a.M = M; a.xin = xin; a.rows = rows;
     a.gamma = gamma; a.eps = eps; a.F = F; a.pro = pro; a.mode = mode; a.ep = ep;
-    a.x8 = x8; a.mt_in = mt; a.kt_in = kt;
+    a.x8 = x8; a.mt_in = mt; a.kt_in = kt; a.lg_ns = lg_ns;
     int lg = 0;
     while ((1 << lg) < K) ++lg;
     a.lg_k = lg;
     const int G = (N + 15) / 16;
-    const int ncta = G < g_num_sms ? G : g_num_sms;
+    const int ncta = G < g_num_sms * cta_per_sm ? G : g_num_sms * cta_per_sm;
     a.rg_q = G / ncta;
     a.rg_r = G % ncta;
     if (pro != PRO_NORMQUANT && pro != PRO_ACTQUANT && pro != PRO_NONE) return cudaErrorNotSupported;
-    if (mode != EPI_QKV && mode != EPI_RESADD && mode != EPI_SWIGLU && mode != EPI_LOGITS)
+    if (mode != EPI_QKV && mode != EPI_RESADD && mode != EPI_SWIGLU && mode != EPI_LOGITS &&
+        !(mode == EPI_RAW && pro == PRO_NONE))
         return cudaErrorNotSupported;
+    if (!pdl) {
+        // the weights may come from the previous kernel: plain stream order
+        k_sgemv<<<ncta, SG_THREADS, smem, s>>>(a);
+        return cudaGetLastError();
+    }
     return launch_pdl(k_sgemv, dim3(ncta), dim3(SG_THREADS), smem, s, a);
 }
 

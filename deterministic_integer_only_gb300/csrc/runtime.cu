@@ -295,7 +295,7 @@ static bool decode_fusable(const detint_model* m, int T) {
         const int KC = K <= 1024 ? K : 1024;
         if (K % KC) return false;
         const size_t smem = (size_t)4 * 16 * (KC + 64) + (size_t)8 * (K + 64) + 16384 + 2 * K + 2048;
-        if (smem > 176 * 1024) return false;
+        if (smem > 200 * 1024) return false;
     }
     // one warp per q head of a kv group plus one for the K/V head
     return ((m->H & (m->H - 1)) == 0) && nkv >= 1 && (1 << m->lg_grp) < 8;
@@ -665,6 +665,15 @@ int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, i
     }
     Epi e{};
     e.out = C; e.ldo = N;
+    // up to 8 rows: the streaming decode GEMV (weights through the bulk-TMA
+    // ring); up to 32: the register-streaming GEMV; beyond: the tiled GEMM
+    if (M <= 8) {
+        cudaError_t ce = launch_sgemv(B, N, K, M, nullptr, nullptr, nullptr, 0, 0, 0, EPI_RAW, e, s,
+                                      A, nullptr, nullptr, false);
+        if (ce == cudaSuccess) return DETINT_OK;
+        if (ce != cudaErrorNotSupported) return fail(DETINT_E_CUDA, cudaGetErrorString(ce));
+        cudaGetLastError();
+    }
     if (M <= 32 && (K % 64) == 0) { CK(launch_gemv(B, A, M, N, K, EPI_RAW, e, s)); }
     else { CK(launch_gemm(A, B, M, N, K, EPI_RAW, e, s)); }
     return DETINT_OK;
