@@ -222,16 +222,18 @@ def _graph_time(fn, stream, n):
 
 
 def run_lmhead(args):
-    """The dominant decode kernel alone (streaming GEMV at the lm_head shape,
-    151936 x 1024, M = --batch), for profiler captures."""
+    """One exact GEMM shape launched repeatedly (default: the dominant decode
+    kernel, the streaming GEMV at the lm_head shape 151936 x 1024 with
+    M = --batch), for profiler captures."""
     import torch
     from deterministic_integer_only_gb300 import build
     build.build()
     import deterministic_integer_only_gb300 as pkg
     dev = torch.device("cuda")
-    W = torch.randint(-127, 128, (151936, 1024), dtype=torch.int8, device=dev)
-    X = torch.randint(-127, 128, (args.batch, 1024), dtype=torch.int8, device=dev)
-    C = torch.empty((args.batch, 151936), dtype=torch.int32, device=dev)
+    M, N, K = (args.batch, 151936, 1024) if not args.shape else [int(v) for v in args.shape.split(",")]
+    W = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev)
+    X = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev)
+    C = torch.empty((M, N), dtype=torch.int32, device=dev)
     for _ in range(args.warmup + args.steps):
         pkg.detint_gemm_i8(X, W, C)
     torch.cuda.synchronize()
@@ -275,6 +277,8 @@ def main():
     ap.add_argument("--impl", default="detint", choices=["detint", "reference"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default=None, help="M,N,K for --workload lmhead (default 1,151936,1024 "
+                    "with M = --batch)")
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "gemm", "lmhead"],
                     help="decode (the headline line), prefill (4 x 4096 prompt throughput) or "
                          "gemm (exact int8 GEMM sweep over the Llama-3.2-1B projection shapes)")
@@ -375,13 +379,28 @@ def main():
     wmat = torch.randint(-127, 128, (V, H), dtype=torch.int8, device=dev)
     xmat = torch.randint(-127, 128, (B, H), dtype=torch.int8, device=dev)
     cmat = torch.empty((B, V), dtype=torch.int32, device=dev)
-    kms = _graph_time(lambda: pkg.detint_gemm_i8(xmat, wmat, cmat, stream=s), s, 50)
+    # cold-L2 time per launch: each launch follows a 256 MB write that evicts
+    # the 129 MB L2 (graph of flush+launch minus graph of flush alone), as it
+    # is inside a decode step where 440 MB of other weights pass in between
+    flush = torch.empty(256 << 20, dtype=torch.int8, device=dev)
+
+    def _flush():
+        flush.fill_(1)
+
+    def _both():
+        _flush()
+        pkg.detint_gemm_i8(xmat, wmat, cmat, stream=s)
+
+    kms = _graph_time(_both, s, 20) - _graph_time(_flush, s, 20)
+    kms_warm = _graph_time(lambda: pkg.detint_gemm_i8(xmat, wmat, cmat, stream=s), s, 50)
+    del flush
     kbytes = V * H + B * H + 4 * B * V
     achieved = kbytes / (kms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": "k_sgemv (decode streaming GEMV), lm_head shape 151936x1024, M=%d" % B,
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": kbytes,
-                "us_per_launch": kms * 1e3}
+                "us_per_launch": kms * 1e3, "us_per_launch_l2_warm": kms_warm * 1e3,
+                "timing": "CUDA events around graph replays; L2 evicted before every launch"}
     # whole-step roofline: algorithmic bytes of one decode step
     L, nq, nkv, d, F = model.n_layers, model.n_q, model.n_kv, model.head_dim, model.ffn
     wbytes = L * ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F) + V * H
