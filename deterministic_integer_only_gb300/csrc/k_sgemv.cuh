@@ -305,7 +305,9 @@ __device__ void sg_epilogue(const SgArgs& a, const SgShared& sh, int32_t* red, i
     }
 }
 
-__global__ void __launch_bounds__(SG_THREADS, 1) k_sgemv(SgArgs a) {
+// MINB = 2: the long-stream variant (two CTAs per SM, registers capped to fit)
+template <int MINB>
+__global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ SgShared sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

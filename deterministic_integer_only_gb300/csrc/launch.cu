@@ -191,10 +191,12 @@ cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xi
         return cudaErrorNotSupported;
     if (!pdl) {
         // the weights may come from the previous kernel: plain stream order
-        k_sgemv<<<ncta, SG_THREADS, smem, s>>>(a);
+        if (cta_per_sm == 2) k_sgemv<2><<<ncta, SG_THREADS, smem, s>>>(a);
+        else k_sgemv<1><<<ncta, SG_THREADS, smem, s>>>(a);
         return cudaGetLastError();
     }
-    return launch_pdl(k_sgemv, dim3(ncta), dim3(SG_THREADS), smem, s, a);
+    if (cta_per_sm == 2) return launch_pdl(k_sgemv<2>, dim3(ncta), dim3(SG_THREADS), smem, s, a);
+    return launch_pdl(k_sgemv<1>, dim3(ncta), dim3(SG_THREADS), smem, s, a);
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s) {
@@ -276,7 +278,8 @@ cudaError_t kernels_init() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attn_decode<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     const int sgm = (int)SG_SMEM_MAX;
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RESADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
