@@ -23,3 +23,9 @@ def tiny_artifact():
 def qwen_artifact():
     import synth
     return synth.ensure_artifact("qwen3-0.6b", 0)
+
+
+@pytest.fixture(scope="session")
+def llama_artifact():
+    import synth
+    return synth.ensure_artifact("llama-1b", 0)
