@@ -760,6 +760,7 @@ __global__ void __launch_bounds__(256) k_gemv(const int8_t* __restrict__ W,
 }  // namespace detint
 #include "k_sgemv.cuh"
 #include "k_gemm.cuh"
+#include "k_attn_prefill.cuh"
 namespace detint {
 
 // ----------------------------------------------------------- argmax (a11)

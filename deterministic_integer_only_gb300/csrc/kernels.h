@@ -1,5 +1,6 @@
 // Host-side launchers of the detint CUDA kernels (internal to the library).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -108,6 +109,30 @@ cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xi
                          bool pdl = true);   // pdl: W is immutable (streamed before the wait)
 // decode attention fused with the QKV post-processing (one token per sequence)
 cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s);
+
+// prefill attention on the int8 tensor pipe: one CTA per (query block, kv
+// head); a query block is up to 64 / G consecutive tokens of one sequence
+struct PfArgs {
+    const int8_t* q8;          // [T][nq][d]
+    const int32_t* mq;         // [T][nq]
+    const int32_t* kq;
+    const int32_t* block_table;
+    int mbs;
+    const int32_t* qblk;       // [nqb][4]: first token, tokens, sequence, first position
+    int nqb;
+    const int32_t* kvp;        // [nkv][8 + d/2]
+    int32_t* o;                // [T][nq d] Q12
+    int nq, nkv, lg_grp;
+    int krow0, vrow0;          // this layer's first row in the K / V^T cache maps
+    int32_t* status;
+};
+// tensor maps over the whole K cache ([units * 64][d] bytes) and V^T cache
+// ([units * d][64] bytes), units = layers * blocks * kv heads
+cudaError_t make_kv_maps(CUtensorMap* kmap, CUtensorMap* vmap, const int8_t* kc,
+                         const int8_t* vc, long long units, int d);
+cudaError_t launch_attn_prefill(const PfArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                int d, cudaStream_t s);
+constexpr int PF_ROWS = 64;   // query rows (token x q head) per prefill attention CTA
 
 cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int rows, int npart,
                                 int32_t* next_tok, const int32_t* tok_seq, int32_t* seq_len,

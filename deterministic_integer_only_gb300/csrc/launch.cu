@@ -2,6 +2,7 @@
 // attributes, programmatic dependent launch. Kernel code lives in the
 // .cuh files.
 #include <cudaTypedefs.h>
+#include <algorithm>
 
 #include "kernels.cuh"
 
@@ -257,6 +258,54 @@ cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, i
     return cudaGetLastError();
 }
 
+cudaError_t make_kv_maps(CUtensorMap* kmap, CUtensorMap* vmap, const int8_t* kc, const int8_t* vc,
+                         long long units, int d) {
+    if ((d != 64 && d != 128) || units < 1 || units * 128 > 2147483647LL) return cudaErrorInvalidValue;
+    if (((uintptr_t)kc & 15) || ((uintptr_t)vc & 15)) return cudaErrorInvalidValue;
+    cudaError_t e = get_encode();
+    if (e != cudaSuccess) return e;
+    const cuuint32_t estr[2] = {1, 1};
+    // K: rows of d bytes, a 64-key box; the swizzle span equals the row
+    cuuint64_t kdims[2] = {(cuuint64_t)d, (cuuint64_t)units * 64};
+    cuuint64_t kstr[1] = {(cuuint64_t)d};
+    cuuint32_t kbox[2] = {(cuuint32_t)d, 64};
+    CUresult r = g_encode(kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(kc), kdims, kstr,
+                          kbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // V^T: rows of 64 key bytes, a d-channel box
+    cuuint64_t vdims[2] = {64, (cuuint64_t)units * d};
+    cuuint64_t vstr[1] = {64};
+    cuuint32_t vbox[2] = {64, (cuuint32_t)d};
+    r = g_encode(vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(vc), vdims, vstr, vbox, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_prefill(const PfArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                int d, cudaStream_t s) {
+    if (a.lg_grp > 6 || a.nqb < 1) return cudaErrorInvalidValue;
+    // grid x: kv heads (fastest, so the heaviest query blocks of every head
+    // start first), grid y: query blocks in chunks of at most 65535
+    for (int b0 = 0; b0 < a.nqb; b0 += 65535) {
+        PfArgs c = a;
+        c.qblk = a.qblk + 4 * (size_t)b0;
+        c.nqb = std::min(65535, a.nqb - b0);
+        const dim3 grid(a.nkv, c.nqb);
+        if (d == 128)
+            k_attn_prefill<128><<<grid, PF_THREADS, PfCfg<128>::SMEM, s>>>(kmap, vmap, c);
+        else if (d == 64)
+            k_attn_prefill<64><<<grid, PF_THREADS, PfCfg<64>::SMEM, s>>>(kmap, vmap, c);
+        else
+            return cudaErrorInvalidValue;
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 template <int MODE>
 static cudaError_t gemv_attr_all() {
     cudaError_t e = gemv_attr<1, MODE>();
@@ -284,6 +333,8 @@ cudaError_t kernels_init() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RESADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<128>::SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_prefill<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<64>::SMEM);
     int dev = 0;
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);

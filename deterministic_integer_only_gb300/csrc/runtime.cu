@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <array>
 #include <map>
 #include <mutex>
 #include <string>
@@ -137,6 +138,11 @@ struct detint_model {
     int32_t* status = nullptr;
     int use_graph = 1;
     int fused_decode = 1;    // 0: decode through the separate row kernels (tests compare both)
+    int tc_prefill = 1;      // 0: prefill attention through the per-token kernel (tests compare both)
+    int pf_ok = 0;           // the tensor-core prefill attention supports this shape
+    CUtensorMap kmap, vmap;  // whole K / V^T caches for the prefill attention
+    int32_t* qblk = nullptr; // prefill query blocks [Tcap + max_batch][4]
+    int nqb = 0;
     std::map<std::string, GraphEntry> graphs;
     int32_t* pinned = nullptr;       // host staging for small copies
     size_t pinned_elems = 0;
@@ -200,7 +206,8 @@ static int ensure_scratch(detint_model* m, int T) {
            o_ts = take((size_t)Tn * 4), o_tp = take((size_t)Tn * 4), o_rows = take((size_t)Tn * 4),
            o_x8 = take((size_t)Tn * wmax), o_q8 = take((size_t)Tn * m->nq * m->d),
            o_pv = take((size_t)rows_out * m->npart * 4), o_pi = take((size_t)rows_out * m->npart * 4),
-           o_lg = take((size_t)rows_out * m->V * 4);
+           o_lg = take((size_t)rows_out * m->V * 4),
+           o_qb = take((size_t)(Tn + m->max_batch) * 16);
     cudaError_t e = cudaMalloc(&m->scratch, off);
     if (e != cudaSuccess) { m->scratch = nullptr; m->Tcap = 0; return fail(DETINT_E_OOM, "scratch allocation failed"); }
     unsigned char* b = m->scratch;
@@ -210,6 +217,7 @@ static int ensure_scratch(detint_model* m, int T) {
     m->tok_pos = (int32_t*)(b + o_tp); m->rows = (int32_t*)(b + o_rows);
     m->x8 = (int8_t*)(b + o_x8); m->q8 = (int8_t*)(b + o_q8);
     m->pval = (int32_t*)(b + o_pv); m->pidx = (int32_t*)(b + o_pi); m->logits_int = (int32_t*)(b + o_lg);
+    m->qblk = (int32_t*)(b + o_qb);
     m->Tcap = Tn;
     return DETINT_OK;
 }
@@ -330,7 +338,18 @@ static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode
         aa.block_table = m->block_table; aa.mbs = m->mbs; aa.tok_seq = m->tok_seq;
         aa.tok_pos = m->tok_pos; aa.kvp = w.kvp; aa.o = m->o; aa.T = T; aa.nq = nq; aa.nkv = nkv;
         aa.d = d; aa.lg_grp = m->lg_grp; aa.ctx_cap = m->ctx_cap;
-        CK(launch_attention(aa, s));
+        if (!decode && m->pf_ok && m->tc_prefill) {
+            PfArgs pa{};
+            pa.q8 = m->q8; pa.mq = m->mq; pa.kq = m->kq; pa.block_table = m->block_table;
+            pa.mbs = m->mbs; pa.qblk = m->qblk; pa.nqb = m->nqb; pa.kvp = w.kvp; pa.o = m->o;
+            pa.nq = nq; pa.nkv = nkv; pa.lg_grp = m->lg_grp;
+            pa.krow0 = (int)((long long)l * m->nblocks * nkv * KV_BLK);
+            pa.vrow0 = (int)((long long)l * m->nblocks * nkv * d);
+            pa.status = m->status;
+            CK(launch_attn_prefill(pa, m->kmap, m->vmap, d, s));
+        } else {
+            CK(launch_attention(aa, s));
+        }
         CK(launch_actquant(m->o, T, nq * d, 12, m->x8, m->mt, m->kt, s));
         e.out = m->h; e.ldo = H; e.mc = w.m_o; e.fout = 16;
         CK(gemm_epi(m->x8, w.w_o, T, H, nq * d, EPI_RESADD, e, s));
@@ -545,6 +564,10 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
     if (ce == cudaSuccess) ce = cudaMemset(m->vcache, 0, m->kv_layer_elems * m->L);
     if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
     m->seq_len.assign(max_batch, 0);
+    // the tensor-core prefill attention takes head_dim 64 or 128 and up to 64 q heads per kv head
+    m->pf_ok = (d == 64 || d == 128) && m->lg_grp <= 6 &&
+               make_kv_maps(&m->kmap, &m->vmap, m->kcache, m->vcache,
+                            (long long)m->L * m->nblocks * nkv, d) == cudaSuccess;
     int rc = ensure_scratch(m, std::max(64, max_batch));
     if (rc != DETINT_OK) { detint_free(m); return rc; }
     ce = kernels_init();
@@ -592,7 +615,24 @@ int detint_prefill(detint_model* m, int n_seq, const int32_t* seq_ids, const int
     }
     std::vector<int32_t> newlen(m->seq_len.begin(), m->seq_len.end());
     for (int i = 0; i < n_seq; ++i) newlen[seq_ids[i]] += cu_lens[i + 1] - cu_lens[i];
-    rc = stage_copies(m, s, {{m->tok_seq, &ts}, {m->tok_pos, &tp}, {m->rows, &rows}});
+    // query blocks of up to 64 / G tokens of one sequence, the longest key
+    // ranges first so that the heaviest CTAs start first
+    const int bq = PF_ROWS >> m->lg_grp;
+    std::vector<std::array<int32_t, 4>> blocks;
+    for (int i = 0; i < n_seq; ++i) {
+        const int sid = seq_ids[i];
+        for (int j = cu_lens[i]; j < cu_lens[i + 1]; j += bq)
+            blocks.push_back({j, std::min(bq, cu_lens[i + 1] - j), sid, m->seq_len[sid] + (j - cu_lens[i])});
+    }
+    std::stable_sort(blocks.begin(), blocks.end(), [](const std::array<int32_t, 4>& x,
+                                                      const std::array<int32_t, 4>& y) {
+        return x[3] + x[1] > y[3] + y[1];
+    });
+    std::vector<int32_t> qb(blocks.size() * 4);
+    for (size_t b = 0; b < blocks.size(); ++b)
+        for (int k = 0; k < 4; ++k) qb[4 * b + k] = blocks[b][k];
+    m->nqb = (int)blocks.size();
+    rc = stage_copies(m, s, {{m->tok_seq, &ts}, {m->tok_pos, &tp}, {m->rows, &rows}, {m->qblk, &qb}});
     if (rc) return rc;
     rc = run_forward(m, T, tokens, 0, n_seq, m->rows, logits, next_tok, s);
     if (rc) return rc;
@@ -718,6 +758,7 @@ int detint_set_option(detint_model* m, int option, int value) {
     if (!m || (value != 0 && value != 1)) return fail(DETINT_E_ARG, "bad argument");
     if (option == DETINT_OPT_GRAPH) m->use_graph = value;
     else if (option == DETINT_OPT_FUSED_DECODE) { m->fused_decode = value; free_graphs(m); }
+    else if (option == DETINT_OPT_TC_PREFILL) m->tc_prefill = value;
     else return fail(DETINT_E_ARG, "unknown option");
     return DETINT_OK;
 }

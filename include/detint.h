@@ -133,11 +133,13 @@ int detint_status(detint_model* m, int32_t* flags, detint_stream_t s);
 int detint_set_graph(detint_model* m, int enable);
 
 /* Options: DETINT_OPT_GRAPH (1 = replay decode steps as CUDA graphs, the
- * default; same as detint_set_graph) and DETINT_OPT_FUSED_DECODE (1 = decode
+ * default; same as detint_set_graph), DETINT_OPT_FUSED_DECODE (1 = decode
  * batches of up to 8 sequences through the fused streaming kernels, the
- * default; 0 = through the separate row kernels). Both settings give
- * bit-identical results. Errors: ARG. */
-enum { DETINT_OPT_GRAPH = 0, DETINT_OPT_FUSED_DECODE = 1 };
+ * default; 0 = through the separate row kernels) and DETINT_OPT_TC_PREFILL
+ * (1 = prefill attention on the int8 tensor pipe in two sweeps over the keys,
+ * the default where head_dim is 64 or 128; 0 = the per-token attention
+ * kernel). Every setting gives bit-identical results. Errors: ARG. */
+enum { DETINT_OPT_GRAPH = 0, DETINT_OPT_FUSED_DECODE = 1, DETINT_OPT_TC_PREFILL = 2 };
 int detint_set_option(detint_model* m, int option, int value);
 
 /* Shape of the loaded model: info[0..9] = n_layers, hidden, n_q, n_kv,
