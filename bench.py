@@ -164,7 +164,7 @@ def run_prefill(args):
     from deterministic_integer_only_gb300 import build
     build.build()
     import deterministic_integer_only_gb300 as pkg
-    B, L = 4, 4096
+    B, L = args.prefill_seqs, args.prefill_len
     path = synth.ensure_artifact(SHAPE, SEED)
     model = pkg.Model(path, max_batch=B, max_ctx=L)
     dev = torch.device("cuda")
@@ -190,7 +190,7 @@ def run_prefill(args):
     H, F, nq, nkv, d, Lyr = model.hidden, model.ffn, model.n_q, model.n_kv, model.head_dim, model.n_layers
     gemm_ops = 2.0 * B * L * Lyr * ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F)
     attn_ops = 2.0 * B * Lyr * nq * d * (L * (L + 1) / 2) * 3    # QK^T + two E.V limbs, causal
-    line = {"metric": "prefill tok/s (Qwen3-0.6B shape, 4 x 4096)", "value": B * L / (ms / 1e3),
+    line = {"metric": f"prefill tok/s (Qwen3-0.6B shape, {B} x {L})", "value": B * L / (ms / 1e3),
             "unit": "tok/s", "ms": ms, "steps": args.steps, "warmup": args.warmup,
             "gemm_tops": gemm_ops / (ms / 1e3) / 1e12, "attn_ops_T": attn_ops / 1e12,
             "gemm_ops_T": gemm_ops / 1e12, "dtype": "int8/int32", "data": "synthetic"}
@@ -279,6 +279,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default=None, help="M,N,K for --workload lmhead (default 1,151936,1024 "
                     "with M = --batch)")
+    ap.add_argument("--prefill-seqs", type=int, default=4, help="prefill workload: sequences")
+    ap.add_argument("--prefill-len", type=int, default=4096, help="prefill workload: tokens each")
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "gemm", "lmhead"],
                     help="decode (the headline line), prefill (4 x 4096 prompt throughput) or "
                          "gemm (exact int8 GEMM sweep over the Llama-3.2-1B projection shapes)")

@@ -97,14 +97,13 @@ __device__ __forceinline__ u64 quant_mult(u64 a, int* e_out) {
     return udiv64(127ull << (e + 16), a);
 }
 
-// one SwiGLU channel from saturated Q12 gate/up values (Q10 result)
-__device__ __forceinline__ int swiglu_dev(int g, int u) {
-    i64 ag = g < 0 ? -(i64)g : (i64)g;
-    i64 z = rshr(ag * 47274LL, 17);
-    int Ez = exp2q_dev(-z);
+// Q15 sigmoid of the SwiGLU gate from z = Q10 of |g| log2 e: with
+// D = 2^15 + exp2q(-z), round(2^30 / D) = floor((2^31 + D) / 2D) <= 2^15,
+// = 2^15 only for D = 2^15 (every z > 23552); otherwise 15 quotient bits by
+// restoring division in 32 bits
+__device__ __forceinline__ unsigned sigmoid_q15(i64 z) {
+    const int Ez = exp2q_dev(-z);
     const unsigned D = 32768u + (unsigned)Ez;            // [2^15, 2^16]
-    // round(2^30 / D) = floor((2^31 + D) / 2D) <= 2^15, and = 2^15 only for
-    // D = 2^15; otherwise 15 quotient bits by restoring division in 32 bits
     unsigned q = 32768u;
     if (D != 32768u) {
         unsigned num = 0x80000000u + D, dd = D << 15;   // 2D * 2^14 < 2^32
@@ -116,9 +115,23 @@ __device__ __forceinline__ int swiglu_dev(int g, int u) {
             dd >>= 1;
         }
     }
-    i64 sg = g >= 0 ? (i64)q : 32768LL - (i64)q;
-    i64 silu = rshr((i64)g * sg, 15);
+    return q;
+}
+
+__device__ __forceinline__ i64 swiglu_z(int g) {
+    const i64 ag = g < 0 ? -(i64)g : (i64)g;
+    return rshr(ag * 47274LL, 17);
+}
+
+__device__ __forceinline__ int swiglu_finish(int g, int u, unsigned q) {
+    const i64 sg = g >= 0 ? (i64)q : 32768LL - (i64)q;
+    const i64 silu = rshr((i64)g * sg, 15);
     return sat32(rshr(silu * (i64)u, 14));
+}
+
+// one SwiGLU channel from saturated Q12 gate/up values (Q10 result)
+__device__ __forceinline__ int swiglu_dev(int g, int u) {
+    return swiglu_finish(g, u, sigmoid_q15(swiglu_z(g)));
 }
 
 // ------------------------------------------------ warp-cooperative forms

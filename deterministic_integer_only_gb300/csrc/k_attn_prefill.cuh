@@ -259,14 +259,24 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         const uint32_t tV = tK + C::KT;
 #pragma unroll
-        for (int n = 0; n < NT2; ++n) {
-            // matrices: 16-key chunks 0..3 of channels c .. c + 7
-            int v0, v1, v2, v3;
-            ldsm_x4(tV + pf_voff(hf * (D >> 1) + n * 8 + ri, mi), v0, v1, v2, v3);
-            mma_s8(accH[n], ah[0][0], ah[0][1], ah[0][2], ah[0][3], v0, v1);
-            mma_s8(accH[n], ah[1][0], ah[1][1], ah[1][2], ah[1][3], v2, v3);
-            mma_u8s8(accL[n], al[0][0], al[0][1], al[0][2], al[0][3], v0, v1);
-            mma_u8s8(accL[n], al[1][0], al[1][1], al[1][2], al[1][3], v2, v3);
+        for (int n = 0; n < NT2; n += 2) {
+            // matrices: 16-key chunks 0..3 of channels c .. c + 7; two n-tiles
+            // at a time so that dependent MMAs are four issues apart
+            int v[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                ldsm_x4(tV + pf_voff(hf * (D >> 1) + (n + j) * 8 + ri, mi), v[j][0], v[j][1], v[j][2],
+                        v[j][3]);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    mma_s8(accH[n + j], ah[kk][0], ah[kk][1], ah[kk][2], ah[kk][3], v[j][2 * kk],
+                           v[j][2 * kk + 1]);
+                    mma_u8s8(accL[n + j], al[kk][0], al[kk][1], al[kk][2], al[kk][3], v[j][2 * kk],
+                             v[j][2 * kk + 1]);
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
                             ep.status[ST_SAT_GU] = 1;
                         yg = sat_b(yg, 1 << 24);
                         yu = sat_b(yu, 1 << 24);
-                        ep.out[(size_t)m * ep.ldo + (n >> 1)] = swiglu_dev((int)yg, (int)yu);
+                        ep.out[(size_t)m * ep.ldo + (n >> 1)] = swiglu_tab((int)yg, (int)yu);
                     }
                 } else {
                     if (n < N) epi_store<MODE>(ep, m, n, c0);

@@ -757,6 +757,24 @@ __global__ void __launch_bounds__(256) k_gemv(const int8_t* __restrict__ W,
     }
 }
 
+// sigmoid_q15(z) for every z below SIG_TAB_N (all larger z give 2^15), one
+// table per device, filled by k_sig_table when the kernels are initialised;
+// the tiled GEMM's SwiGLU epilogue looks the sigmoid up instead of running
+// the 15-step division for each of its many outputs
+constexpr int SIG_TAB_N = 24576;
+__device__ uint16_t g_sig_tab[SIG_TAB_N];
+
+__global__ void k_sig_table() {
+    const int z = blockIdx.x * blockDim.x + threadIdx.x;
+    if (z < SIG_TAB_N) g_sig_tab[z] = (uint16_t)sigmoid_q15(z);
+}
+
+__device__ __forceinline__ int swiglu_tab(int g, int u) {
+    const i64 z = swiglu_z(g);
+    const unsigned q = z < SIG_TAB_N ? (unsigned)__ldg(&g_sig_tab[z]) : 32768u;
+    return swiglu_finish(g, u, q);
+}
+
 }  // namespace detint
 #include "k_sgemv.cuh"
 #include "k_gemm.cuh"

@@ -335,6 +335,11 @@ cudaError_t kernels_init() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<128>::SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_prefill<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<64>::SMEM);
+    if (e == cudaSuccess) {
+        k_sig_table<<<(SIG_TAB_N + 255) / 256, 256>>>();
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(0);
     int dev = 0;
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
