@@ -146,6 +146,9 @@ class Model:
     def set_fused_decode(self, enable: bool):
         _check(lib().detint_set_option(self._h, 1, int(bool(enable))), "detint_set_option")
 
+    def set_staged_decode(self, enable: bool):
+        _check(lib().detint_set_option(self._h, 3, int(bool(enable))), "detint_set_option")
+
     def set_tc_prefill(self, enable: bool):
         _check(lib().detint_set_option(self._h, 2, int(bool(enable))), "detint_set_option")
 

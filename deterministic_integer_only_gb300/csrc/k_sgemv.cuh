@@ -337,6 +337,7 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
 
     if (warp == 8) {
         // producer: weight rows of each (row group, K-chunk) unit into the ring
+        const uint64_t pol = l2_evict_first();
         int u = 0;
         for (int g = g0; g < g1; ++g) {
             for (int kc = 0; kc < a.nkc; ++kc, ++u) {
@@ -356,15 +357,15 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
                     const uint32_t bytes = (uint32_t)rows * (uint32_t)a.K;
                     if (lane == 0) {
                         mbar_arrive_expect_tx(fb, bytes);
-                        bulk_g2s(smem_u32(ring + (size_t)s * 16 * P), a.W + (size_t)g * 16 * a.K, bytes, fb);
+                        bulk_g2s_hint(smem_u32(ring + (size_t)s * 16 * P), a.W + (size_t)g * 16 * a.K, bytes, fb, pol);
                     }
                 } else {
                     if (lane == 0) mbar_arrive_expect_tx(fb, 16u * a.KC);
                     __syncwarp();
                     if (lane < 16) {
                         const int row = min(g * 16 + lane, a.N - 1);
-                        bulk_g2s(smem_u32(ring + ((size_t)s * 16 + lane) * P),
-                                 a.W + (size_t)row * a.K + (size_t)kc * a.KC, a.KC, fb);
+                        bulk_g2s_hint(smem_u32(ring + ((size_t)s * 16 + lane) * P),
+                                      a.W + (size_t)row * a.K + (size_t)kc * a.KC, a.KC, fb, pol);
                     }
                 }
             }

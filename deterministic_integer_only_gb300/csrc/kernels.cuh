@@ -219,10 +219,13 @@ __device__ void qk_norm_warp(i64 (&y)[EPL], const int16_t* gamma, int lane, int 
 // head `slot - nq` (K/V written into the paged cache) of token t;
 // cr/sr: RoPE row of this token's position, kvp: its kv head's parameters,
 // gq/gk: QK-norm gammas (global or shared memory)
+// ks/vs (optional): the new key row and value column also go to these
+// shared-memory copies of the cache block (value stride KV_BLK)
 template <int EPL>
 __device__ void qkv_head_p(const QkvPostArgs& a, int t, int slot, int8_t* q_dst, int32_t* mq_dst,
                            int32_t* kq_dst, const int16_t* cr, const int16_t* sr,
-                           const int32_t* kvp, const int16_t* gq, const int16_t* gk);
+                           const int32_t* kvp, const int16_t* gq, const int16_t* gk,
+                           int8_t* ks = nullptr, int8_t* vs = nullptr);
 
 template <int EPL>
 __device__ void qkv_head(const QkvPostArgs& a, int t, int slot, int8_t* q_dst, int32_t* mq_dst,
@@ -238,7 +241,8 @@ __device__ void qkv_head(const QkvPostArgs& a, int t, int slot, int8_t* q_dst, i
 template <int EPL>
 __device__ void qkv_head_p(const QkvPostArgs& a, int t, int slot, int8_t* q_dst, int32_t* mq_dst,
                            int32_t* kq_dst, const int16_t* cr, const int16_t* sr,
-                           const int32_t* kvp, const int16_t* gq, const int16_t* gk) {
+                           const int32_t* kvp, const int16_t* gq, const int16_t* gk,
+                           int8_t* ks, int8_t* vs) {
     const int lane = threadIdx.x & 31;
     const int nq = a.nq, nkv = a.nkv, d = a.d, dh2 = d >> 1;
     const int lg_d = (EPL == 4) ? 7 : 6;
@@ -312,8 +316,14 @@ __device__ void qkv_head_p(const QkvPostArgs& a, int t, int slot, int8_t* q_dst,
         for (int j = 0; j < EPL; ++j) {
             const int i = lane + 32 * j;
             const int ec = kvp[8 + (i & (dh2 - 1))];
-            kd[i] = (int8_t)sat127(rshr(y[j] * (1LL << ec) * KQM, KQS));
-            vd[(size_t)i * KV_BLK] = (int8_t)sat127(rshr((i64)vrow[i] * VQM, VQS));
+            const int8_t k8 = (int8_t)sat127(rshr(y[j] * (1LL << ec) * KQM, KQS));
+            const int8_t v8 = (int8_t)sat127(rshr((i64)vrow[i] * VQM, VQS));
+            kd[i] = k8;
+            vd[(size_t)i * KV_BLK] = v8;
+            if (ks) {
+                ks[i] = k8;
+                vs[(size_t)i * KV_BLK] = v8;
+            }
         }
     }
 }
@@ -779,6 +789,7 @@ __device__ __forceinline__ int swiglu_tab(int g, int u) {
 #include "k_sgemv.cuh"
 #include "k_gemm.cuh"
 #include "k_attn_prefill.cuh"
+#include "k_attn_decode.cuh"
 namespace detint {
 
 // ----------------------------------------------------------- argmax (a11)

@@ -92,7 +92,8 @@ struct AttnArgs {
     int32_t* o;              // [T][nq d] Q12
     int T, nq, nkv, d, lg_grp;
     int ctx_cap;             // keys that fit the shared-memory row
-    const int32_t* seq_len;  // decode: lengths before this step (L2 prefetch only)
+    const int32_t* seq_len;  // decode: lengths before this step
+    int32_t* status;         // staged decode: timeout flag of its bounded waits
 };
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 size_t attention_smem_bytes(int grp, int d, int ctx_cap);
@@ -108,7 +109,13 @@ cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xi
                          const int32_t* mt = nullptr, const int32_t* kt = nullptr,
                          bool pdl = true);   // pdl: W is immutable (streamed before the wait)
 // decode attention fused with the QKV post-processing (one token per sequence)
-cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s);
+// staged: the variant that copies the sequence's K/V blocks into shared
+// memory before the wait (a.ctx_cap = its staged key capacity, a multiple of
+// 64; every sequence's context after the step must fit)
+cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s,
+                               bool staged = false);
+// dynamic shared memory of the staged variant for a capacity of cap keys
+size_t attn_dec_smem(int grp, int d, int cap);
 
 // prefill attention on the int8 tensor pipe: one CTA per (query block, kv
 // head); a query block is up to 64 / G consecutive tokens of one sequence

@@ -200,7 +200,27 @@ cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xi
     return launch_pdl(k_sgemv<1>, dim3(ncta), dim3(SG_THREADS), smem, s, a);
 }
 
-cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s) {
+size_t attn_dec_smem(int grp, int d, int cap) { return attn_dec_smem_bytes(grp, d, cap); }
+
+using AttnDecFn = void (*)(AttnArgs, QkvPostArgs);
+static AttnDecFn attn_dec_kernel(int d, int lg_grp) {
+    static const AttnDecFn k128[4] = {k_attn_dec_staged<4, 1>, k_attn_dec_staged<4, 2>,
+                                      k_attn_dec_staged<4, 4>, k_attn_dec_staged<4, 8>};
+    static const AttnDecFn k64[4] = {k_attn_dec_staged<2, 1>, k_attn_dec_staged<2, 2>,
+                                     k_attn_dec_staged<2, 4>, k_attn_dec_staged<2, 8>};
+    if (lg_grp < 0 || lg_grp > 3) return nullptr;
+    return d == 128 ? k128[lg_grp] : (d == 64 ? k64[lg_grp] : nullptr);
+}
+
+cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStream_t s, bool staged) {
+    if (staged) {
+        if ((a.ctx_cap & 63) || a.ctx_cap > AD_MAXB * KV_BLK || a.lg_grp > 3) return cudaErrorInvalidValue;
+        const size_t sm2 = attn_dec_smem_bytes(1 << a.lg_grp, a.d, a.ctx_cap);
+        const dim3 grid(a.T, a.nkv);
+        auto k = attn_dec_kernel(a.d, a.lg_grp);
+        if (!k) return cudaErrorInvalidValue;
+        return launch_pdl(k, grid, dim3(AD_THREADS), sm2, s, a, qa);
+    }
     const size_t smem = attention_smem_bytes(1 << a.lg_grp, a.d, a.ctx_cap);
     const dim3 grid(a.T, a.nkv);
     if (a.d == 128) return launch_pdl(k_attn_decode<4>, grid, dim3(256), smem, s, a, qa);
@@ -333,6 +353,11 @@ cudaError_t kernels_init() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RESADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+    for (int lg = 0; lg < 4 && e == cudaSuccess; ++lg) {
+        e = cudaFuncSetAttribute(attn_dec_kernel(128, lg), cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM_MAX);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_dec_kernel(64, lg), cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM_MAX);
+    }
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<128>::SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_prefill<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<64>::SMEM);
     if (e == cudaSuccess) {

@@ -139,6 +139,9 @@ struct detint_model {
     int use_graph = 1;
     int fused_decode = 1;    // 0: decode through the separate row kernels (tests compare both)
     int tc_prefill = 1;      // 0: prefill attention through the per-token kernel (tests compare both)
+    int staged_decode = 1;   // 0: decode attention through the per-token kernel (tests compare both)
+    int dec_cap = 0;         // keys the staged decode attention holds (0: unsupported shape)
+    int dec_staged = 0;      // this step uses the staged decode attention
     int pf_ok = 0;           // the tensor-core prefill attention supports this shape
     CUtensorMap kmap, vmap;  // whole K / V^T caches for the prefill attention
     int32_t* qblk = nullptr; // prefill query blocks [Tcap + max_batch][4]
@@ -273,9 +276,10 @@ static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32
         AttnArgs aa{};
         aa.kc = qa.kc; aa.vc = qa.vc; aa.block_table = m->block_table; aa.mbs = m->mbs;
         aa.tok_seq = m->tok_seq; aa.tok_pos = m->tok_pos; aa.kvp = w.kvp; aa.o = m->o; aa.T = T;
-        aa.nq = nq; aa.nkv = nkv; aa.d = d; aa.lg_grp = m->lg_grp; aa.ctx_cap = m->ctx_cap;
-        aa.seq_len = m->seq_len_dev;
-        CK(launch_attn_decode(aa, qa, s));
+        aa.nq = nq; aa.nkv = nkv; aa.d = d; aa.lg_grp = m->lg_grp;
+        aa.ctx_cap = m->dec_staged ? m->dec_cap : m->ctx_cap;
+        aa.seq_len = m->seq_len_dev; aa.status = m->status;
+        CK(launch_attn_decode(aa, qa, s, m->dec_staged != 0));
         e.out = m->h; e.ldo = H; e.mc = w.m_o; e.fout = 16;
         if ((rc = gemv(w.w_o, H, nq * d, m->o, nullptr, 12, 2, EPI_RESADD, e))) return rc;
         e.out = m->sbuf; e.ldo = F; e.mc = w.m_gu; e.fout = 12;
@@ -568,6 +572,14 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
     m->pf_ok = (d == 64 || d == 128) && m->lg_grp <= 6 &&
                make_kv_maps(&m->kmap, &m->vmap, m->kcache, m->vcache,
                             (long long)m->L * m->nblocks * nkv, d) == cudaSuccess;
+    // staged decode attention: the largest block multiple of keys whose K/V
+    // copies and score rows fit the shared-memory budget
+    m->dec_cap = 0;
+    if ((d == 64 || d == 128) && m->lg_grp <= 3) {
+        const int want = std::min(m->mbs * KV_BLK, 64 * KV_BLK);
+        for (int cap = KV_BLK; cap <= want; cap += KV_BLK)
+            if (attn_dec_smem(1 << m->lg_grp, d, cap) <= 220 * 1024) m->dec_cap = cap;
+    }
     int rc = ensure_scratch(m, std::max(64, max_batch));
     if (rc != DETINT_OK) { detint_free(m); return rc; }
     ce = kernels_init();
@@ -652,6 +664,11 @@ int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const
     cudaStream_t s = (cudaStream_t)sp;
     rc = ensure_scratch(m, n_seq);
     if (rc) return rc;
+    {
+        int mx = 0;
+        for (int i = 0; i < n_seq; ++i) mx = std::max(mx, m->seq_len[seq_ids[i]] + 1);
+        m->dec_staged = (m->staged_decode && m->dec_cap > 0 && mx <= m->dec_cap) ? 1 : 0;
+    }
     const bool graph = m->use_graph && s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread;
     if (!graph) {
         std::vector<int32_t> ids(seq_ids, seq_ids + n_seq);
@@ -661,7 +678,8 @@ int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const
         if (rc) return rc;
     } else {
         char key[128];
-        snprintf(key, sizeof key, "%d|%p|%p|%p|", n_seq, (const void*)tok, (void*)logits, (void*)next_tok);
+        snprintf(key, sizeof key, "%d|%d|%p|%p|%p|", n_seq, m->dec_staged, (const void*)tok, (void*)logits,
+                 (void*)next_tok);
         std::string k(key);
         for (int i = 0; i < n_seq; ++i) k += std::to_string(seq_ids[i]) + ",";
         auto it = m->graphs.find(k);
@@ -759,6 +777,7 @@ int detint_set_option(detint_model* m, int option, int value) {
     if (option == DETINT_OPT_GRAPH) m->use_graph = value;
     else if (option == DETINT_OPT_FUSED_DECODE) { m->fused_decode = value; free_graphs(m); }
     else if (option == DETINT_OPT_TC_PREFILL) m->tc_prefill = value;
+    else if (option == DETINT_OPT_STAGED_DECODE) { m->staged_decode = value; free_graphs(m); }
     else return fail(DETINT_E_ARG, "unknown option");
     return DETINT_OK;
 }

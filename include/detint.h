@@ -138,8 +138,13 @@ int detint_set_graph(detint_model* m, int enable);
  * default; 0 = through the separate row kernels) and DETINT_OPT_TC_PREFILL
  * (1 = prefill attention on the int8 tensor pipe in two sweeps over the keys,
  * the default where head_dim is 64 or 128; 0 = the per-token attention
- * kernel). Every setting gives bit-identical results. Errors: ARG. */
-enum { DETINT_OPT_GRAPH = 0, DETINT_OPT_FUSED_DECODE = 1, DETINT_OPT_TC_PREFILL = 2 };
+ * kernel) and DETINT_OPT_STAGED_DECODE (1 = fused decode attention with the
+ * sequence's cached K/V copied into shared memory before the step's data is
+ * ready, the default while every context fits that copy; 0 = the attention
+ * kernel that reads the cache from global memory). Every setting gives
+ * bit-identical results. Errors: ARG. */
+enum { DETINT_OPT_GRAPH = 0, DETINT_OPT_FUSED_DECODE = 1, DETINT_OPT_TC_PREFILL = 2,
+       DETINT_OPT_STAGED_DECODE = 3 };
 int detint_set_option(detint_model* m, int option, int value);
 
 /* Shape of the loaded model: info[0..9] = n_layers, hidden, n_q, n_kv,

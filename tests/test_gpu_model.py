@@ -172,3 +172,34 @@ def test_tiny_batch_sizes_match_oracle(torch_cuda, tiny_artifact, B):
         assert np.array_equal(toks[b], ot)
         assert all(np.array_equal(rows[s][b], orows[s]) for s in range(6))
     m.close()
+
+
+@pytest.mark.parametrize("name", ["qwen", "llama"])
+def test_staged_decode_attention_equals_per_token(torch_cuda, request, name):
+    """The decode attention that stages the cached K/V in shared memory gives
+    the per-token kernel's logits: a batch of 3 ragged prompts, 24 steps."""
+    path = request.getfixturevalue({"qwen": "qwen_artifact", "llama": "llama_artifact"}[name])
+    V = {"qwen": 151936, "llama": 128256}[name]
+    prompts = [synth.prompt_ids(8, i, n, V) for i, n in enumerate((5, 64, 190))]
+    out = {}
+    for staged in (True, False):
+        m = _load(path, 4, 512)
+        m.set_staged_decode(staged)
+        out[staged] = m.generate(prompts, 24, keep_logits="hash")
+        m.close()
+    assert np.array_equal(out[True][0], out[False][0])
+    assert out[True][1] == out[False][1]
+
+
+def test_staged_decode_capacity_crossing(torch_cuda, qwen_artifact):
+    """A context that grows past the staged capacity (768 keys at this shape)
+    mid-generation switches kernels without changing a logit."""
+    prompt = synth.prompt_ids(8, 9, 760, 151936)
+    out = {}
+    for staged in (True, False):
+        m = _load(qwen_artifact, 1, 1024)
+        m.set_staged_decode(staged)
+        out[staged] = m.generate([prompt], 16, keep_logits="hash")
+        m.close()
+    assert np.array_equal(out[True][0], out[False][0])
+    assert out[True][1] == out[False][1]
