@@ -53,6 +53,12 @@ def lib():
         L.or_seq_len.argtypes = [C.c_void_p]
         L.or_seq_feed.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.POINTER(i32),
                                   C.POINTER(i32), C.POINTER(i32)]
+        L.or_splitmix64.restype = u64; L.or_splitmix64.argtypes = [u64, u64]
+        L.or_sample.restype = C.c_int
+        L.or_sample.argtypes = [C.POINTER(i32), C.c_int, i32, i32, i32, u64, u64]
+        L.or_sample_set.restype = C.c_int
+        L.or_sample_set.argtypes = [C.POINTER(i32), C.c_int, i32, i32, i32, C.POINTER(C.c_char),
+                                    C.POINTER(i64), C.POINTER(i64)]
         _lib = L
     return _lib
 
@@ -212,6 +218,33 @@ def attention_row(q8, mq, kq, K8, V8, kvp):
 def argmax(x):
     x = np.ascontiguousarray(x, np.int32)
     return int(lib().or_argmax(_p(x, C.c_int32), C.c_int(x.size)))
+
+
+def splitmix64(seed: int, counter: int) -> int:
+    return int(lib().or_splitmix64(C.c_uint64(seed), C.c_uint64(counter)))
+
+
+def sample(logits, inv_temp: int = 65536, top_k: int = 0, top_p: int = 65536, seed: int = 0,
+           counter: int = 0) -> int:
+    """Integer sampling of one logits row (temperature Q16 inverse, top-k,
+    top-p Q16, SplitMix64 draw); returns the token index."""
+    x = np.ascontiguousarray(logits, np.int32)
+    tok = lib().or_sample(_p(x, C.c_int32), x.size, int(inv_temp), int(top_k), int(top_p),
+                          C.c_uint64(seed), C.c_uint64(counter))
+    check()
+    return int(tok)
+
+
+def sample_set(logits, inv_temp: int = 65536, top_k: int = 0, top_p: int = 65536):
+    """Kept set (bool [n]), weights E (int64 [n]) and their kept sum S."""
+    x = np.ascontiguousarray(logits, np.int32)
+    keep = np.zeros(x.size, np.uint8)
+    E = np.zeros(x.size, np.int64)
+    S = C.c_int64(0)
+    lib().or_sample_set(_p(x, C.c_int32), x.size, int(inv_temp), int(top_k), int(top_p),
+                        keep.ctypes.data_as(C.POINTER(C.c_char)), _p(E, C.c_int64), C.byref(S))
+    check()
+    return keep.astype(bool), E, int(S.value)
 
 
 # --------------------------------------------------------------------- model

@@ -400,6 +400,105 @@ int or_argmax(const int32_t* x, int n) {
     return best;
 }
 
+/* ------------------------------------------------------- integer sampling */
+/* Next-token draw from one logits row: temperature, top-k, top-p and one
+ * draw by cumulative integer weights, all in integers ([BITEXACT] "Fix the
+ * arithmetic, not just the random seed" and "Reproducibility has a cost":
+ * integer sampling rules, deterministic sampling). The pages give no
+ * algorithm; the steps follow the reading written in the arithmetic
+ * specification (section "Integer sampling"), in that order. */
+
+/* the (counter+1)-th output of SplitMix64 seeded with `seed` (Steele, Lea
+ * and Flood, "Fast splittable pseudorandom number generators", 2014) */
+uint64_t or_splitmix64(uint64_t seed, uint64_t counter) {
+    uint64_t z = seed + (counter + 1) * 0x9E3779B97F4A7C15ULL;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+static const int32_t* g_sort_keys;   /* qsort has no context argument */
+static int cmp_logit_desc(const void* a, const void* b) {
+    const int ia = *(const int*)a, ib = *(const int*)b;
+    const int32_t la = g_sort_keys[ia], lb = g_sort_keys[ib];
+    if (la != lb) return la > lb ? -1 : 1;
+    return ia < ib ? -1 : (ia > ib ? 1 : 0);
+}
+
+/* steps 1-5: the kept set K2 (keep_out), every weight E_i and S = sum over
+ * K2; returns |K2| */
+int or_sample_set(const int32_t* logits, int n, int32_t inv_temp, int32_t top_k, int32_t top_p,
+                  char* keep_out, i64* E_out, i64* S_out) {
+    CHECK(n >= 1);
+    CHECK(inv_temp >= 0 && inv_temp <= (1 << 20));
+    CHECK(top_p >= 1 && top_p <= 65536);
+    if (n < 1) { *S_out = 0; return 0; }
+    i64* u = (i64*)malloc(sizeof(i64) * (size_t)n);
+    int* order = (int*)malloc(sizeof(int) * (size_t)n);
+    /* 1. base-2 logits in Q10 at the temperature */
+    for (int i = 0; i < n; i++) {
+        const i64 a = or_rshr((i64)logits[i] * 47274, 21);
+        u[i] = or_rshr(a * inv_temp, 16);
+    }
+    /* 2. weights relative to the maximum */
+    i64 M = u[0];
+    for (int i = 1; i < n; i++) if (u[i] > M) M = u[i];
+    for (int i = 0; i < n; i++) E_out[i] = or_exp2q(u[i] - M);
+    /* 3. logits descending, ties by index */
+    for (int i = 0; i < n; i++) order[i] = i;
+    g_sort_keys = logits;
+    qsort(order, (size_t)n, sizeof(int), cmp_logit_desc);
+    /* 4. top-k */
+    const int k1 = (top_k > 0 && top_k < n) ? top_k : n;
+    i64 S1 = 0;
+    for (int j = 0; j < k1; j++) S1 += E_out[order[j]];
+    /* 5. top-p: shortest prefix reaching top_p / 65536 of S1, boundary ties kept */
+    int k2 = k1;
+    if (top_p < 65536) {
+        i64 P = 0;
+        int L = 0;
+        while (L < k1) {
+            P += E_out[order[L]];
+            L++;
+            if ((__int128)P * 65536 >= (__int128)top_p * S1) break;
+        }
+        const i64 dstar = u[order[L - 1]] - M;
+        k2 = L;
+        while (k2 < k1 && u[order[k2]] - M >= dstar) k2++;
+    }
+    i64 S = 0;
+    memset(keep_out, 0, (size_t)n);
+    for (int j = 0; j < k2; j++) { keep_out[order[j]] = 1; S += E_out[order[j]]; }
+    CHECK(S >= 32768);
+    *S_out = S;
+    free(u); free(order);
+    return k2;
+}
+
+/* steps 1-7: the sampled token */
+int or_sample(const int32_t* logits, int n, int32_t inv_temp, int32_t top_k, int32_t top_p,
+              uint64_t seed, uint64_t counter) {
+    if (n < 1) { CHECK(n >= 1); return -1; }
+    char* keep = (char*)malloc((size_t)n);
+    i64* E = (i64*)malloc(sizeof(i64) * (size_t)n);
+    i64 S = 0;
+    or_sample_set(logits, n, inv_temp, top_k, top_p, keep, E, &S);
+    /* 6-7. one draw by cumulative weights in index order */
+    const uint64_t r = or_splitmix64(seed, counter);
+    const i64 t = (i64)(((unsigned __int128)r * (unsigned __int128)(u64)S) >> 64);
+    int tok = -1;
+    i64 cum = 0;
+    for (int i = 0; i < n; i++) {
+        if (!keep[i]) continue;
+        cum += E[i];
+        if (cum > t) { tok = i; break; }
+    }
+    CHECK(tok >= 0);
+    free(keep);
+    free(E);
+    return tok;
+}
+
 /* ------------------------------------------------------------- the model */
 typedef struct {
     const int16_t *attn_gamma, *ffn_gamma, *q_gamma, *k_gamma;
