@@ -25,7 +25,7 @@ ERRORS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "token id o
 # every entry point of include/detint.h
 SYMBOLS = ["detint_load", "detint_prefill", "detint_decode_step", "detint_gemm_i8",
            "detint_reset_seq", "detint_seq_len", "detint_status", "detint_set_graph",
-           "detint_set_option", "detint_argmax_noalloc",
+           "detint_set_option", "detint_argmax_noalloc", "detint_sample",
            "detint_model_info", "detint_free", "detint_strerror", "detint_last_error"]
 
 
@@ -55,6 +55,7 @@ def lib():
         L.detint_set_graph.argtypes = [vp, C.c_int]
         L.detint_set_option.argtypes = [vp, C.c_int, C.c_int]
         L.detint_argmax_noalloc.argtypes = [vp, C.c_int, C.c_int, vp, vp]
+        L.detint_sample.argtypes = [vp, C.c_int, C.c_int, C.POINTER(SamplingParams), vp, vp]
         L.detint_model_info.argtypes = [vp, i32p]
         L.detint_free.argtypes = [vp]
         L.detint_free.restype = None
@@ -100,6 +101,34 @@ def detint_argmax_noalloc(logits, out, stream=None):
     rows, n = logits.shape
     _check(lib().detint_argmax_noalloc(_ptr(logits), rows, n, _ptr(out), _stream(stream)),
            "detint_argmax_noalloc")
+    return out
+
+
+class SamplingParams(C.Structure):
+    """detint_sampling_t: seed, counter (SplitMix64 draw index), inv_temp
+    (Q16 of 1/T), top_k (0: off), top_p (Q16, 65536: off)."""
+    _fields_ = [("seed", C.c_uint64), ("counter", C.c_uint64), ("inv_temp", C.c_int32),
+                ("top_k", C.c_int32), ("top_p", C.c_int32), ("reserved", C.c_int32)]
+
+
+def detint_sample(logits, params, out=None, stream=None):
+    """One integer-sampled token per row of an int32 cuda tensor [rows, n];
+    params: one dict (or SamplingParams) per row, or one for every row."""
+    import torch
+    rows, n = logits.shape
+    if isinstance(params, (dict, SamplingParams)):
+        params = [params] * rows
+    arr = (SamplingParams * rows)()
+    for r, p in enumerate(params):
+        if isinstance(p, SamplingParams):
+            arr[r] = p
+        else:
+            arr[r] = SamplingParams(int(p.get("seed", 0)), int(p.get("counter", 0)),
+                                    int(p.get("inv_temp", 65536)), int(p.get("top_k", 0)),
+                                    int(p.get("top_p", 65536)), 0)
+    if out is None:
+        out = torch.empty(rows, dtype=torch.int32, device=logits.device)
+    _check(lib().detint_sample(_ptr(logits), rows, n, arr, _ptr(out), _stream(stream)), "detint_sample")
     return out
 
 

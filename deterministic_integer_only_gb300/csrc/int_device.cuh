@@ -34,7 +34,7 @@ __device__ __forceinline__ int sat32(i64 x) { return (int)sat_b(x, 2147483647LL)
 __device__ __forceinline__ int sat127(i64 x) { return (int)sat_b(x, 127); }
 
 // floor(n / d) for d >= 1, by restoring long division over the quotient bits
-__device__ __noinline__ u64 udiv64(u64 n, u64 d) {
+static __device__ __noinline__ u64 udiv64(u64 n, u64 d) {
     if (n < d) return 0;
     int sh = bitlen_u64(n) - bitlen_u64(d);
     u64 dd = d << sh;
@@ -48,7 +48,7 @@ __device__ __noinline__ u64 udiv64(u64 n, u64 d) {
 }
 
 // floor(sqrt(n)), digit by digit
-__device__ __noinline__ u64 isqrt_u64(u64 n) {
+static __device__ __noinline__ u64 isqrt_u64(u64 n) {
     u64 r = 0, bit = 1ull << 62;
     while (bit > n) bit >>= 2;
     while (bit) {
@@ -60,7 +60,7 @@ __device__ __noinline__ u64 isqrt_u64(u64 n) {
 }
 
 // (m, k): m = round(N 2^k / D) (ties up) with 2^14 <= N 2^k / D < 2^15
-__device__ __noinline__ void dyadic_dev(u64 N, u64 D, int* m_out, int* k_out) {
+static __device__ __noinline__ void dyadic_dev(u64 N, u64 D, int* m_out, int* k_out) {
     int k = 14 + bitlen_u64(D) - bitlen_u64(N);
     for (int it = 0; it < 4; ++it) {   // the estimate is within one of k
         u64 lhs, lo;

@@ -132,6 +132,33 @@ int detint_status(detint_model* m, int32_t* flags, detint_stream_t s);
  * (README, "Usage": use_graph). */
 int detint_set_graph(detint_model* m, int enable);
 
+/* Integer sampling parameters of one row (see detint_sample). */
+typedef struct {
+    uint64_t seed;      /* SplitMix64 seed */
+    uint64_t counter;   /* draw index: output counter + 1 of the generator */
+    int32_t inv_temp;   /* Q16 of 1/temperature, 0 .. 2^20 (65536: T = 1; 0: uniform) */
+    int32_t top_k;      /* keep the top_k largest logits (0 or >= n: off) */
+    int32_t top_p;      /* Q16 nucleus mass, 1 .. 65536 (65536: off) */
+    int32_t reserved;   /* set to 0 */
+} detint_sampling_t;
+
+/* Draw one token per logits row with integer arithmetic only: weights
+ * E_i = exp2q(u_i - max u), u = the logit in base-2 Q10 at the temperature;
+ * the top_k largest logits (ties by lower index), then the shortest prefix
+ * of them (logit order) holding top_p of their weight plus its boundary ties;
+ * then t = floor(r S / 2^64) with r = SplitMix64(seed, counter) and S the
+ * kept weight, and the token is the first index (index order) whose
+ * cumulative kept weight exceeds t. The pages ask for integer sampling rules
+ * and deterministic sampling (BitExact LLM post, "Fix the arithmetic, not
+ * just the random seed"; "Reproducibility has a cost") without an algorithm;
+ * this is the reading in the arithmetic specification, section "Integer
+ * sampling". top_k = 1 gives the tie-low argmax for every seed.
+ * logits: device int32 [rows][n] (caller-owned); params: host [rows];
+ * out: device int32 [rows]. Asynchronous on s; allocates nothing.
+ * Errors: ARG (null pointer, rows or n < 1, a parameter out of range), CUDA. */
+int detint_sample(const int32_t* logits, int rows, int n, const detint_sampling_t* params,
+                  int32_t* out, detint_stream_t s);
+
 /* Options: DETINT_OPT_GRAPH (1 = replay decode steps as CUDA graphs, the
  * default; same as detint_set_graph), DETINT_OPT_FUSED_DECODE (1 = decode
  * batches of up to 8 sequences through the fused streaming kernels, the
