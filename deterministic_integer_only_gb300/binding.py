@@ -178,6 +178,9 @@ class Model:
     def set_staged_decode(self, enable: bool):
         _check(lib().detint_set_option(self._h, 3, int(bool(enable))), "detint_set_option")
 
+    def set_persistent(self, enable: bool):
+        _check(lib().detint_set_option(self._h, 4, int(bool(enable))), "detint_set_option")
+
     def set_tc_prefill(self, enable: bool):
         _check(lib().detint_set_option(self._h, 2, int(bool(enable))), "detint_set_option")
 

@@ -305,97 +305,54 @@ __device__ void sg_epilogue(const SgArgs& a, const SgShared& sh, int32_t* red, i
     }
 }
 
-// MINB = 2: the long-stream variant (two CTAs per SM, registers capped to fit)
-template <int MINB>
-__global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ SgShared sh;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // ring row pitch: a whole 16-row group arrives in one bulk copy when the
-    // rows are not chunked (pitch K); chunked rows get a 64-byte pad so
-    // fragment loads of neighbouring rows fall in different banks
-    const int P = a.nkc == 1 ? a.K : a.KC + 64;
-    const int XP = a.K + 64;                      // activation row pitch
-    unsigned char* ring = smem;
-    const int NS = 1 << a.lg_ns;
-    int8_t* xs = (int8_t*)(smem + sg_ring_bytes(a.KC, NS));
-    int32_t* red = (int32_t*)(xs + (size_t)8 * XP);     // [SG_GB][8 warps][16][8]
-    const int c = blockIdx.x;
-    const int g0 = c * a.rg_q + min(c, a.rg_r);
-    const int g1 = g0 + a.rg_q + (c < a.rg_r ? 1 : 0);
-    const int units = (g1 - g0) * a.nkc;
-
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(smem_u32(&sh.full[s]), 1);
-            mbar_init(smem_u32(&sh.empty[s]), 8);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    pdl_launch();
-
-    if (warp == 8) {
-        // producer: weight rows of each (row group, K-chunk) unit into the ring
-        const uint64_t pol = l2_evict_first();
-        int u = 0;
-        for (int g = g0; g < g1; ++g) {
-            for (int kc = 0; kc < a.nkc; ++kc, ++u) {
-                const int s = u & (NS - 1);
-                if (u >= NS && lane == 0) {
-                    // bounded: on a timeout the status word records it and the
-                    // stream continues (results are then invalid, nothing hangs)
-                    if (!mbar_wait(smem_u32(&sh.empty[s]), ((u >> a.lg_ns) - 1) & 1))
-                        a.ep.status[ST_TIMEOUT] = 1;
+// producer warp: the weight rows of each (row group, K-chunk) unit of row
+// groups [g0, g1) into the ring; u counts ring units across calls (stage
+// u mod NS, phase parity from u / NS), SB is the ring's stage stride
+__device__ __forceinline__ void sg_produce(const SgArgs& a, SgShared& sh, unsigned char* ring, int P,
+                                           size_t SB, int NS, int lg_ns, int g0, int g1, int& u,
+                                           uint64_t pol) {
+    const int lane = threadIdx.x & 31;
+    for (int g = g0; g < g1; ++g) {
+        for (int kc = 0; kc < a.nkc; ++kc, ++u) {
+            const int s = u & (NS - 1);
+            if (u >= NS && lane == 0) {
+                // bounded: on a timeout the status word records it and the
+                // stream continues (results are then invalid, nothing hangs)
+                if (!mbar_wait(smem_u32(&sh.empty[s]), ((u >> lg_ns) - 1) & 1))
+                    a.ep.status[ST_TIMEOUT] = 1;
+            }
+            __syncwarp();
+            const uint32_t fb = smem_u32(&sh.full[s]);
+            if (a.nkc == 1) {
+                // the group's rows are contiguous: one copy (the last group
+                // may hold fewer than 16 rows; its missing rows are never stored)
+                const int rows = min(16, a.N - g * 16);
+                const uint32_t bytes = (uint32_t)rows * (uint32_t)a.K;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, bytes);
+                    bulk_g2s_hint(smem_u32(ring + (size_t)s * SB), a.W + (size_t)g * 16 * a.K, bytes, fb, pol);
                 }
+            } else {
+                if (lane == 0) mbar_arrive_expect_tx(fb, 16u * a.KC);
                 __syncwarp();
-                const uint32_t fb = smem_u32(&sh.full[s]);
-                if (a.nkc == 1) {
-                    // the group's rows are contiguous: one copy (the last group
-                    // may hold fewer than 16 rows; its missing rows are never stored)
-                    const int rows = min(16, a.N - g * 16);
-                    const uint32_t bytes = (uint32_t)rows * (uint32_t)a.K;
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(fb, bytes);
-                        bulk_g2s_hint(smem_u32(ring + (size_t)s * 16 * P), a.W + (size_t)g * 16 * a.K, bytes, fb, pol);
-                    }
-                } else {
-                    if (lane == 0) mbar_arrive_expect_tx(fb, 16u * a.KC);
-                    __syncwarp();
-                    if (lane < 16) {
-                        const int row = min(g * 16 + lane, a.N - 1);
-                        bulk_g2s_hint(smem_u32(ring + ((size_t)s * 16 + lane) * P),
-                                      a.W + (size_t)row * a.K + (size_t)kc * a.KC, a.KC, fb, pol);
-                    }
+                if (lane < 16) {
+                    const int row = min(g * 16 + lane, a.N - 1);
+                    bulk_g2s_hint(smem_u32(ring + (size_t)s * SB + (size_t)lane * P),
+                                  a.W + (size_t)row * a.K + (size_t)kc * a.KC, a.KC, fb, pol);
                 }
             }
         }
-        return;
     }
+}
 
-    // compute warps: copy the (immutable) RMSNorm gamma and this CTA's weight
-    // channel scales before the wait
-    int16_t* gam = (int16_t*)(red + SG_GB * 1024);
-    if (a.pro == PRO_NORMQUANT)
-        for (int i = tid * 8; i < a.K; i += 256 * 8) *(int4*)(gam + i) = *(const int4*)(a.gamma + i);
-    int32_t* hold = (int32_t*)(gam + a.K);
-    int32_t* mcs = hold + 256;
-    const bool mc_pre = a.ep.mc && (g1 - g0) * 16 <= 256;
-    if (mc_pre && tid < (g1 - g0) * 16) mcs[tid] = a.ep.mc[min(g0 * 16 + tid, a.N - 1)];
-    pdl_wait();
-    // residual add: issue the loads of this CTA's old residual values now so
-    // they overlap the quantisation prologue
-    const bool pre = a.mode == EPI_RESADD && (g1 - g0) * 128 <= 256;
-    int hv = 0;
-    if (pre && tid < (g1 - g0) * 128) {
-        const int tk = tid & 7, n = g0 * 16 + (tid >> 3);
-        if (tk < a.M && n < a.N) hv = a.ep.out[(size_t)tk * a.ep.ldo + n];
-    }
-    if (a.pro == PRO_NONE) sg_load_x8(a, sh, xs, XP);
-    else sg_prologue(a, sh, xs, XP, gam);
-    if (pre && tid < (g1 - g0) * 128) hold[tid] = hv;
-    bar_named(1, 256);
-
+// compute warps: dot products of the quantised tile with the ring's weight
+// units of row groups [g0, g1), then the epilogue per SG_GB groups; hold:
+// preloaded residual values (or null), mcs: staged channel scales (or null)
+__device__ __forceinline__ void sg_consume(const SgArgs& a, SgShared& sh, const unsigned char* ring,
+                                           int P, size_t SB, int NS, int lg_ns, const int8_t* xs,
+                                           int XP, int32_t* red, int g0, int g1, int& u,
+                                           const int32_t* hold, const int32_t* mcs) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
     const int nch = a.KC >> 6;
     // up to 4 tokens: dp4a on the integer pipe (one multiply per weight per
@@ -403,7 +360,6 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
     // run at the same int8 rate, so the m16n8 tile's unused columns would
     // cost up to 8x the integer work at one token.
     const bool dp = a.M <= 4;
-    int u = 0;
     for (int gb = g0; gb < g1; gb += SG_GB) {
         const int nb = min(SG_GB, g1 - gb);
         if (dp) {
@@ -421,8 +377,8 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
                 for (int tk = 0; tk < 4; ++tk) acc[tk][0] = acc[tk][1] = acc[tk][2] = acc[tk][3] = 0;
                 for (int kc = 0; kc < a.nkc; ++kc, ++u) {
                     const int s = u & (NS - 1);
-                    if (!mbar_wait(smem_u32(&sh.full[s]), (u >> a.lg_ns) & 1)) a.ep.status[ST_TIMEOUT] = 1;
-                    const unsigned char* wr = ring + ((size_t)s * 16 + r) * P;
+                    if (!mbar_wait(smem_u32(&sh.full[s]), (u >> lg_ns) & 1)) a.ep.status[ST_TIMEOUT] = 1;
+                    const unsigned char* wr = ring + (size_t)s * SB + (size_t)r * P;
                     const int8_t* xk = xs + (size_t)kc * a.KC;
                     for (int c0 = hl; c0 < nc; c0 += 64) {
                         int4 w[4];
@@ -472,7 +428,7 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
                 }
             }
             bar_named(1, 256);
-            sg_epilogue(a, sh, red, gb, nb, pre ? hold : nullptr, g0, mc_pre ? mcs : nullptr, 1);
+            sg_epilogue(a, sh, red, gb, nb, hold, g0, mcs, 1);
             bar_named(1, 256);
             continue;
         }
@@ -480,8 +436,8 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
             int acc[4] = {0, 0, 0, 0}, acc2[4] = {0, 0, 0, 0};
             for (int kc = 0; kc < a.nkc; ++kc, ++u) {
                 const int s = u & (NS - 1);
-                if (!mbar_wait(smem_u32(&sh.full[s]), (u >> a.lg_ns) & 1)) a.ep.status[ST_TIMEOUT] = 1;
-                const int8_t* st = (const int8_t*)ring + (size_t)s * 16 * P;
+                if (!mbar_wait(smem_u32(&sh.full[s]), (u >> lg_ns) & 1)) a.ep.status[ST_TIMEOUT] = 1;
+                const int8_t* st = (const int8_t*)ring + (size_t)s * SB;
                 const int8_t* wlo = st + g * P + 16 * tq;
                 const int8_t* whi = wlo + 8 * P;
                 const int8_t* xb = xs + g * XP + kc * a.KC + 16 * tq;
@@ -505,9 +461,74 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
             rw[(g + 8) * 8 + 2 * tq + 1] = acc[3];
         }
         bar_named(1, 256);
-        sg_epilogue(a, sh, red, gb, nb, pre ? hold : nullptr, g0, mc_pre ? mcs : nullptr, 8);
+        sg_epilogue(a, sh, red, gb, nb, hold, g0, mcs, 8);
         bar_named(1, 256);
     }
+}
+
+// MINB = 2: the long-stream variant (two CTAs per SM, registers capped to fit)
+template <int MINB>
+__global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ SgShared sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // ring row pitch: a whole 16-row group arrives in one bulk copy when the
+    // rows are not chunked (pitch K); chunked rows get a 64-byte pad so
+    // fragment loads of neighbouring rows fall in different banks
+    const int P = a.nkc == 1 ? a.K : a.KC + 64;
+    const int XP = a.K + 64;                      // activation row pitch
+    unsigned char* ring = smem;
+    const int NS = 1 << a.lg_ns;
+    int8_t* xs = (int8_t*)(smem + sg_ring_bytes(a.KC, NS));
+    int32_t* red = (int32_t*)(xs + (size_t)8 * XP);     // [SG_GB][8 warps][16][8]
+    const int c = blockIdx.x;
+    const int g0 = c * a.rg_q + min(c, a.rg_r);
+    const int g1 = g0 + a.rg_q + (c < a.rg_r ? 1 : 0);
+    const int units = (g1 - g0) * a.nkc;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), 1);
+            mbar_init(smem_u32(&sh.empty[s]), 8);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_launch();
+
+    if (warp == 8) {
+        const uint64_t pol = l2_evict_first();
+        int u = 0;
+        sg_produce(a, sh, ring, P, (size_t)16 * P, NS, a.lg_ns, g0, g1, u, pol);
+        return;
+    }
+
+    // compute warps: copy the (immutable) RMSNorm gamma and this CTA's weight
+    // channel scales before the wait
+    int16_t* gam = (int16_t*)(red + SG_GB * 1024);
+    if (a.pro == PRO_NORMQUANT)
+        for (int i = tid * 8; i < a.K; i += 256 * 8) *(int4*)(gam + i) = *(const int4*)(a.gamma + i);
+    int32_t* hold = (int32_t*)(gam + a.K);
+    int32_t* mcs = hold + 256;
+    const bool mc_pre = a.ep.mc && (g1 - g0) * 16 <= 256;
+    if (mc_pre && tid < (g1 - g0) * 16) mcs[tid] = a.ep.mc[min(g0 * 16 + tid, a.N - 1)];
+    pdl_wait();
+    // residual add: issue the loads of this CTA's old residual values now so
+    // they overlap the quantisation prologue
+    const bool pre = a.mode == EPI_RESADD && (g1 - g0) * 128 <= 256;
+    int hv = 0;
+    if (pre && tid < (g1 - g0) * 128) {
+        const int tk = tid & 7, n = g0 * 16 + (tid >> 3);
+        if (tk < a.M && n < a.N) hv = a.ep.out[(size_t)tk * a.ep.ldo + n];
+    }
+    if (a.pro == PRO_NONE) sg_load_x8(a, sh, xs, XP);
+    else sg_prologue(a, sh, xs, XP, gam);
+    if (pre && tid < (g1 - g0) * 128) hold[tid] = hv;
+    bar_named(1, 256);
+
+    int u = 0;
+    sg_consume(a, sh, ring, P, (size_t)16 * P, NS, a.lg_ns, xs, XP, red, g0, g1, u,
+               pre ? hold : nullptr, mc_pre ? mcs : nullptr);
     // every issued copy has completed before the CTA exits (bounded wait;
     // normally these phases completed long ago)
     if (tid == 0) {

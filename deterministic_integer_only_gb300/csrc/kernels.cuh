@@ -790,6 +790,7 @@ __device__ __forceinline__ int swiglu_tab(int g, int u) {
 #include "k_gemm.cuh"
 #include "k_attn_prefill.cuh"
 #include "k_attn_decode.cuh"
+#include "k_persistent.cuh"
 namespace detint {
 
 // ----------------------------------------------------------- argmax (a11)

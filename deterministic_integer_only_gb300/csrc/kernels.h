@@ -141,6 +141,45 @@ cudaError_t launch_attn_prefill(const PfArgs& a, const CUtensorMap& kmap, const 
                                 int d, cudaStream_t s);
 constexpr int PF_ROWS = 64;   // query rows (token x q head) per prefill attention CTA
 
+// one decode step in one cooperative launch (k_persistent.cuh)
+// the layer's weights, scales and caches (a device array of these)
+struct PdLayer {
+    const int8_t *w_qkv, *w_o, *w_gu, *w_d;
+    const int32_t *m_qkv, *m_o, *m_gu, *m_d, *kvp;
+    const int16_t *attn_gamma, *ffn_gamma, *q_gamma, *k_gamma;
+    int8_t *kc, *vc;
+};
+
+struct PdArgs {
+    const PdLayer* layers;
+    int L, T, H, nq, nkv, d, F, V, lg_grp, qk_norm, max_pos, mbs, lg_H;
+    long long eps_h, eps_qk;
+    const int8_t* embed;
+    const int32_t* embed_m;
+    const int16_t *final_gamma, *rope_cos, *rope_sin;
+    const int32_t* block_table;
+    const int32_t* tokens;      // [T] this step's input ids
+    const int32_t* tok_seq;     // [T] sequence of each token
+    int32_t* tok_pos;           // [T] position (written by the embedding phase)
+    int32_t* seq_len;           // [max_batch] advanced by the final phase
+    int32_t *h, *qkv, *o, *sbuf, *logits, *pval, *pidx;
+    int npart;
+    int32_t* next_tok;
+    int32_t* status;
+    unsigned* bar;              // grid barrier arrival counter (zeroed before each launch)
+    int rg[5][2];               // row groups per CTA (q, r) of the five GEMV shapes
+    int lg_ns;                  // log2 ring stages
+    int attn_cap;               // keys the attention scratch holds
+    size_t off_xs, off_red, off_gam, off_hold;   // dynamic shared memory layout
+};
+
+// d: head_dim, grp: q heads per kv head; cudaErrorNotSupported for shapes
+// without an instantiation
+cudaError_t launch_decode_persistent(const PdArgs& a, int grid, size_t smem, cudaStream_t s);
+bool decode_persistent_supported(int d, int grp);
+// the occupancy check of the cooperative launch (1 CTA per SM with smem bytes)
+bool decode_persistent_fits(int d, int grp, size_t smem);
+
 cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int rows, int npart,
                                 int32_t* next_tok, const int32_t* tok_seq, int32_t* seq_len,
                                 cudaStream_t s, bool pdl = false);

@@ -334,6 +334,42 @@ static cudaError_t gemv_attr_all() {
     return e;
 }
 
+using PdFn = void (*)(PdArgs);
+static PdFn pd_kernel(int d, int grp) {
+    if (d == 128 && grp == 2) return k_decode_persistent<4, 2>;
+    if (d == 64 && grp == 4) return k_decode_persistent<2, 4>;
+    if (d == 64 && grp == 2) return k_decode_persistent<2, 2>;
+    return nullptr;
+}
+bool decode_persistent_supported(int d, int grp) { return pd_kernel(d, grp) != nullptr; }
+bool decode_persistent_fits(int d, int grp, size_t smem) {
+    PdFn k = pd_kernel(d, grp);
+    if (!k || smem > 227 * 1024) return false;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return false;
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, SG_THREADS, smem) != cudaSuccess) return false;
+    return nb >= 1;
+}
+
+cudaError_t launch_decode_persistent(const PdArgs& a, int grid, size_t smem, cudaStream_t s) {
+    PdFn k = pd_kernel(a.d, 1 << a.lg_grp);
+    if (!k) return cudaErrorNotSupported;
+    cudaError_t e = cudaMemsetAsync(a.bar, 0, sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(SG_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: the grid barriers need it
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, a);
+}
+
 cudaError_t kernels_init() {
     cudaError_t e = gemv_attr_all<EPI_RAW>();
     if (e == cudaSuccess) e = gemv_attr_all<EPI_QKV>();

@@ -141,7 +141,13 @@ struct detint_model {
     int tc_prefill = 1;      // 0: prefill attention through the per-token kernel (tests compare both)
     int staged_decode = 1;   // 0: decode attention through the per-token kernel (tests compare both)
     int dec_cap = 0;         // keys the staged decode attention holds (0: unsupported shape)
-    int dec_staged = 0;      // this step uses the staged decode attention
+    int dec_staged = 0;      // this step's decode: 0 kernels (global K/V), 1 kernels (staged K/V), 2 one persistent launch
+    int persistent = 0;      // 1: decode steps as one persistent launch where supported (tests compare both)
+    int pd_ok = 0;           // the persistent step supports this shape
+    PdLayer* pd_layers = nullptr;
+    unsigned* pd_bar = nullptr;
+    size_t pd_smem = 0, pd_off[4] = {0, 0, 0, 0};
+    int pd_lg_ns = 0, pd_cap = 0, nsm = 0;
     int pf_ok = 0;           // the tensor-core prefill attention supports this shape
     CUtensorMap kmap, vmap;  // whole K / V^T caches for the prefill attention
     int32_t* qblk = nullptr; // prefill query blocks [Tcap + max_batch][4]
@@ -239,8 +245,12 @@ static cudaError_t gemm_epi(const int8_t* X, const int8_t* W, int M, int N, int 
 // m->rows (prefill) or for every token (decode, rows == nullptr).
 // Decode with at most 8 sequences: 5 kernels per layer chained by
 // programmatic dependent launch (weights stream ahead of the dependency).
+static int run_decode_persistent(detint_model* m, int T, const int32_t* tokens, int32_t* logits,
+                                 int32_t* next_tok, cudaStream_t s);
+
 static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32_t* logits,
                             int32_t* next_tok, cudaStream_t s) {
+    if (m->dec_staged == 2) return run_decode_persistent(m, T, tokens, logits, next_tok, s);
     const int H = m->H, d = m->d, nq = m->nq, nkv = m->nkv, F = m->F;
     const int nqkv = (nq + 2 * nkv) * d;
     // from 3 sequences on, each row is quantised once by a row kernel (one CTA
@@ -375,6 +385,88 @@ static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode
     return DETINT_OK;
 }
 
+// The persistent decode step: its shared-memory layout (weight ring, int8
+// activation tile, partial sums, gamma, residual/scale staging), the
+// attention scratch capacity, the per-layer pointer table and the grid
+// barrier words. Leaves pd_ok = 0 for shapes it does not cover.
+static int setup_persistent(detint_model* m) {
+    m->pd_ok = 0;
+    const int H = m->H, d = m->d, G = 1 << m->lg_grp, nqd = m->nq * d, F = m->F;
+    if ((H & (H - 1)) || !decode_persistent_supported(d, G)) return DETINT_OK;
+    for (int K : {H, nqd, F})
+        if ((K & 63) || (K > 1024 && (K & 1023))) return DETINT_OK;
+    if (cudaDeviceGetAttribute(&m->nsm, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess) return DETINT_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&m->nsm, cudaDevAttrMultiProcessorCount, dev);
+    const size_t Kmax = (size_t)std::max(H, std::max(nqd, F));
+    const size_t xs = 8 * (Kmax + 64), red = 4 * 1024 * 4, gam = ((size_t)H * 2 + 15) & ~(size_t)15;
+    for (int lg = 3; lg >= 1; --lg) {
+        const size_t ring = ((size_t)1 << lg) * 16 * 1088;
+        const size_t o_xs = ring, o_red = o_xs + xs, o_gam = o_red + red, o_hold = o_gam + gam;
+        const size_t total = o_hold + 512 * 4;
+        if (total > 220 * 1024) continue;
+        // attention scratch over the tile and partial sums: q [G][d], S [G][cap]
+        // int32, E_lo/E_hi [G][cap], P.V limbs [G][d][2] int32
+        const size_t region = o_gam - o_xs, fixed = (size_t)G * d + (size_t)G * d * 8;
+        if (region <= fixed) continue;
+        int cap = (int)((region - fixed) / ((size_t)G * 6));
+        cap &= ~15;
+        if (cap < 16 || !decode_persistent_fits(d, G, total)) continue;
+        m->pd_lg_ns = lg;
+        m->pd_smem = total;
+        m->pd_off[0] = o_xs; m->pd_off[1] = o_red; m->pd_off[2] = o_gam; m->pd_off[3] = o_hold;
+        m->pd_cap = std::min(cap, m->max_ctx);
+        break;
+    }
+    if (m->pd_smem == 0) return DETINT_OK;
+    std::vector<PdLayer> pl(m->L);
+    for (int l = 0; l < m->L; ++l) {
+        const LayerW& w = m->layers[l];
+        PdLayer& p = pl[l];
+        p.w_qkv = w.w_qkv; p.w_o = w.w_o; p.w_gu = w.w_gu; p.w_d = w.w_d;
+        p.m_qkv = w.m_qkv; p.m_o = w.m_o; p.m_gu = w.m_gu; p.m_d = w.m_d; p.kvp = w.kvp;
+        p.attn_gamma = w.attn_gamma; p.ffn_gamma = w.ffn_gamma; p.q_gamma = w.q_gamma; p.k_gamma = w.k_gamma;
+        p.kc = m->kcache + (size_t)l * m->kv_layer_elems;
+        p.vc = m->vcache + (size_t)l * m->kv_layer_elems;
+    }
+    if (cudaMalloc(&m->pd_layers, sizeof(PdLayer) * pl.size()) != cudaSuccess ||
+        cudaMalloc(&m->pd_bar, 2 * sizeof(unsigned)) != cudaSuccess)
+        return fail(DETINT_E_OOM, "persistent decode tables");
+    if (cudaMemcpy(m->pd_layers, pl.data(), sizeof(PdLayer) * pl.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(m->pd_bar, 0, 2 * sizeof(unsigned)) != cudaSuccess)
+        return fail(DETINT_E_CUDA, "persistent decode tables");
+    m->pd_ok = 1;
+    return DETINT_OK;
+}
+
+static int run_decode_persistent(detint_model* m, int T, const int32_t* tokens, int32_t* logits,
+                                 int32_t* next_tok, cudaStream_t s) {
+    PdArgs a{};
+    a.layers = m->pd_layers;
+    a.L = m->L; a.T = T; a.H = m->H; a.nq = m->nq; a.nkv = m->nkv; a.d = m->d; a.F = m->F; a.V = m->V;
+    a.lg_grp = m->lg_grp; a.qk_norm = m->qk_norm; a.max_pos = m->max_ctx; a.mbs = m->mbs;
+    a.lg_H = ilog2i(m->H);
+    a.eps_h = m->eps_h; a.eps_qk = m->eps_qk;
+    a.embed = m->embed; a.embed_m = m->embed_m; a.final_gamma = m->final_gamma;
+    a.rope_cos = m->rope_cos; a.rope_sin = m->rope_sin; a.block_table = m->block_table;
+    a.tokens = tokens; a.tok_seq = m->tok_seq; a.tok_pos = m->tok_pos; a.seq_len = m->seq_len_dev;
+    a.h = m->h; a.qkv = m->qkv; a.o = m->o; a.sbuf = m->sbuf; a.logits = logits ? logits : m->logits_int;
+    a.pval = m->pval; a.pidx = m->pidx; a.npart = m->npart; a.next_tok = next_tok; a.status = m->status;
+    a.bar = m->pd_bar;
+    const int nqkv = (m->nq + 2 * m->nkv) * m->d;
+    const int Ns[5] = {nqkv, m->H, 2 * m->F, m->H, m->V};
+    for (int p = 0; p < 5; ++p) {
+        const int Gp = (Ns[p] + 15) / 16;
+        a.rg[p][0] = Gp / m->nsm;
+        a.rg[p][1] = Gp % m->nsm;
+    }
+    a.lg_ns = m->pd_lg_ns;
+    a.attn_cap = m->pd_cap;
+    a.off_xs = m->pd_off[0]; a.off_red = m->pd_off[1]; a.off_gam = m->pd_off[2]; a.off_hold = m->pd_off[3];
+    CK(launch_decode_persistent(a, m->nsm, m->pd_smem, s));
+    return DETINT_OK;
+}
+
 // ------------------------------------------------------------------ ABI
 extern "C" {
 
@@ -408,6 +500,8 @@ void detint_free(detint_model* m) {
     if (m->block_table) cudaFree(m->block_table);
     if (m->seq_len_dev) cudaFree(m->seq_len_dev);
     if (m->status) cudaFree(m->status);
+    if (m->pd_layers) cudaFree(m->pd_layers);
+    if (m->pd_bar) cudaFree(m->pd_bar);
     if (m->pinned) cudaFreeHost(m->pinned);
     if (m->pinned_done) cudaEventDestroy(m->pinned_done);
     delete m;
@@ -584,6 +678,8 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
     if (rc != DETINT_OK) { detint_free(m); return rc; }
     ce = kernels_init();
     if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
+    rc = setup_persistent(m);
+    if (rc != DETINT_OK) { detint_free(m); return rc; }
     ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
     *out = m;
@@ -668,6 +764,7 @@ int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const
         int mx = 0;
         for (int i = 0; i < n_seq; ++i) mx = std::max(mx, m->seq_len[seq_ids[i]] + 1);
         m->dec_staged = (m->staged_decode && m->dec_cap > 0 && mx <= m->dec_cap) ? 1 : 0;
+        if (m->persistent && m->pd_ok && m->fused_decode && n_seq <= 8 && mx <= m->pd_cap) m->dec_staged = 2;
     }
     const bool graph = m->use_graph && s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread;
     if (!graph) {
@@ -778,6 +875,7 @@ int detint_set_option(detint_model* m, int option, int value) {
     else if (option == DETINT_OPT_FUSED_DECODE) { m->fused_decode = value; free_graphs(m); }
     else if (option == DETINT_OPT_TC_PREFILL) m->tc_prefill = value;
     else if (option == DETINT_OPT_STAGED_DECODE) { m->staged_decode = value; free_graphs(m); }
+    else if (option == DETINT_OPT_PERSISTENT) { m->persistent = value; free_graphs(m); }
     else return fail(DETINT_E_ARG, "unknown option");
     return DETINT_OK;
 }

@@ -168,10 +168,13 @@ int detint_sample(const int32_t* logits, int rows, int n, const detint_sampling_
  * kernel) and DETINT_OPT_STAGED_DECODE (1 = fused decode attention with the
  * sequence's cached K/V copied into shared memory before the step's data is
  * ready, the default while every context fits that copy; 0 = the attention
- * kernel that reads the cache from global memory). Every setting gives
- * bit-identical results. Errors: ARG. */
+ * kernel that reads the cache from global memory) and DETINT_OPT_PERSISTENT
+ * (1 = a fused decode step of up to 8 sequences runs as one cooperative
+ * launch of one CTA per SM with grid barriers between its phases, where the
+ * shape and context fit; 0 = one kernel per phase, the default, measured
+ * faster on GB300). Every setting gives bit-identical results. Errors: ARG. */
 enum { DETINT_OPT_GRAPH = 0, DETINT_OPT_FUSED_DECODE = 1, DETINT_OPT_TC_PREFILL = 2,
-       DETINT_OPT_STAGED_DECODE = 3 };
+       DETINT_OPT_STAGED_DECODE = 3, DETINT_OPT_PERSISTENT = 4 };
 int detint_set_option(detint_model* m, int option, int value);
 
 /* Shape of the loaded model: info[0..9] = n_layers, hidden, n_q, n_kv,

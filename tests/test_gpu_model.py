@@ -203,3 +203,23 @@ def test_staged_decode_capacity_crossing(torch_cuda, qwen_artifact):
         m.close()
     assert np.array_equal(out[True][0], out[False][0])
     assert out[True][1] == out[False][1]
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen", "llama"])
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_persistent_decode_equals_kernel_chain(torch_cuda, request, name, B):
+    """The one-launch decode step (cooperative grid, grid barriers between
+    phases) gives the kernel chain's logits and tokens, batch of B."""
+    path = request.getfixturevalue({"tiny": "tiny_artifact", "qwen": "qwen_artifact",
+                                    "llama": "llama_artifact"}[name])
+    V = {"tiny": 1024, "qwen": 151936, "llama": 128256}[name]
+    prompts = [synth.prompt_ids(12, i, n, V) for i, n in enumerate((9, 70, 33, 5, 128, 17, 64, 40)[:B])]
+    out = {}
+    for pers in (True, False):
+        m = _load(path, 8, 256)
+        m.set_persistent(pers)
+        out[pers] = m.generate(prompts, 12, keep_logits="hash")
+        assert not m.status().any()
+        m.close()
+    assert np.array_equal(out[True][0], out[False][0])
+    assert out[True][1] == out[False][1]
