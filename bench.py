@@ -269,6 +269,48 @@ def run_gemm_sweep(args):
                       "sweep": rows}), flush=True)
 
 
+def _decode_rate(pkg, path, B, K, W, dev, dist, ws):
+    """(tok/s over all ranks, ms per step) of K graph-replayed decode steps
+    of B sequences, inputs resident on the device."""
+    import torch
+    import synth
+    max_ctx = PROMPT_LEN + W + 2 * K + 280
+    model = pkg.Model(path, max_batch=B, max_ctx=((max_ctx + 63) // 64) * 64)
+    V = model.vocab
+    prompts = [synth.prompt_ids(SEED, 0, PROMPT_LEN, V)]
+    prompts += [synth.prompt_ids(SEED, 100 + i, int(n), V)
+                for i, n in enumerate(synth.coprompt_lengths(SEED, B - 1))]
+    s = model.stream
+    seq_ids = list(range(B))
+    cu = np.zeros(B + 1, np.int64)
+    cu[1:] = np.cumsum([len(p) for p in prompts])
+    flat = torch.tensor(np.concatenate(prompts), dtype=torch.int32, device=dev)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(s):
+        model.prefill(seq_ids, flat, cu, None, tok)
+        for _ in range(W):
+            model.decode_step(seq_ids, tok, None, tok)
+    s.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(K):
+            model.decode_step(seq_ids, tok, None, tok)
+        e1.record(s)
+    s.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    model.close()
+    return B * K * ws / (ms / 1e3), ms / K
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -277,6 +319,8 @@ def main():
     ap.add_argument("--impl", default="detint", choices=["detint", "reference"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-companion", dest="companion", action="store_false",
+                    help="skip the B=8 companion measurement of the decode line")
     ap.add_argument("--shape", default=None, help="M,N,K for --workload lmhead (default 1,151936,1024 "
                     "with M = --batch)")
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prefill workload: sequences")
@@ -412,11 +456,22 @@ def main():
     step = {"bytes": step_bytes, "achieved_gbs": step_bytes / (ms / K / 1e3) / 1e9,
             "frac": step_bytes / (ms / K / 1e3) / 1e9 / peak}
 
+    model.close()
+    # companion number for the metric's second batch size: the same workload
+    # with 8 sequences (row 0 = the prompt above, 7 seeded co-prompts)
+    other = None
+    if args.companion and B != 8:
+        other = _decode_rate(pkg, path, 8, K, W, dev, dist, ws)
+
     if rank == 0:
         cb = None
         if not args.no_cpu_baseline and ws == 1:
             cb = cpu_baseline()
-        gpu_launches = K * (1 + L * 10 + 3)
+        # kernels per fused decode step: embedding, 5 per layer (QKV, attention,
+        # o_proj, gate/up, down; plus 4 row-quantisation kernels per layer from
+        # 3 sequences on), lm_head (+ its row kernel), final argmax
+        sep = B >= 3
+        gpu_launches = K * (1 + L * (9 if sep else 5) + (2 if sep else 1) + 1)
         line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": K,
                 "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "int8/int32", "data": "synthetic",
@@ -426,8 +481,10 @@ def main():
                            "l2": "weights 596 MB > 129 MB L2 every step (no flush needed)"},
                 "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline,
                 "step_roofline": step, "clocks": clk.summary(), "cpu_baseline": cb}
+        if other is not None:
+            line["batch8"] = {"value": other[0], "unit": "tok/s", "ms_per_step": other[1],
+                              "config": "same workload, B=8 (7 seeded co-prompts of 16-256 tokens)"}
         print(json.dumps(line), flush=True)
-    model.close()
     if dist:
         dist.destroy_process_group()
 

@@ -25,7 +25,7 @@ ERRORS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "token id o
 # every entry point of include/detint.h
 SYMBOLS = ["detint_load", "detint_prefill", "detint_decode_step", "detint_gemm_i8",
            "detint_reset_seq", "detint_seq_len", "detint_status", "detint_set_graph",
-           "detint_set_option", "detint_argmax_noalloc", "detint_sample",
+           "detint_set_option", "detint_argmax_noalloc", "detint_sample", "detint_fork_seq",
            "detint_model_info", "detint_free", "detint_strerror", "detint_last_error"]
 
 
@@ -55,6 +55,7 @@ def lib():
         L.detint_set_graph.argtypes = [vp, C.c_int]
         L.detint_set_option.argtypes = [vp, C.c_int, C.c_int]
         L.detint_argmax_noalloc.argtypes = [vp, C.c_int, C.c_int, vp, vp]
+        L.detint_fork_seq.argtypes = [vp, C.c_int, C.c_int, C.c_int, vp]
         L.detint_sample.argtypes = [vp, C.c_int, C.c_int, C.POINTER(SamplingParams), vp, vp]
         L.detint_model_info.argtypes = [vp, i32p]
         L.detint_free.argtypes = [vp]
@@ -186,6 +187,11 @@ class Model:
 
     def reset_seq(self, seq_id: int):
         _check(lib().detint_reset_seq(self._h, int(seq_id)), "detint_reset_seq")
+
+    def fork_seq(self, src: int, dst: int, n_tokens: int):
+        """dst starts with src's first n_tokens positions (shared KV blocks)."""
+        _check(lib().detint_fork_seq(self._h, int(src), int(dst), int(n_tokens), self.stream.cuda_stream),
+               "detint_fork_seq")
 
     def seq_len(self, seq_id: int) -> int:
         v = C.c_int32()

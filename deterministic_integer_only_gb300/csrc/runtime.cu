@@ -126,6 +126,12 @@ struct detint_model {
     int8_t *kcache = nullptr, *vcache = nullptr;
     size_t kv_layer_elems;
     int32_t* block_table = nullptr;
+    // paged KV pool: blocks are taken from a free list as sequences grow and
+    // shared (reference counted) between sequences forked from one prefix
+    std::vector<int32_t> bt_host;          // [max_batch][mbs] mirror of block_table
+    std::vector<std::vector<int>> seq_blocks;
+    std::vector<int> refcnt, free_blocks;
+    bool bt_dirty = false;
     int32_t* seq_len_dev = nullptr;
     std::vector<int> seq_len;
     // scratch for up to Tcap tokens
@@ -383,6 +389,41 @@ static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode
     CK(launch_argmax_final(m->pval, m->pidx, R, m->npart, next_tok, m->tok_seq,
                            decode ? m->seq_len_dev : nullptr, s));
     return DETINT_OK;
+}
+
+// Blocks for positions [0, len) of sequence sid: take free blocks for the
+// missing tail. Returns CTX when the pool is exhausted.
+static int ensure_blocks(detint_model* m, int sid, int len) {
+    std::vector<int>& sb = m->seq_blocks[sid];
+    const int need = (len + KV_BLK - 1) / KV_BLK;
+    if (need > m->mbs) return fail(DETINT_E_CTX, "context exceeds max_ctx");
+    while ((int)sb.size() < need) {
+        if (m->free_blocks.empty()) return fail(DETINT_E_CTX, "KV block pool exhausted");
+        const int b = m->free_blocks.back();
+        m->free_blocks.pop_back();
+        m->refcnt[b] = 1;
+        m->bt_host[(size_t)sid * m->mbs + sb.size()] = b;
+        sb.push_back(b);
+        m->bt_dirty = true;
+    }
+    return DETINT_OK;
+}
+
+static void release_blocks(detint_model* m, int sid) {
+    for (int b : m->seq_blocks[sid])
+        if (--m->refcnt[b] == 0) m->free_blocks.push_back(b);
+    m->seq_blocks[sid].clear();
+    for (int i = 0; i < m->mbs; ++i) m->bt_host[(size_t)sid * m->mbs + i] = 0;
+    m->bt_dirty = true;
+}
+
+// upload the block table when it changed (stream-ordered, before the kernels
+// that read it)
+static int sync_block_table(detint_model* m, cudaStream_t s) {
+    if (!m->bt_dirty) return DETINT_OK;
+    int rc = stage_copies(m, s, {{m->block_table, &m->bt_host}});
+    if (rc == DETINT_OK) m->bt_dirty = false;
+    return rc;
 }
 
 // The persistent decode step: its shared-memory layout (weight ring, int8
@@ -647,8 +688,14 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
         detint_free(m);
         return fail(DETINT_E_OOM, "KV cache allocation failed");
     }
-    std::vector<int32_t> bt((size_t)max_batch * m->mbs);
-    for (size_t i = 0; i < bt.size(); ++i) bt[i] = (int32_t)i;   // sequence s owns blocks [s*mbs, (s+1)*mbs)
+    // every entry starts at block 0 (a valid block whose keys lie past every
+    // sequence's length, so they are never used); blocks are assigned on demand
+    std::vector<int32_t> bt((size_t)max_batch * m->mbs, 0);
+    m->bt_host = bt;
+    m->seq_blocks.assign(max_batch, {});
+    m->refcnt.assign(m->nblocks, 0);
+    m->free_blocks.clear();
+    for (int b = m->nblocks - 1; b >= 0; --b) m->free_blocks.push_back(b);
     if (cudaMalloc(&m->block_table, bt.size() * 4) != cudaSuccess ||
         cudaMalloc(&m->seq_len_dev, (size_t)max_batch * 4) != cudaSuccess ||
         cudaMalloc(&m->status, ST_N * 4) != cudaSuccess) {
@@ -723,6 +770,12 @@ int detint_prefill(detint_model* m, int n_seq, const int32_t* seq_ids, const int
     }
     std::vector<int32_t> newlen(m->seq_len.begin(), m->seq_len.end());
     for (int i = 0; i < n_seq; ++i) newlen[seq_ids[i]] += cu_lens[i + 1] - cu_lens[i];
+    for (int i = 0; i < n_seq; ++i) {
+        rc = ensure_blocks(m, seq_ids[i], newlen[seq_ids[i]]);
+        if (rc) return rc;
+    }
+    rc = sync_block_table(m, s);
+    if (rc) return rc;
     // query blocks of up to 64 / G tokens of one sequence, the longest key
     // ranges first so that the heaviest CTAs start first
     const int bq = PF_ROWS >> m->lg_grp;
@@ -759,6 +812,12 @@ int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const
         if (m->seq_len[seq_ids[i]] + 1 > m->max_ctx) return fail(DETINT_E_CTX, "decode exceeds max_ctx");
     cudaStream_t s = (cudaStream_t)sp;
     rc = ensure_scratch(m, n_seq);
+    if (rc) return rc;
+    for (int i = 0; i < n_seq; ++i) {
+        rc = ensure_blocks(m, seq_ids[i], m->seq_len[seq_ids[i]] + 1);
+        if (rc) return rc;
+    }
+    rc = sync_block_table(m, s);
     if (rc) return rc;
     {
         int mx = 0;
@@ -839,8 +898,51 @@ int detint_reset_seq(detint_model* m, int seq_id) {
     if (seq_id < 0 || seq_id >= m->max_batch) return fail(DETINT_E_SEQ, "sequence id out of range");
     CK(cudaDeviceSynchronize());
     m->seq_len[seq_id] = 0;
+    release_blocks(m, seq_id);
     const int32_t z = 0;
     CK(cudaMemcpy(m->seq_len_dev + seq_id, &z, 4, cudaMemcpyHostToDevice));
+    return DETINT_OK;
+}
+
+int detint_fork_seq(detint_model* m, int src, int dst, int n_tokens, detint_stream_t sp) {
+    if (!m) return fail(DETINT_E_ARG, "null model");
+    if (src < 0 || src >= m->max_batch || dst < 0 || dst >= m->max_batch || src == dst)
+        return fail(DETINT_E_SEQ, "sequence id out of range or equal");
+    if (m->seq_len[dst] != 0) return fail(DETINT_E_SEQ, "the destination sequence is not empty");
+    if (n_tokens < 0 || n_tokens > m->seq_len[src]) return fail(DETINT_E_ARG, "n_tokens outside the source");
+    cudaStream_t s = (cudaStream_t)sp;
+    const int full = n_tokens / KV_BLK, part = n_tokens % KV_BLK;
+    std::vector<int>& sb = m->seq_blocks[src];
+    std::vector<int>& db = m->seq_blocks[dst];
+    for (int i = 0; i < full; ++i) {          // whole blocks: shared
+        const int b = sb[i];
+        ++m->refcnt[b];
+        m->bt_host[(size_t)dst * m->mbs + i] = b;
+        db.push_back(b);
+    }
+    if (part) {                               // the partial block: a private copy
+        if (m->free_blocks.empty()) { release_blocks(m, dst); return fail(DETINT_E_CTX, "KV block pool exhausted"); }
+        const int b = m->free_blocks.back();
+        m->free_blocks.pop_back();
+        m->refcnt[b] = 1;
+        m->bt_host[(size_t)dst * m->mbs + full] = b;
+        db.push_back(b);
+        const size_t blk = (size_t)m->nkv * KV_BLK * m->d;   // bytes of one block of one layer
+        for (int l = 0; l < m->L; ++l) {
+            const size_t base = (size_t)l * m->kv_layer_elems;
+            CK(cudaMemcpyAsync(m->kcache + base + (size_t)b * blk, m->kcache + base + (size_t)sb[full] * blk,
+                               blk, cudaMemcpyDeviceToDevice, s));
+            CK(cudaMemcpyAsync(m->vcache + base + (size_t)b * blk, m->vcache + base + (size_t)sb[full] * blk,
+                               blk, cudaMemcpyDeviceToDevice, s));
+        }
+    }
+    m->bt_dirty = true;
+    int rc = sync_block_table(m, s);
+    if (rc) return rc;
+    std::vector<int32_t> nl(1, n_tokens);
+    rc = stage_copies(m, s, {{m->seq_len_dev + dst, &nl}});
+    if (rc) return rc;
+    m->seq_len[dst] = n_tokens;
     return DETINT_OK;
 }
 

@@ -132,6 +132,17 @@ int detint_status(detint_model* m, int32_t* flags, detint_stream_t s);
  * (README, "Usage": use_graph). */
 int detint_set_graph(detint_model* m, int enable);
 
+/* Start sequence dst (which must be empty) with the first n_tokens positions
+ * of sequence src, without recomputing them: whole 64-token KV blocks are
+ * shared by reference count, the partial last block is copied, and later
+ * appends to either sequence go to blocks of its own. Continuing dst gives
+ * the same logits, bit for bit, as prefilling the same tokens afresh
+ * (scheduler invariance: BitExact LLM post, "What the checks actually
+ * compare" lists shared prefixes among the tested scheduler changes).
+ * Stream-ordered on s. Errors: ARG, SEQ (ids out of range or equal, dst not
+ * empty), CTX (block pool exhausted), CUDA. */
+int detint_fork_seq(detint_model* m, int src, int dst, int n_tokens, detint_stream_t s);
+
 /* Integer sampling parameters of one row (see detint_sample). */
 typedef struct {
     uint64_t seed;      /* SplitMix64 seed */
