@@ -154,6 +154,9 @@ def cpu_baseline(seconds: float = 12.0):
 # int8 tensor-pipe peak of this GPU: mma.sync m16n8k32 s8, measured with a
 # register-only issue loop on a GB300 (measurement)
 MMA_S8_PEAK_TOPS = 150.3
+# DRAM traffic of one lm_head GEMV launch at M=1, read + write, from one ncu
+# capture of the current kernel (profiles/k_sgemv_lmhead_151936x1024.md)
+LMHEAD_DRAM_BYTES = 155664896 + 2895104
 
 
 def run_prefill(args):
@@ -444,7 +447,10 @@ def main():
     achieved = kbytes / (kms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": "k_sgemv (decode streaming GEMV), lm_head shape 151936x1024, M=%d" % B,
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": kbytes,
+                "peak_kind": peak_kind, "traffic": LMHEAD_DRAM_BYTES if B == 1 else None,
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch at M=1 "
+                                  "(profiles/k_sgemv_lmhead_151936x1024.md)",
+                "bytes_per_launch": kbytes,
                 "us_per_launch": kms * 1e3, "us_per_launch_l2_warm": kms_warm * 1e3,
                 "timing": "CUDA events around graph replays; L2 evicted before every launch"}
     # whole-step roofline: algorithmic bytes of one decode step
