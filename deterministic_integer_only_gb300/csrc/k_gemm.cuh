@@ -43,13 +43,18 @@ __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 12
 template <int MODE>
 __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constant__ CUtensorMap mapA,
                                                             const __grid_constant__ CUtensorMap mapW,
-                                                            int M, int N, int K, Epi ep) {
+                                                            int M, int N, int K, Epi ep, int ksl) {
     extern __shared__ unsigned char gsm_raw[];
     __shared__ unsigned long long full[GM_STAGES], empty[GM_STAGES];
     unsigned char* gsm = (unsigned char*)(((uintptr_t)gsm_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int m0 = blockIdx.y * GM_BM, n0 = blockIdx.x * GM_BN;
-    const int nk = (K + GM_BK - 1) / GM_BK;
+    // split K (raw int32 output only): this CTA takes k-tiles [kt0, kt0 + nk)
+    // and adds its partial sums into the zeroed output; integer addition is
+    // exact, so the result does not depend on the order of the adds
+    const int nk_all = (K + GM_BK - 1) / GM_BK;
+    const int kt0 = blockIdx.z * ksl;
+    const int nk = min(nk_all, kt0 + ksl) - kt0;
 
     if (tid == 0) {
         for (int s = 0; s < GM_STAGES; ++s) {
@@ -70,8 +75,8 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
                 const uint32_t fb = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(fb, GM_STAGE_BYTES);
                 const uint32_t base = smem_u32(gsm + (size_t)s * GM_STAGE_BYTES);
-                tma_load_2d(base, &mapA, kt * GM_BK, m0, fb);
-                tma_load_2d(base + GM_BM * GM_BK, &mapW, kt * GM_BK, n0, fb);
+                tma_load_2d(base, &mapA, (kt0 + kt) * GM_BK, m0, fb);
+                tma_load_2d(base + GM_BM * GM_BK, &mapW, (kt0 + kt) * GM_BK, n0, fb);
             }
         }
         return;
@@ -135,6 +140,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
                         yu = sat_b(yu, 1 << 24);
                         ep.out[(size_t)m * ep.ldo + (n >> 1)] = swiglu_tab((int)yg, (int)yu);
                     }
+                } else if (MODE == EPI_RAW && gridDim.z > 1) {
+                    if (n < N) atomicAdd(ep.out + (size_t)m * ep.ldo + n, c0);
+                    if (n + 1 < N) atomicAdd(ep.out + (size_t)m * ep.ldo + n + 1, c1);
                 } else {
                     if (n < N) epi_store<MODE>(ep, m, n, c0);
                     if (n + 1 < N) epi_store<MODE>(ep, m, n + 1, c1);

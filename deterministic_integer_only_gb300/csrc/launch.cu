@@ -267,12 +267,26 @@ cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, i
     e = make_map(&ma, A, M, K);
     if (e == cudaSuccess) e = make_map(&mw, W, N, K);
     if (e != cudaSuccess) return e;
-    const dim3 grid((N + GM_BN - 1) / GM_BN, (M + GM_BM - 1) / GM_BM);
+    const int tiles_n = (N + GM_BN - 1) / GM_BN, tiles_m = (M + GM_BM - 1) / GM_BM;
+    const int nk = (K + GM_BK - 1) / GM_BK;
+    // raw output with fewer tiles than SMs: split K over up to two CTAs per
+    // SM, at least two k-tiles each, partial sums added into a zeroed C
+    int splits = 1, ksl = nk;
+    if (mode == EPI_RAW && g_num_sms > 0 && tiles_n * tiles_m < g_num_sms && nk >= 4) {
+        splits = std::min(nk / 2, (2 * g_num_sms + tiles_n * tiles_m - 1) / (tiles_n * tiles_m));
+        ksl = (nk + splits - 1) / splits;
+        splits = (nk + ksl - 1) / ksl;
+        if (splits > 1) {
+            e = cudaMemsetAsync(ep.out, 0, (size_t)M * ep.ldo * sizeof(int32_t), s);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    const dim3 grid(tiles_n, tiles_m, splits);
     switch (mode) {
-        case EPI_RAW: k_gemm_tma<EPI_RAW><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep); break;
-        case EPI_QKV: k_gemm_tma<EPI_QKV><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep); break;
-        case EPI_RESADD: k_gemm_tma<EPI_RESADD><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep); break;
-        case EPI_SWIGLU: k_gemm_tma<EPI_SWIGLU><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep); break;
+        case EPI_RAW: k_gemm_tma<EPI_RAW><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl); break;
+        case EPI_QKV: k_gemm_tma<EPI_QKV><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl); break;
+        case EPI_RESADD: k_gemm_tma<EPI_RESADD><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl); break;
+        case EPI_SWIGLU: k_gemm_tma<EPI_SWIGLU><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
