@@ -40,7 +40,9 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, int& r0, int& r1, int& r2
 // byte offset of 16-byte chunk c of tile row r under the 128-byte swizzle
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-template <int MODE>
+// BM: rows of the CTA tile (128, or 64 for at most 64 rows so that no MMA
+// works on zero rows); the 8 consumer warps tile it as (BM / 64) x (8 / (BM / 64))
+template <int MODE, int BM>
 __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constant__ CUtensorMap mapA,
                                                             const __grid_constant__ CUtensorMap mapW,
                                                             int M, int N, int K, Epi ep, int ksl) {
@@ -48,7 +50,10 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
     __shared__ unsigned long long full[GM_STAGES], empty[GM_STAGES];
     unsigned char* gsm = (unsigned char*)(((uintptr_t)gsm_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.y * GM_BM, n0 = blockIdx.x * GM_BN;
+    constexpr int WN = BM == 128 ? 4 : 8;            // warps along N
+    constexpr int NTW = GM_BN / WN / 8;              // 8-column n-tiles per warp
+    constexpr int STAGE = (BM + GM_BN) * GM_BK;
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * GM_BN;
     // split K (raw int32 output only): this CTA takes k-tiles [kt0, kt0 + nk)
     // and adds its partial sums into the zeroed output; integer addition is
     // exact, so the result does not depend on the order of the adds
@@ -73,47 +78,47 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
                     !mbar_wait(smem_u32(&empty[s]), ((kt / GM_STAGES) - 1) & 1))
                     ep.status[ST_TIMEOUT] = 1;
                 const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, GM_STAGE_BYTES);
-                const uint32_t base = smem_u32(gsm + (size_t)s * GM_STAGE_BYTES);
+                mbar_arrive_expect_tx(fb, STAGE);
+                const uint32_t base = smem_u32(gsm + (size_t)s * STAGE);
                 tma_load_2d(base, &mapA, (kt0 + kt) * GM_BK, m0, fb);
-                tma_load_2d(base + GM_BM * GM_BK, &mapW, (kt0 + kt) * GM_BK, n0, fb);
+                tma_load_2d(base + BM * GM_BK, &mapW, (kt0 + kt) * GM_BK, n0, fb);
             }
         }
         return;
     }
 
-    const int wm = warp >> 2, wn = warp & 3;     // 2 x 4 warps
+    const int wm = warp / WN, wn = warp % WN;
     const int g = lane >> 2, tq = lane & 3;
     const int mi = lane >> 3, ri = lane & 7;     // ldmatrix matrix / row within it
-    int acc[4][4][4];
+    int acc[4][NTW][4];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b][0] = acc[a][b][1] = acc[a][b][2] = acc[a][b][3] = 0;
+        for (int b = 0; b < NTW; ++b) acc[a][b][0] = acc[a][b][1] = acc[a][b][2] = acc[a][b][3] = 0;
 
     for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % GM_STAGES;
         if (!mbar_wait(smem_u32(&full[s]), (kt / GM_STAGES) & 1)) ep.status[ST_TIMEOUT] = 1;
-        const uint32_t tA = smem_u32(gsm + (size_t)s * GM_STAGE_BYTES);
-        const uint32_t tW = tA + GM_BM * GM_BK;
+        const uint32_t tA = smem_u32(gsm + (size_t)s * STAGE);
+        const uint32_t tW = tA + BM * GM_BK;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            int af[4][4], bf[4][2];
+            int af[4][4], bf[NTW][2];
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {
                 const int r = wm * 64 + mt * 16 + ri + 8 * (mi & 1);
                 ldsm_x4(tA + swz(r, 2 * kk + (mi >> 1)), af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
             }
 #pragma unroll
-            for (int np = 0; np < 2; ++np) {
-                const int r = wn * 32 + np * 16 + ri + 8 * (mi >> 1);
+            for (int np = 0; np < NTW / 2; ++np) {
+                const int r = wn * (NTW * 8) + np * 16 + ri + 8 * (mi >> 1);
                 ldsm_x4(tW + swz(r, 2 * kk + (mi & 1)), bf[2 * np][0], bf[2 * np][1],
                         bf[2 * np + 1][0], bf[2 * np + 1][1]);
             }
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
+                for (int nt = 0; nt < NTW; ++nt)
                     mma_s8(acc[mt][nt], af[mt][0], af[mt][1], af[mt][2], af[mt][3], bf[nt][0], bf[nt][1]);
         }
         __syncwarp();
@@ -124,8 +129,8 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int n = n0 + wn * 32 + nt * 8 + 2 * tq;
+        for (int nt = 0; nt < NTW; ++nt) {
+            const int n = n0 + wn * (NTW * 8) + nt * 8 + 2 * tq;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int m = m0 + wm * 64 + mt * 16 + g + 8 * h;

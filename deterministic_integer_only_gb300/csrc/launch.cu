@@ -245,16 +245,36 @@ static cudaError_t get_encode() {
 
 // int8 matrix [rows][K] (K % 16 == 0), 128 x 128-byte boxes, 128-byte swizzle,
 // zero fill outside the matrix
-static cudaError_t make_map(CUtensorMap* map, const void* base, int rows, int K) {
+static cudaError_t make_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows = 128) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K};
-    cuuint32_t box[2] = {(cuuint32_t)GM_BK, 128};
+    cuuint32_t box[2] = {(cuuint32_t)GM_BK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+using GemmFn = void (*)(CUtensorMap, CUtensorMap, int, int, int, Epi, int);
+static GemmFn gemm_kernel(int mode, int bm) {
+    if (bm == 64) {
+        switch (mode) {
+            case EPI_RAW: return k_gemm_tma<EPI_RAW, 64>;
+            case EPI_QKV: return k_gemm_tma<EPI_QKV, 64>;
+            case EPI_RESADD: return k_gemm_tma<EPI_RESADD, 64>;
+            case EPI_SWIGLU: return k_gemm_tma<EPI_SWIGLU, 64>;
+            default: return nullptr;
+        }
+    }
+    switch (mode) {
+        case EPI_RAW: return k_gemm_tma<EPI_RAW, 128>;
+        case EPI_QKV: return k_gemm_tma<EPI_QKV, 128>;
+        case EPI_RESADD: return k_gemm_tma<EPI_RESADD, 128>;
+        case EPI_SWIGLU: return k_gemm_tma<EPI_SWIGLU, 128>;
+        default: return nullptr;
+    }
 }
 
 cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, int mode,
@@ -264,10 +284,11 @@ cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, i
     cudaError_t e = get_encode();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mw;
-    e = make_map(&ma, A, M, K);
+    const int BM = M <= 64 ? 64 : 128;    // no tile rows past a short M
+    e = make_map(&ma, A, M, K, BM);
     if (e == cudaSuccess) e = make_map(&mw, W, N, K);
     if (e != cudaSuccess) return e;
-    const int tiles_n = (N + GM_BN - 1) / GM_BN, tiles_m = (M + GM_BM - 1) / GM_BM;
+    const int tiles_n = (N + GM_BN - 1) / GM_BN, tiles_m = (M + BM - 1) / BM;
     const int nk = (K + GM_BK - 1) / GM_BK;
     // raw output with fewer tiles than SMs: split K over up to two CTAs per
     // SM, at least two k-tiles each, partial sums added into a zeroed C
@@ -282,13 +303,9 @@ cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, i
         }
     }
     const dim3 grid(tiles_n, tiles_m, splits);
-    switch (mode) {
-        case EPI_RAW: k_gemm_tma<EPI_RAW><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl); break;
-        case EPI_QKV: k_gemm_tma<EPI_QKV><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl); break;
-        case EPI_RESADD: k_gemm_tma<EPI_RESADD><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl); break;
-        case EPI_SWIGLU: k_gemm_tma<EPI_SWIGLU><<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl); break;
-        default: return cudaErrorInvalidValue;
-    }
+    auto k = gemm_kernel(mode, BM);
+    if (!k) return cudaErrorInvalidValue;
+    k<<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl);
     return cudaGetLastError();
 }
 
@@ -399,10 +416,10 @@ cudaError_t kernels_init() {
     const int sgm = (int)SG_SMEM_MAX;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_RESADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tma<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+    for (int bm : {64, 128})
+        for (int mode : {EPI_RAW, EPI_QKV, EPI_RESADD, EPI_SWIGLU})
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gemm_kernel(mode, bm), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     for (int lg = 0; lg < 4 && e == cudaSuccess; ++lg) {
         e = cudaFuncSetAttribute(attn_dec_kernel(128, lg), cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM_MAX);
         if (e == cudaSuccess)

@@ -77,6 +77,21 @@ def test_gemm_llama_sweep_sampled(torch_cuda, M, N, K):
     assert np.array_equal(got, A @ B.T)
 
 
+@pytest.mark.parametrize("M,N,K", [(33, 136, 144), (50, 520, 1040), (64, 256, 2064), (65, 136, 1040),
+                                   (100, 520, 2064), (200, 392, 784), (64, 130, 4112)])
+def test_gemm_short_rows_and_split_k_exact(torch_cuda, M, N, K):
+    """Every entry of the 64-row-tile and split-K paths (ragged M, N and a
+    last k-tile that is partly past K) against numpy int64."""
+    torch = torch_cuda
+    import deterministic_integer_only_gb300 as pkg
+    rng = np.random.default_rng(M * 7 + N + K)
+    A = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    B = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    c = torch.full((M, N), 12345, dtype=torch.int32, device="cuda")
+    pkg.detint_gemm_i8(torch.tensor(A, device="cuda"), torch.tensor(B, device="cuda"), c)
+    assert np.array_equal(c.cpu().numpy(), A.astype(np.int64) @ B.astype(np.int64).T)
+
+
 def test_gemm_rejects_bad_k(torch_cuda):
     import deterministic_integer_only_gb300 as pkg
     torch = torch_cuda
