@@ -91,6 +91,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time: replicas run independently, so the job's
+    throughput is every rank's units over this time (no data exchange)."""
+    import torch
+    if dist is None:
+        return ms
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -307,9 +318,7 @@ def _decode_rate(pkg, path, B, K, W, dev, dist, ws):
     s.synchronize()
     ms = e0.elapsed_time(e1)
     if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dist, dev)
     model.close()
     return B * K * ws / (ms / 1e3), ms / K
 
@@ -396,9 +405,7 @@ def main():
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dist, dev)
         dist.barrier()
     value = B * K * ws / (ms / 1e3)
 
