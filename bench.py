@@ -170,6 +170,54 @@ MMA_S8_PEAK_TOPS = 150.3
 LMHEAD_DRAM_BYTES = 155664896 + 2895104
 
 
+def run_llama_b32(args):
+    """Llama-3.2-1B-shaped decode at batch 32 with 1024-token seeded contexts:
+    32 x 1024 prefilled, then K timed decode steps (CUDA-graph replays)."""
+    import torch
+    import synth
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+    B, C = 32, 1024
+    K, W = args.steps, args.warmup
+    path = synth.ensure_artifact("llama-1b", SEED)
+    model = pkg.Model(path, max_batch=B, max_ctx=((C + W + K + 64) // 64) * 64)
+    dev = torch.device("cuda")
+    prompts = [synth.prompt_ids(9, i, C, model.vocab) for i in range(B)]
+    flat = torch.tensor(np.concatenate(prompts), dtype=torch.int32, device=dev)
+    cu = np.arange(B + 1) * C
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    s = model.stream
+    ids = list(range(B))
+    with torch.cuda.stream(s):
+        model.prefill(ids, flat, cu, None, tok)
+        for _ in range(W):
+            model.decode_step(ids, tok, None, tok)
+    s.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(K):
+            model.decode_step(ids, tok, None, tok)
+        e1.record(s)
+    s.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    L, H, nq, nkv, d, F, V = (model.n_layers, model.hidden, model.n_q, model.n_kv, model.head_dim,
+                              model.ffn, model.vocab)
+    wbytes = L * ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F) + V * H
+    kv = L * nkv * d * 2 * (C + W + K / 2) * B
+    peak, peak_kind = _peaks()
+    step_bytes = wbytes + kv + 4 * B * V
+    line = {"metric": "decode tok/s (Llama-3.2-1B shape, B=32, 1024-token contexts)",
+            "value": B / (ms / 1e3), "unit": "tok/s", "ms_per_step": ms, "steps": K, "warmup": W,
+            "step_roofline": {"bytes": step_bytes, "achieved_gbs": step_bytes / (ms / 1e3) / 1e9,
+                              "frac": step_bytes / (ms / 1e3) / 1e9 / peak, "peak_kind": peak_kind},
+            "dtype": "int8/int32", "data": "synthetic"}
+    print(json.dumps(line), flush=True)
+    model.close()
+
+
 def run_prefill(args):
     """Prefill throughput: 4 sequences x 4096 seeded tokens on the Qwen3-0.6B
     shape in one detint_prefill call (last-position logits per sequence)."""
@@ -337,7 +385,8 @@ def main():
                     "with M = --batch)")
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prefill workload: sequences")
     ap.add_argument("--prefill-len", type=int, default=4096, help="prefill workload: tokens each")
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "gemm", "lmhead"],
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "prefill", "gemm", "lmhead", "llama-b32"],
                     help="decode (the headline line), prefill (4 x 4096 prompt throughput) or "
                          "gemm (exact int8 GEMM sweep over the Llama-3.2-1B projection shapes)")
     args = ap.parse_args()
@@ -345,6 +394,8 @@ def main():
         return run_reference(args)
     if args.workload == "prefill":
         return run_prefill(args)
+    if args.workload == "llama-b32":
+        return run_llama_b32(args)
     if args.workload == "gemm":
         return run_gemm_sweep(args)
     if args.workload == "lmhead":

@@ -40,18 +40,21 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, int& r0, int& r1, int& r2
 // byte offset of 16-byte chunk c of tile row r under the 128-byte swizzle
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-// BM: rows of the CTA tile (128, or 64 for at most 64 rows so that no MMA
-// works on zero rows); the 8 consumer warps tile it as (BM / 64) x (8 / (BM / 64))
+// BM: rows of the CTA tile (128; 64 or 32 for short M, so that few MMAs work
+// on zero rows); the 8 consumer warps tile it as WM x WN, each warp
+// MT m16 tiles by NTW n8 tiles
 template <int MODE, int BM>
 __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constant__ CUtensorMap mapA,
                                                             const __grid_constant__ CUtensorMap mapW,
-                                                            int M, int N, int K, Epi ep, int ksl) {
+                                                            int M, int N, int K, Epi ep, int ksl,
+                                                            int32_t* wsp, int* tcnt) {
     extern __shared__ unsigned char gsm_raw[];
     __shared__ unsigned long long full[GM_STAGES], empty[GM_STAGES];
     unsigned char* gsm = (unsigned char*)(((uintptr_t)gsm_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int WN = BM == 128 ? 4 : 8;            // warps along N
     constexpr int NTW = GM_BN / WN / 8;              // 8-column n-tiles per warp
+    constexpr int MT = BM == 32 ? 2 : 4;             // 16-row m-tiles per warp
     constexpr int STAGE = (BM + GM_BN) * GM_BK;
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * GM_BN;
     // split K (raw int32 output only): this CTA takes k-tiles [kt0, kt0 + nk)
@@ -90,9 +93,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
     const int wm = warp / WN, wn = warp % WN;
     const int g = lane >> 2, tq = lane & 3;
     const int mi = lane >> 3, ri = lane & 7;     // ldmatrix matrix / row within it
-    int acc[4][NTW][4];
+    int acc[MT][NTW][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < MT; ++a)
 #pragma unroll
         for (int b = 0; b < NTW; ++b) acc[a][b][0] = acc[a][b][1] = acc[a][b][2] = acc[a][b][3] = 0;
 
@@ -103,9 +106,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
         const uint32_t tW = tA + BM * GM_BK;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            int af[4][4], bf[NTW][2];
+            int af[MT][4], bf[NTW][2];
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
+            for (int mt = 0; mt < MT; ++mt) {
                 const int r = wm * 64 + mt * 16 + ri + 8 * (mi & 1);
                 ldsm_x4(tA + swz(r, 2 * kk + (mi >> 1)), af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
             }
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
                         bf[2 * np + 1][0], bf[2 * np + 1][1]);
             }
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int nt = 0; nt < NTW; ++nt)
                     mma_s8(acc[mt][nt], af[mt][0], af[mt][1], af[mt][2], af[mt][3], bf[nt][0], bf[nt][1]);
@@ -125,9 +128,103 @@ __global__ void __launch_bounds__(GM_THREADS, 1) k_gemm_tma(const __grid_constan
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     }
 
+    if (MODE != EPI_RAW && gridDim.z > 1) {
+        // split K under an epilogue: every split stores its partial tile in
+        // the workspace [split][rows][N]; the tile's last split (counted on
+        // the tile's counter, which it resets) adds the partials in split
+        // order and applies the epilogue
+        const size_t TM = (size_t)gridDim.y * BM;
+        __shared__ int last_split;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt) {
+                const int n = n0 + wn * (NTW * 8) + nt * 8 + 2 * tq;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int m = m0 + wm * 64 + mt * 16 + g + 8 * h;
+                    if (m >= M) continue;
+                    int32_t* w = wsp + ((size_t)blockIdx.z * TM + m) * N + n;
+                    if (n < N) w[0] = acc[mt][nt][2 * h];
+                    if (n + 1 < N) w[1] = acc[mt][nt][2 * h + 1];
+                }
+            }
+        __threadfence();
+        bar_named(1, 256);
+        if (tid == 0) {
+            int* c = tcnt + blockIdx.y * gridDim.x + blockIdx.x;
+            const int old = atomicAdd(c, 1);
+            last_split = old == (int)gridDim.z - 1;
+            if (last_split) *c = 0;
+        }
+        bar_named(1, 256);
+        if (!last_split) return;
+        __threadfence();
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt) {
+                const int n = n0 + wn * (NTW * 8) + nt * 8 + 2 * tq;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int m = m0 + wm * 64 + mt * 16 + g + 8 * h;
+                    if (m >= M) continue;
+                    int c0 = 0, c1 = 0;
+                    for (int z = 0; z < (int)gridDim.z; ++z) {
+                        const int32_t* w = wsp + ((size_t)z * TM + m) * N + n;
+                        if (n < N) c0 += __ldcg(w);
+                        if (n + 1 < N) c1 += __ldcg(w + 1);
+                    }
+                    acc[mt][nt][2 * h] = c0;
+                    acc[mt][nt][2 * h + 1] = c1;
+                }
+            }
+    }
+
+    if (MODE == EPI_LOGITS) {
+        // int32 logits, and per 16-column group the largest (lowest column on
+        // ties) as the argmax partial of that group: a group is two n-tiles
+        // of one warp, spread over the 4 lanes of a quad
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int m = m0 + wm * 64 + mt * 16 + g + 8 * h;
+#pragma unroll
+                for (int j = 0; j < NTW / 2; ++j) {
+                    int bv = -2147483647 - 1, bi = 2147483647;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int n = n0 + wn * (NTW * 8) + (2 * j + q) * 8 + 2 * tq + e;
+                            if (m < M && n < N) {
+                                const i64 y = requant_dev(acc[mt][2 * j + q][2 * h + e], ep, m, n);
+                                if (y > 2147483647LL || y < -2147483647LL) ep.status[ST_SAT_LOGIT] = 1;
+                                const int v = sat32(y);
+                                ep.out[(size_t)m * ep.ldo + n] = v;
+                                if (v > bv || (v == bv && n < bi)) { bv = v; bi = n; }
+                            }
+                        }
+#pragma unroll
+                    for (int o = 1; o <= 2; o <<= 1) {
+                        const int v = __shfl_xor_sync(0xffffffffu, bv, o);
+                        const int i = __shfl_xor_sync(0xffffffffu, bi, o);
+                        if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+                    }
+                    const int grp = (n0 + wn * (NTW * 8) + j * 16) >> 4;
+                    if (tq == 0 && m < M && grp * 16 < N) {
+                        ep.pval[(size_t)m * ep.npart + grp] = bv;
+                        ep.pidx[(size_t)m * ep.npart + grp] = bi;
+                    }
+                }
+            }
+        return;
+    }
+
     // epilogue straight from the accumulator fragments
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
+    for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int nt = 0; nt < NTW; ++nt) {
             const int n = n0 + wn * (NTW * 8) + nt * 8 + 2 * tq;

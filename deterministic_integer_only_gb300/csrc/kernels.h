@@ -40,9 +40,13 @@ struct Epi {
 cudaError_t launch_gemv(const int8_t* W, const int8_t* X, int M, int N, int K, int mode,
                         const Epi& ep, cudaStream_t s);
 
-// tiled GEMM for any M (TMA + mma.sync); K % 16 == 0
+// tiled GEMM for any M (TMA + mma.sync); K % 16 == 0. Grids with fewer
+// tiles than SMs split K: raw outputs add partials into a zeroed C; the other
+// epilogues need a workspace of ws_elems int32 and tcnt_n zeroed tile
+// counters (else they run unsplit)
 cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, int mode,
-                        const Epi& ep, cudaStream_t s);
+                        const Epi& ep, cudaStream_t s, int32_t* wsp = nullptr, size_t ws_elems = 0,
+                        int* tcnt = nullptr, int tcnt_n = 0);
 
 cudaError_t launch_embed(const int32_t* tokens, int T, const int32_t* tok_seq, int32_t* tok_pos,
                          const int32_t* seq_len, int decode, int max_pos, const int8_t* E,

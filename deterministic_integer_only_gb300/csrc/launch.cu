@@ -257,14 +257,25 @@ static cudaError_t make_map(CUtensorMap* map, const void* base, int rows, int K,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-using GemmFn = void (*)(CUtensorMap, CUtensorMap, int, int, int, Epi, int);
+using GemmFn = void (*)(CUtensorMap, CUtensorMap, int, int, int, Epi, int, int32_t*, int*);
 static GemmFn gemm_kernel(int mode, int bm) {
+    if (bm == 32) {
+        switch (mode) {
+            case EPI_RAW: return k_gemm_tma<EPI_RAW, 32>;
+            case EPI_QKV: return k_gemm_tma<EPI_QKV, 32>;
+            case EPI_RESADD: return k_gemm_tma<EPI_RESADD, 32>;
+            case EPI_SWIGLU: return k_gemm_tma<EPI_SWIGLU, 32>;
+            case EPI_LOGITS: return k_gemm_tma<EPI_LOGITS, 32>;
+            default: return nullptr;
+        }
+    }
     if (bm == 64) {
         switch (mode) {
             case EPI_RAW: return k_gemm_tma<EPI_RAW, 64>;
             case EPI_QKV: return k_gemm_tma<EPI_QKV, 64>;
             case EPI_RESADD: return k_gemm_tma<EPI_RESADD, 64>;
             case EPI_SWIGLU: return k_gemm_tma<EPI_SWIGLU, 64>;
+            case EPI_LOGITS: return k_gemm_tma<EPI_LOGITS, 64>;
             default: return nullptr;
         }
     }
@@ -273,18 +284,20 @@ static GemmFn gemm_kernel(int mode, int bm) {
         case EPI_QKV: return k_gemm_tma<EPI_QKV, 128>;
         case EPI_RESADD: return k_gemm_tma<EPI_RESADD, 128>;
         case EPI_SWIGLU: return k_gemm_tma<EPI_SWIGLU, 128>;
+        case EPI_LOGITS: return k_gemm_tma<EPI_LOGITS, 128>;
         default: return nullptr;
     }
 }
 
 cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, int mode,
-                        const Epi& ep, cudaStream_t s) {
+                        const Epi& ep, cudaStream_t s, int32_t* wsp, size_t ws_elems, int* tcnt,
+                        int tcnt_n) {
     if ((K & 15) || K < 16 || M < 1 || N < 1) return cudaErrorInvalidValue;
     if (((uintptr_t)A & 15) || ((uintptr_t)W & 15)) return cudaErrorInvalidValue;
     cudaError_t e = get_encode();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mw;
-    const int BM = M <= 64 ? 64 : 128;    // no tile rows past a short M
+    const int BM = M <= 32 ? 32 : (M <= 64 ? 64 : 128);    // few tile rows past a short M
     e = make_map(&ma, A, M, K, BM);
     if (e == cudaSuccess) e = make_map(&mw, W, N, K);
     if (e != cudaSuccess) return e;
@@ -293,11 +306,17 @@ cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, i
     // raw output with fewer tiles than SMs: split K over up to two CTAs per
     // SM, at least two k-tiles each, partial sums added into a zeroed C
     int splits = 1, ksl = nk;
-    if (mode == EPI_RAW && g_num_sms > 0 && tiles_n * tiles_m < g_num_sms && nk >= 4) {
-        splits = std::min(nk / 2, (2 * g_num_sms + tiles_n * tiles_m - 1) / (tiles_n * tiles_m));
+    const int tiles = tiles_n * tiles_m;
+    // under an epilogue the partial tiles go through the caller's workspace
+    const bool fixup_ok = mode != EPI_RAW && wsp && tcnt && tiles <= tcnt_n;
+    if ((mode == EPI_RAW || fixup_ok) && g_num_sms > 0 && tiles < g_num_sms && nk >= 4) {
+        splits = std::min(nk / 2, (2 * g_num_sms + tiles - 1) / tiles);
+        if (mode != EPI_RAW)
+            splits = std::min<long long>(splits, (long long)(ws_elems / ((size_t)tiles_m * BM * N)));
+        splits = std::max(splits, 1);
         ksl = (nk + splits - 1) / splits;
         splits = (nk + ksl - 1) / ksl;
-        if (splits > 1) {
+        if (splits > 1 && mode == EPI_RAW) {
             e = cudaMemsetAsync(ep.out, 0, (size_t)M * ep.ldo * sizeof(int32_t), s);
             if (e != cudaSuccess) return e;
         }
@@ -305,7 +324,7 @@ cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, i
     const dim3 grid(tiles_n, tiles_m, splits);
     auto k = gemm_kernel(mode, BM);
     if (!k) return cudaErrorInvalidValue;
-    k<<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl);
+    k<<<grid, GM_THREADS, GM_SMEM, s>>>(ma, mw, M, N, K, ep, ksl, wsp, tcnt);
     return cudaGetLastError();
 }
 
@@ -416,8 +435,8 @@ cudaError_t kernels_init() {
     const int sgm = (int)SG_SMEM_MAX;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
-    for (int bm : {64, 128})
-        for (int mode : {EPI_RAW, EPI_QKV, EPI_RESADD, EPI_SWIGLU})
+    for (int bm : {32, 64, 128})
+        for (int mode : {EPI_RAW, EPI_QKV, EPI_RESADD, EPI_SWIGLU, EPI_LOGITS})
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(gemm_kernel(mode, bm), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
     for (int lg = 0; lg < 4 && e == cudaSuccess; ++lg) {

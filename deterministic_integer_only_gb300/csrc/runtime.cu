@@ -154,6 +154,10 @@ struct detint_model {
     unsigned* pd_bar = nullptr;
     size_t pd_smem = 0, pd_off[4] = {0, 0, 0, 0};
     int pd_lg_ns = 0, pd_cap = 0, nsm = 0;
+    int32_t* gws = nullptr;  // split-K workspace of the short-M tiled GEMMs
+    size_t gws_elems = 0;
+    int* gcnt = nullptr;     // their tile counters (self-resetting)
+    int gcnt_n = 0;
     int pf_ok = 0;           // the tensor-core prefill attention supports this shape
     CUtensorMap kmap, vmap;  // whole K / V^T caches for the prefill attention
     int32_t* qblk = nullptr; // prefill query blocks [Tcap + max_batch][4]
@@ -237,11 +241,28 @@ static int ensure_scratch(detint_model* m, int T) {
     return DETINT_OK;
 }
 
-// GEMM of X[M][K] by W[N][K] with an epilogue; small M streams the weights
-// once per 32 tokens through the GEMV kernel, larger M uses the tiled GEMM.
-static cudaError_t gemm_epi(const int8_t* X, const int8_t* W, int M, int N, int K, int mode,
-                            const Epi& ep, cudaStream_t s) {
-    if (M <= 32) return launch_gemv(W, X, M, N, K, mode, ep, s);
+// GEMM of X[M][K] by W[N][K] with an epilogue.
+static cudaError_t gemm_epi(detint_model* m, const int8_t* X, const int8_t* W, int M, int N, int K,
+                            int mode, const Epi& ep, cudaStream_t s) {
+    // up to 8 rows the register GEMV streams the weights once; beyond, the
+    // tiled GEMM (32/64/128-row tiles) keeps the int8 tensor pipe busy
+    if (mode == EPI_LOGITS && M <= 8) {
+        // few rows: the GEMV streams the vocabulary once
+        for (int r0 = 0; r0 < M; r0 += 32) {
+            Epi e = ep;
+            e.out = ep.out + (size_t)r0 * ep.ldo;
+            e.mt = ep.mt + r0;
+            e.kt = ep.kt + r0;
+            e.pval = ep.pval + (size_t)r0 * ep.npart;
+            e.pidx = ep.pidx + (size_t)r0 * ep.npart;
+            cudaError_t ce = launch_gemv(W, X + (size_t)r0 * K, std::min(32, M - r0), N, K, mode, e, s);
+            if (ce != cudaSuccess) return ce;
+        }
+        return cudaSuccess;
+    }
+    if (M <= 8 || (K & 15)) return launch_gemv(W, X, M, N, K, mode, ep, s);
+    // short M: small grids split K through the model's workspace
+    if (M <= 64) return launch_gemm(X, W, M, N, K, mode, ep, s, m->gws, m->gws_elems, m->gcnt, m->gcnt_n);
     return launch_gemm(X, W, M, N, K, mode, ep, s);
 }
 
@@ -345,20 +366,26 @@ static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode
         e.status = m->status;
         e.mt = m->mt; e.kt = m->kt;
         e.out = m->qkv; e.ldo = nqkv; e.mc = w.m_qkv; e.fout = 12;
-        CK(gemm_epi(m->x8, w.w_qkv, T, nqkv, H, EPI_QKV, e, s));
+        CK(gemm_epi(m, m->x8, w.w_qkv, T, nqkv, H, EPI_QKV, e, s));
         QkvPostArgs qa{};
         qa.qkv = m->qkv; qa.q_gamma = w.q_gamma; qa.k_gamma = w.k_gamma; qa.qk_norm = m->qk_norm;
         qa.eps_qk = m->eps_qk; qa.rope_cos = m->rope_cos; qa.rope_sin = m->rope_sin; qa.kvp = w.kvp;
         qa.tok_seq = m->tok_seq; qa.tok_pos = m->tok_pos; qa.block_table = m->block_table;
         qa.mbs = m->mbs; qa.q8 = m->q8; qa.mq = m->mq; qa.kq = m->kq; qa.kc = kc; qa.vc = vc;
         qa.T = T; qa.nq = nq; qa.nkv = nkv; qa.d = d; qa.lg_grp = m->lg_grp;
-        CK(launch_qkv_post(qa, s));
         AttnArgs aa{};
         aa.q8 = m->q8; aa.mq = m->mq; aa.kq = m->kq; aa.kc = kc; aa.vc = vc;
         aa.block_table = m->block_table; aa.mbs = m->mbs; aa.tok_seq = m->tok_seq;
         aa.tok_pos = m->tok_pos; aa.kvp = w.kvp; aa.o = m->o; aa.T = T; aa.nq = nq; aa.nkv = nkv;
         aa.d = d; aa.lg_grp = m->lg_grp; aa.ctx_cap = m->ctx_cap;
-        if (!decode && m->pf_ok && m->tc_prefill) {
+        if (decode && m->dec_staged == 1) {
+            // one token per sequence: QKV post-processing fused into the
+            // staged decode attention, as in the fused step
+            aa.ctx_cap = m->dec_cap;
+            aa.seq_len = m->seq_len_dev; aa.status = m->status;
+            CK(launch_attn_decode(aa, qa, s, true));
+        } else if (!decode && m->pf_ok && m->tc_prefill) {
+            CK(launch_qkv_post(qa, s));
             PfArgs pa{};
             pa.q8 = m->q8; pa.mq = m->mq; pa.kq = m->kq; pa.block_table = m->block_table;
             pa.mbs = m->mbs; pa.qblk = m->qblk; pa.nqb = m->nqb; pa.kvp = w.kvp; pa.o = m->o;
@@ -368,24 +395,25 @@ static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode
             pa.status = m->status;
             CK(launch_attn_prefill(pa, m->kmap, m->vmap, d, s));
         } else {
+            CK(launch_qkv_post(qa, s));
             CK(launch_attention(aa, s));
         }
         CK(launch_actquant(m->o, T, nq * d, 12, m->x8, m->mt, m->kt, s));
         e.out = m->h; e.ldo = H; e.mc = w.m_o; e.fout = 16;
-        CK(gemm_epi(m->x8, w.w_o, T, H, nq * d, EPI_RESADD, e, s));
+        CK(gemm_epi(m, m->x8, w.w_o, T, H, nq * d, EPI_RESADD, e, s));
         CK(launch_normquant(m->h, nullptr, T, H, w.ffn_gamma, m->eps_h, m->x8, m->mt, m->kt, s));
         e.out = m->sbuf; e.ldo = F; e.mc = w.m_gu; e.fout = 12;
-        CK(gemm_epi(m->x8, w.w_gu, T, 2 * F, H, EPI_SWIGLU, e, s));
+        CK(gemm_epi(m, m->x8, w.w_gu, T, 2 * F, H, EPI_SWIGLU, e, s));
         CK(launch_actquant(m->sbuf, T, F, 10, m->x8, m->mt, m->kt, s));
         e.out = m->h; e.ldo = H; e.mc = w.m_d; e.fout = 16;
-        CK(gemm_epi(m->x8, w.w_d, T, H, F, EPI_RESADD, e, s));
+        CK(gemm_epi(m, m->x8, w.w_d, T, H, F, EPI_RESADD, e, s));
     }
     CK(launch_normquant(m->h, rows, R, H, m->final_gamma, m->eps_h, m->x8, m->mt, m->kt, s));
     Epi e{};
     e.status = m->status; e.mt = m->mt; e.kt = m->kt;
     e.out = logits ? logits : m->logits_int; e.ldo = m->V; e.mc = m->embed_m; e.fout = 16;
     e.pval = m->pval; e.pidx = m->pidx; e.npart = m->npart;
-    CK(gemm_epi(m->x8, m->embed, R, m->V, H, EPI_LOGITS, e, s));
+    CK(gemm_epi(m, m->x8, m->embed, R, m->V, H, EPI_LOGITS, e, s));
     CK(launch_argmax_final(m->pval, m->pidx, R, m->npart, next_tok, m->tok_seq,
                            decode ? m->seq_len_dev : nullptr, s));
     return DETINT_OK;
@@ -542,6 +570,8 @@ void detint_free(detint_model* m) {
     if (m->seq_len_dev) cudaFree(m->seq_len_dev);
     if (m->status) cudaFree(m->status);
     if (m->pd_layers) cudaFree(m->pd_layers);
+    if (m->gws) cudaFree(m->gws);
+    if (m->gcnt) cudaFree(m->gcnt);
     if (m->pd_bar) cudaFree(m->pd_bar);
     if (m->pinned) cudaFreeHost(m->pinned);
     if (m->pinned_done) cudaEventDestroy(m->pinned_done);
@@ -727,6 +757,19 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
     if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
     rc = setup_persistent(m);
     if (rc != DETINT_OK) { detint_free(m); return rc; }
+    {
+        // split-K workspace for GEMMs of at most 64 rows: 8 splits of 64 x N
+        const int nqkv = (m->nq + 2 * m->nkv) * m->d;
+        const int nmax = std::max(std::max(nqkv, m->H), 2 * m->F);
+        m->gws_elems = (size_t)8 * 64 * nmax;
+        m->gcnt_n = 2 * ((nmax + 127) / 128);
+        if (cudaMalloc(&m->gws, m->gws_elems * 4) != cudaSuccess ||
+            cudaMalloc(&m->gcnt, (size_t)m->gcnt_n * 4) != cudaSuccess ||
+            cudaMemset(m->gcnt, 0, (size_t)m->gcnt_n * 4) != cudaSuccess) {
+            detint_free(m);
+            return fail(DETINT_E_OOM, "GEMM workspace allocation failed");
+        }
+    }
     ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
     *out = m;
@@ -880,7 +923,8 @@ int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, i
     Epi e{};
     e.out = C; e.ldo = N;
     // up to 8 rows: the streaming decode GEMV (weights through the bulk-TMA
-    // ring); up to 32: the register-streaming GEMV; beyond: the tiled GEMM
+    // ring) where the shape fits it; otherwise and beyond 8 rows the tiled
+    // GEMM (32/64/128-row tiles, split K for small grids)
     if (M <= 8) {
         cudaError_t ce = launch_sgemv(B, N, K, M, nullptr, nullptr, nullptr, 0, 0, 0, EPI_RAW, e, s,
                                       A, nullptr, nullptr, false);
@@ -888,8 +932,7 @@ int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, i
         if (ce != cudaErrorNotSupported) return fail(DETINT_E_CUDA, cudaGetErrorString(ce));
         cudaGetLastError();
     }
-    if (M <= 32 && (K % 64) == 0) { CK(launch_gemv(B, A, M, N, K, EPI_RAW, e, s)); }
-    else { CK(launch_gemm(A, B, M, N, K, EPI_RAW, e, s)); }
+    CK(launch_gemm(A, B, M, N, K, EPI_RAW, e, s));
     return DETINT_OK;
 }
 
