@@ -109,7 +109,8 @@ __global__ void __launch_bounds__(SP_THREADS) k_sample(const int32_t* __restrict
 
     // ---- 1-2: the maximum logit gives max u (u is non-decreasing in l)
     int lmax = -2147483647 - 1;
-    for (int i = tid; i < n; i += SP_THREADS) lmax = max(lmax, x[i]);
+#pragma unroll 8
+    for (int i = tid; i < n; i += SP_THREADS) lmax = max(lmax, __ldg(x + i));
     lmax = sp_max_i32(lmax, red_i);
     const i64 M = sp_u(lmax, invT);
 
@@ -127,8 +128,9 @@ __global__ void __launch_bounds__(SP_THREADS) k_sample(const int32_t* __restrict
             const int sh = shifts[ps], nb = 1 << widths[ps];
             for (int b = tid; b < nb; b += SP_THREADS) sp_hist[b] = 0;
             __syncthreads();
+#pragma unroll 4
             for (int i = tid; i < n; i += SP_THREADS) {
-                const uint32_t k = sp_key(x[i]);
+                const uint32_t k = sp_key(__ldg(x + i));
                 if ((k & pmask) == prefix) atomicAdd(&sp_hist[(k >> sh) & (nb - 1)], 1);
             }
             __syncthreads();
@@ -171,15 +173,21 @@ __global__ void __launch_bounds__(SP_THREADS) k_sample(const int32_t* __restrict
     // ---- delta histogram of the top-k set (weights depend on delta alone)
     for (int b = tid; b < SP_BINS; b += SP_THREADS) sp_hist[b] = 0;
     __syncthreads();
+#pragma unroll 4
     for (int base = 0; base < n; base += SP_THREADS) {   // every thread runs every round
         const int i = base + tid;
-        const int32_t l = i < n ? x[i] : 0;
+        const int32_t l = i < n ? __ldg(x + i) : 0;
         const bool in = i < n && (!topk || l > lk);
         const int b = in ? sp_bin(sp_u(l, invT) - M) : -1;
         const unsigned act = __ballot_sync(0xffffffffu, in);
-        if (in) {
-            const unsigned peers = __match_any_sync(act, b);
-            if ((__ffs(peers) - 1) == lane) atomicAdd(&sp_hist[b], __popc(peers));
+        // one add per warp when its lanes share a bin (a flat or hot row),
+        // else one per lane (bins of spread logits rarely collide)
+        const int b0 = __shfl_sync(0xffffffffu, b, __ffs(act | 1u) - 1);
+        const unsigned same = __ballot_sync(0xffffffffu, in && b == b0);
+        if (same == act) {
+            if (act && lane == __ffs(act) - 1) atomicAdd(&sp_hist[b0], __popc(act));
+        } else if (in) {
+            atomicAdd(&sp_hist[b], 1);
         }
     }
     __syncthreads();
@@ -211,6 +219,11 @@ __global__ void __launch_bounds__(SP_THREADS) k_sample(const int32_t* __restrict
         bstar = s_sel[2];
         S = s_sel64[0];
     }
+    // the histogram is no longer needed: it becomes the kept weight of each
+    // bin (0 below the top-p boundary), looked up per element below
+    __syncthreads();
+    for (int b = tid; b < SP_BINS; b += SP_THREADS) sp_hist[b] = b >= bstar ? (int)sp_binE(b) : 0;
+    __syncthreads();
     // ---- 6-7: the draw
     const uint64_t r = sp_splitmix64(prm.seed, prm.counter);
     const i64 tdraw = (i64)__umul64hi(r, (uint64_t)S);
@@ -223,23 +236,24 @@ __global__ void __launch_bounds__(SP_THREADS) k_sample(const int32_t* __restrict
     int tie_before = 0;
     if (topk) {
         int cnt = 0;
-        for (int i = c0 + lane; i < c1; i += 32) cnt += x[i] == lk;
+#pragma unroll 8
+        for (int i = c0 + lane; i < c1; i += 32) cnt += __ldg(x + i) == lk;
         i64 tot;
         tie_before = (int)sp_warp_excl(sp_warp_sum(cnt), red_l, &tot);
     }
     // kept weight of each chunk
     auto kept_E = [&](int i, int rank) -> i64 {
-        const int32_t l = x[i];
+        const int32_t l = __ldg(x + i);
         if (topk && (l < lk || (l == lk && rank >= quota))) return 0;
-        const int b = sp_bin(sp_u(l, invT) - M);
-        return b >= bstar ? sp_binE(b) : 0;
+        return (i64)sp_hist[sp_bin(sp_u(l, invT) - M)];
     };
     i64 wsum = 0;
     {
         int rank = tie_before;
+#pragma unroll 4
         for (int base = c0; base < c1; base += 32) {
             const int i = base + lane;
-            const bool tie = topk && i < c1 && x[i] == lk;
+            const bool tie = topk && i < c1 && __ldg(x + i) == lk;
             const unsigned tb = __ballot_sync(0xffffffffu, tie);
             const int my = rank + __popc(tb & ((1u << lane) - 1));
             if (i < c1) wsum += kept_E(i, my);
