@@ -170,6 +170,35 @@ MMA_S8_PEAK_TOPS = 150.3
 LMHEAD_DRAM_BYTES = 155664896 + 2895104
 
 
+def run_sample(args):
+    """detint_sample on seeded 151936-wide logits rows (±8 in logit units):
+    microseconds per call for 1, 8 and 32 rows, full distribution and
+    top-k 50 / top-p 0.92."""
+    import torch
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+    rng = np.random.default_rng(SEED)
+    res = []
+    for rows in (1, 8, 32):
+        x = torch.tensor(rng.integers(-(8 << 16), 8 << 16, (rows, 151936)).astype(np.int32), device="cuda")
+        for prm in ({}, {"top_k": 50, "top_p": 60000}):
+            for _ in range(max(3, args.warmup)):
+                pkg.detint_sample(x, prm)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            n = max(20, args.steps)
+            e0.record()
+            for _ in range(n):
+                pkg.detint_sample(x, prm)
+            e1.record()
+            torch.cuda.synchronize()
+            res.append({"rows": rows, "params": prm, "us": e0.elapsed_time(e1) / n * 1e3})
+    print(json.dumps({"metric": "integer sampling latency (151936-wide rows)", "unit": "us",
+                      "results": res}), flush=True)
+
+
 def run_llama_b32(args):
     """Llama-3.2-1B-shaped decode at batch 32 with 1024-token seeded contexts:
     32 x 1024 prefilled, then K timed decode steps (CUDA-graph replays)."""
@@ -386,7 +415,7 @@ def main():
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prefill workload: sequences")
     ap.add_argument("--prefill-len", type=int, default=4096, help="prefill workload: tokens each")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "gemm", "lmhead", "llama-b32"],
+                    choices=["decode", "prefill", "gemm", "lmhead", "llama-b32", "sample"],
                     help="decode (the headline line), prefill (4 x 4096 prompt throughput) or "
                          "gemm (exact int8 GEMM sweep over the Llama-3.2-1B projection shapes)")
     args = ap.parse_args()
@@ -396,6 +425,8 @@ def main():
         return run_prefill(args)
     if args.workload == "llama-b32":
         return run_llama_b32(args)
+    if args.workload == "sample":
+        return run_sample(args)
     if args.workload == "gemm":
         return run_gemm_sweep(args)
     if args.workload == "lmhead":
