@@ -170,6 +170,28 @@ MMA_S8_PEAK_TOPS = 150.3
 LMHEAD_DRAM_BYTES = 155664896 + 2895104
 
 
+def run_gemm_w16(args):
+    """Exact int8 x int16 GEMM (two int8 weight limbs) over the Llama-3.2-1B
+    projection shapes; TOPS counts 2 M N K for the int16 product."""
+    import torch
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+    res = []
+    s = torch.cuda.Stream()
+    for M in (64, 512, 4096):
+        for N, K in ((2048, 2048), (3072, 2048), (16384, 2048), (2048, 8192)):
+            a = torch.randint(-128, 128, (M, K), dtype=torch.int8, device="cuda")
+            w = torch.randint(-32768, 32768, (N, K), dtype=torch.int16, device="cuda")
+            hi, lo = pkg.detint_split_w16(w)
+            c = torch.empty((M, N), dtype=torch.int64, device="cuda")
+            ms = _graph_time(lambda: pkg.detint_gemm_w16(a, hi, lo, c, stream=s), s, 20)
+            res.append({"M": M, "N": N, "K": K, "us": ms * 1e3, "tops": 2.0 * M * N * K / (ms / 1e3) / 1e12})
+            del a, w, hi, lo, c
+    print(json.dumps({"metric": "exact int8 x int16 GEMM sweep (two int8 weight limbs, Llama-3.2-1B shapes)",
+                      "unit": "TOPS", "mma_s8_peak_tops": MMA_S8_PEAK_TOPS, "sweep": res}), flush=True)
+
+
 def run_sample(args):
     """detint_sample on seeded 151936-wide logits rows (±8 in logit units):
     microseconds per call for 1, 8 and 32 rows, full distribution and
@@ -415,7 +437,7 @@ def main():
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prefill workload: sequences")
     ap.add_argument("--prefill-len", type=int, default=4096, help="prefill workload: tokens each")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "gemm", "lmhead", "llama-b32", "sample"],
+                    choices=["decode", "prefill", "gemm", "lmhead", "llama-b32", "sample", "gemm-w16"],
                     help="decode (the headline line), prefill (4 x 4096 prompt throughput) or "
                          "gemm (exact int8 GEMM sweep over the Llama-3.2-1B projection shapes)")
     args = ap.parse_args()
@@ -427,6 +449,8 @@ def main():
         return run_llama_b32(args)
     if args.workload == "sample":
         return run_sample(args)
+    if args.workload == "gemm-w16":
+        return run_gemm_w16(args)
     if args.workload == "gemm":
         return run_gemm_sweep(args)
     if args.workload == "lmhead":

@@ -25,7 +25,7 @@ ERRORS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "token id o
 # every entry point of include/detint.h
 SYMBOLS = ["detint_load", "detint_prefill", "detint_decode_step", "detint_gemm_i8",
            "detint_reset_seq", "detint_seq_len", "detint_status", "detint_set_graph",
-           "detint_set_option", "detint_argmax_noalloc", "detint_sample", "detint_fork_seq",
+           "detint_set_option", "detint_argmax_noalloc", "detint_sample", "detint_fork_seq", "detint_gemm_w16", "detint_split_w16",
            "detint_model_info", "detint_free", "detint_strerror", "detint_last_error"]
 
 
@@ -56,6 +56,8 @@ def lib():
         L.detint_set_option.argtypes = [vp, C.c_int, C.c_int]
         L.detint_argmax_noalloc.argtypes = [vp, C.c_int, C.c_int, vp, vp]
         L.detint_fork_seq.argtypes = [vp, C.c_int, C.c_int, C.c_int, vp]
+        L.detint_gemm_w16.argtypes = [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, vp]
+        L.detint_split_w16.argtypes = [vp, vp, vp, C.c_longlong, vp]
         L.detint_sample.argtypes = [vp, C.c_int, C.c_int, C.POINTER(SamplingParams), vp, vp]
         L.detint_model_info.argtypes = [vp, i32p]
         L.detint_free.argtypes = [vp]
@@ -131,6 +133,27 @@ def detint_sample(logits, params, out=None, stream=None):
         out = torch.empty(rows, dtype=torch.int32, device=logits.device)
     _check(lib().detint_sample(_ptr(logits), rows, n, arr, _ptr(out), _stream(stream)), "detint_sample")
     return out
+
+
+def detint_split_w16(W, stream=None):
+    """(w_hi int8, w_lo uint8) limbs of an int16 cuda tensor, W = 256 hi + lo."""
+    import torch
+    hi = torch.empty(W.shape, dtype=torch.int8, device=W.device)
+    lo = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+    _check(lib().detint_split_w16(_ptr(W), _ptr(hi), _ptr(lo), W.numel(), _stream(stream)), "detint_split_w16")
+    return hi, lo
+
+
+def detint_gemm_w16(A, w_hi, w_lo, C=None, stream=None):
+    """C = A @ W.T exactly in int64 (int8 A [M, K], W = 256 w_hi + w_lo [N, K])."""
+    import torch
+    M, K = A.shape
+    N = w_hi.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.int64, device=A.device)
+    _check(lib().detint_gemm_w16(_ptr(A), _ptr(w_hi), _ptr(w_lo), _ptr(C), M, N, K, _stream(stream)),
+           "detint_gemm_w16")
+    return C
 
 
 def chain_hash(rows, prev: bytes | None = None) -> bytes:

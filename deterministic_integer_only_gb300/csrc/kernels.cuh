@@ -791,6 +791,7 @@ __device__ __forceinline__ int swiglu_tab(int g, int u) {
 #include "k_attn_prefill.cuh"
 #include "k_attn_decode.cuh"
 #include "k_persistent.cuh"
+#include "k_gemm_w16.cuh"
 namespace detint {
 
 // ----------------------------------------------------------- argmax (a11)

@@ -188,6 +188,14 @@ cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int ro
                                 int32_t* next_tok, const int32_t* tok_seq, int32_t* seq_len,
                                 cudaStream_t s, bool pdl = false);
 
+// exact int8 x int16 GEMM from two int8 weight limbs (k_gemm_w16.cuh):
+// C int64 [M][N]; K % 16 == 0, K <= 65536, operands 16-byte aligned
+cudaError_t launch_gemm_w16(const int8_t* A, const int8_t* Wh, const uint8_t* Wl, int64_t* C, int M,
+                            int N, int K, int32_t* status, cudaStream_t s);
+cudaError_t launch_split_w16(const int16_t* W, int8_t* hi, uint8_t* lo, long long n, cudaStream_t s);
+// a status word in device memory for the entry points that take no model
+int32_t* standalone_status();
+
 cudaError_t kernels_init();
 
 }  // namespace detint

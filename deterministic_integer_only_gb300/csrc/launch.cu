@@ -384,6 +384,50 @@ static cudaError_t gemv_attr_all() {
     return e;
 }
 
+cudaError_t launch_split_w16(const int16_t* W, int8_t* hi, uint8_t* lo, long long n, cudaStream_t s) {
+    if (n < 1) return cudaErrorInvalidValue;
+    const long long blocks = std::min<long long>((n + 255) / 256, (long long)std::max(g_num_sms, 1) * 16);
+    k_split_w16<<<(unsigned)blocks, 256, 0, s>>>(W, hi, lo, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_w16(const int8_t* A, const int8_t* Wh, const uint8_t* Wl, int64_t* C, int M,
+                            int N, int K, int32_t* status, cudaStream_t s) {
+    if ((K & 15) || K < 16 || K > 65536 || M < 1 || N < 1) return cudaErrorInvalidValue;
+    if (((uintptr_t)A & 15) || ((uintptr_t)Wh & 15) || ((uintptr_t)Wl & 15)) return cudaErrorInvalidValue;
+    cudaError_t e = get_encode();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mh, ml;
+    e = make_map(&ma, A, M, K, W16_BM);
+    if (e == cudaSuccess) e = make_map(&mh, Wh, N, K);
+    if (e == cudaSuccess) e = make_map(&ml, Wl, N, K);
+    if (e != cudaSuccess) return e;
+    const int tiles_n = (N + GM_BN - 1) / GM_BN, tiles_m = (M + W16_BM - 1) / W16_BM;
+    const int nk = (K + GM_BK - 1) / GM_BK, tiles = tiles_n * tiles_m;
+    int splits = 1, ksl = nk;
+    if (g_num_sms > 0 && tiles < g_num_sms && nk >= 4) {
+        splits = std::min(nk / 2, (2 * g_num_sms + tiles - 1) / tiles);
+        ksl = (nk + splits - 1) / splits;
+        splits = (nk + ksl - 1) / ksl;
+        if (splits > 1) {
+            e = cudaMemsetAsync(C, 0, (size_t)M * N * sizeof(int64_t), s);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    k_gemm_w16<<<dim3(tiles_n, tiles_m, splits), GM_THREADS, W16_SMEM, s>>>(ma, mh, ml, M, N, K, C, ksl,
+                                                                            status);
+    return cudaGetLastError();
+}
+
+__device__ int32_t g_free_status[ST_N];
+int32_t* standalone_status() {
+    static int32_t* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev] && cudaGetSymbolAddress((void**)&addr[dev], g_free_status) != cudaSuccess) return nullptr;
+    return addr[dev];
+}
+
 using PdFn = void (*)(PdArgs);
 static PdFn pd_kernel(int d, int grp) {
     if (d == 128 && grp == 2) return k_decode_persistent<4, 2>;
@@ -435,6 +479,8 @@ cudaError_t kernels_init() {
     const int sgm = (int)SG_SMEM_MAX;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_w16, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W16_SMEM);
     for (int bm : {32, 64, 128})
         for (int mode : {EPI_RAW, EPI_QKV, EPI_RESADD, EPI_SWIGLU, EPI_LOGITS})
             if (e == cudaSuccess)

@@ -906,6 +906,38 @@ int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const
     return DETINT_OK;
 }
 
+// per-device kernel set-up for the entry points that take no model
+static int ensure_kernels() {
+    static std::mutex mu;
+    static int inited[64] = {};
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return fail(DETINT_E_CUDA, "device ordinal out of range");
+    std::lock_guard<std::mutex> lk(mu);
+    if (!inited[dev]) { CK(kernels_init()); inited[dev] = 1; }
+    return DETINT_OK;
+}
+
+int detint_split_w16(const int16_t* W, int8_t* w_hi, uint8_t* w_lo, long long count, detint_stream_t sp) {
+    if (!W || !w_hi || !w_lo || count < 1) return fail(DETINT_E_ARG, "detint_split_w16: bad arguments");
+    int rc = ensure_kernels();
+    if (rc) return rc;
+    CK(launch_split_w16(W, w_hi, w_lo, count, (cudaStream_t)sp));
+    return DETINT_OK;
+}
+
+int detint_gemm_w16(const int8_t* A, const int8_t* w_hi, const uint8_t* w_lo, int64_t* C, int M, int N,
+                    int K, detint_stream_t sp) {
+    if (!A || !w_hi || !w_lo || !C || M < 1 || N < 1 || K < 1) return fail(DETINT_E_ARG, "detint_gemm_w16: bad arguments");
+    if (K % 16 || K > 65536) return fail(DETINT_E_SHAPE, "detint_gemm_w16: K must be a multiple of 16, at most 65536");
+    if (((uintptr_t)A & 15) || ((uintptr_t)w_hi & 15) || ((uintptr_t)w_lo & 15))
+        return fail(DETINT_E_ARG, "detint_gemm_w16: operands must be 16-byte aligned");
+    int rc = ensure_kernels();
+    if (rc) return rc;
+    CK(launch_gemm_w16(A, w_hi, w_lo, C, M, N, K, standalone_status(), (cudaStream_t)sp));
+    return DETINT_OK;
+}
+
 int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, int K,
                    detint_stream_t sp) {
     if (!A || !B || !C || M < 1 || N < 1 || K < 1) return fail(DETINT_E_ARG, "detint_gemm_i8: bad arguments");
@@ -921,7 +953,7 @@ int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, i
         if (inited_dev != dev) { CK(kernels_init()); inited_dev = dev; }
     }
     Epi e{};
-    e.out = C; e.ldo = N;
+    e.out = C; e.ldo = N; e.status = standalone_status();
     // up to 8 rows: the streaming decode GEMV (weights through the bulk-TMA
     // ring) where the shape fits it; otherwise and beyond 8 rows the tiled
     // GEMM (32/64/128-row tiles, split K for small grids)

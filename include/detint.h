@@ -132,6 +132,22 @@ int detint_status(detint_model* m, int32_t* flags, detint_stream_t s);
  * (README, "Usage": use_graph). */
 int detint_set_graph(detint_model* m, int enable);
 
+/* Exact int8 x int16 GEMM for wide-weight ("exact mode") linear layers:
+ * C[m][n] = sum_k A[m][k] W[n][k] in int64, with int8 activations A
+ * [M][K] and int16 weights W [N][K] given as two int8 limbs,
+ * W = 256 * w_hi + w_lo (w_hi int8, w_lo uint8; detint_split_w16 makes them).
+ * Both limb products run on the int8 tensor pipe in one pass and are
+ * combined exactly (BitExact LLM post, "Fix the arithmetic, not just the
+ * random seed": products of split integer limbs combined in wider
+ * accumulators; its exact mode keeps wide weights). Device pointers, all
+ * 16-byte aligned, caller-owned; K % 16 == 0 and K <= 65536. Asynchronous
+ * on s. Errors: ARG, SHAPE, CUDA. */
+int detint_gemm_w16(const int8_t* A, const int8_t* w_hi, const uint8_t* w_lo, int64_t* C, int M, int N,
+                    int K, detint_stream_t s);
+/* w_hi[i] = W[i] >> 8 (floor), w_lo[i] = W[i] & 255, for count elements
+ * (device pointers). Errors: ARG, CUDA. */
+int detint_split_w16(const int16_t* W, int8_t* w_hi, uint8_t* w_lo, long long count, detint_stream_t s);
+
 /* Start sequence dst (which must be empty) with the first n_tokens positions
  * of sequence src, without recomputing them: whole 64-token KV blocks are
  * shared by reference count, the partial last block is copied, and later
