@@ -251,13 +251,16 @@ class Model:
                                         self.stream.cuda_stream), "detint_decode_step")
         return next_tok
 
-    def generate(self, prompts, max_new: int, seq_ids=None, keep_logits: bool = True):
-        """Greedy decode of a ragged batch of prompts (lists of ids).
+    def generate(self, prompts, max_new: int, seq_ids=None, keep_logits: bool = True, sampling=None):
+        """Decode a ragged batch of prompts (lists of ids), greedy by default.
 
         Returns (tokens [B][max_new] int32 numpy, logits rows per step (list of
         [B, V] numpy arrays) or chain-hash digests per row when keep_logits is
         "hash"). Step 0 is the prefill's last-position logits (README, "Usage":
-        generate(ids, max_new)).
+        generate(ids, max_new)). sampling: None (greedy) or a dict of
+        detint_sample parameters (seed, inv_temp, top_k, top_p) or one dict per
+        row; step s of row b draws with counter = s, so a row's tokens do not
+        depend on the rest of the batch.
         """
         torch = self.torch
         B = len(prompts)
@@ -272,11 +275,16 @@ class Model:
         toks = np.zeros((B, max_new), np.int32)
         rows = []
         hashes = [b"\0" * 32] * B
+        if sampling is not None:
+            per_row = sampling if isinstance(sampling, (list, tuple)) else [sampling] * B
         with torch.cuda.stream(self.stream):
             self.prefill(seq_ids, flat, cu, logits, tok)
             for step in range(max_new):
                 if step:
                     self.decode_step(seq_ids, tok, logits, tok)
+                if sampling is not None:
+                    detint_sample(logits, [dict(p, counter=step) for p in per_row], out=tok,
+                                  stream=self.stream)
                 lg = logits.cpu().numpy()
                 toks[:, step] = tok.cpu().numpy()
                 if keep_logits == "hash":
