@@ -309,8 +309,12 @@ cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, i
     const int tiles = tiles_n * tiles_m;
     // under an epilogue the partial tiles go through the caller's workspace
     const bool fixup_ok = mode != EPI_RAW && wsp && tcnt && tiles <= tcnt_n;
-    if ((mode == EPI_RAW || fixup_ok) && g_num_sms > 0 && tiles < g_num_sms && nk >= 4) {
-        splits = std::min(nk / 2, (2 * g_num_sms + tiles - 1) / tiles);
+    // as many splits as fit one wave of two CTAs per SM, each of at least 2
+    // k-tiles (raw: partials added by atomics) or 4 (epilogues: partials
+    // written and re-read through the workspace)
+    const int min_kt = mode == EPI_RAW ? 2 : 4;
+    if ((mode == EPI_RAW || fixup_ok) && g_num_sms > 0 && tiles < g_num_sms && nk >= 2 * min_kt) {
+        splits = std::max(1, std::min(nk / min_kt, (2 * g_num_sms) / tiles));
         if (mode != EPI_RAW)
             splits = std::min<long long>(splits, (long long)(ws_elems / ((size_t)tiles_m * BM * N)));
         splits = std::max(splits, 1);
