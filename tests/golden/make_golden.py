@@ -1,5 +1,8 @@
 """Writes oracle_tiny_seed0.json: the CPU oracle's token stream and chain
-hashes for the tiny model (seed 0, 16-token seeded prompt, 16 greedy steps).
+hashes for the tiny model (seed 0, 16-token seeded prompt, 16 greedy steps),
+and oracle_qwen06b_demo.json: the same for the Qwen3-0.6B-shaped model on the
+pages' demo workload (64-token seeded prompt, 512 greedy steps; DetLLM
+README, "Demo").
 
 It calls only the oracle and the seeded input generator; no value in the
 fixture comes from the CUDA path. Run: python tests/golden/make_golden.py
@@ -16,7 +19,35 @@ import oracle  # noqa: E402
 import synth   # noqa: E402
 
 
+def run(shape, seed, prompt_len, steps, max_ctx):
+    path = synth.ensure_artifact(shape, seed)
+    oracle.set_threads(oracle.max_threads())
+    m = oracle.Model(path)
+    ids = synth.prompt_ids(seed, 0, prompt_len, m.vocab)
+    s = m.new_seq(max_ctx)
+    am, lg = s.feed(ids)
+    h, toks = oracle.chain_hash([lg]), [am]
+    for _ in range(steps - 1):
+        am, lg = s.feed([toks[-1]])
+        h = oracle.chain_hash([lg], h)
+        toks.append(am)
+    return {
+        "what": f"CPU oracle, {shape} model, seed {seed}, prompt index 0, greedy",
+        "seed": seed, "prompt_len": prompt_len, "steps": steps,
+        "artifact_sha256": open(path + ".sha256").read().strip(),
+        "tokens": toks,
+        "logits_hash12": h.hex()[:12],
+        "tokens_hash12": oracle.chain_hash([np.array([t], np.int32) for t in toks]).hex()[:12],
+    }
+
+
 def main():
+    here = os.path.dirname(os.path.abspath(__file__))
+    demo = run("qwen3-0.6b", 0, 64, 512, 640)
+    with open(os.path.join(here, "oracle_qwen06b_demo.json"), "w") as f:
+        json.dump(demo, f, indent=1)
+        f.write("\n")
+    print({k: v for k, v in demo.items() if k != "tokens"})
     seed, prompt_len, steps = 0, 16, 16
     path = synth.ensure_artifact("tiny", seed)
     m = oracle.Model(path)
