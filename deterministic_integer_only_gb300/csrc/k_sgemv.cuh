@@ -50,7 +50,7 @@ struct SgShared {
     unsigned long long full[SG_STAGES];
     unsigned long long empty[SG_STAGES];
     int mt[8], kt[8];
-    long long red64[8][3];     // prologue group reductions (per warp)
+    long long red64[8][5];     // prologue group reductions (per warp)
     long long bc[8][2];        // per-row quantisation multiplier and shift
 };
 
@@ -71,6 +71,22 @@ __device__ __forceinline__ int4 sg_vec(const int4 (&v)[SG_NV], const int32_t* xr
         if (q == j) r = v[q];
     if (j >= SG_NV) r = *(const int4*)(xr + i);
     return r;
+}
+
+// warp reductions on the redux unit: a 64-bit maximum as two 32-bit maxima
+// (high words, then the low words of the lanes holding the highest high
+// word); a 64-bit sum modulo 2^64 as three sums of 22-bit slices (each
+// below 2^27 over 32 lanes)
+__device__ __forceinline__ u64 redux_max_u64(u64 v) {
+    const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(v >> 32));
+    const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(v >> 32) == hi ? (unsigned)v : 0u);
+    return ((u64)hi << 32) | lo;
+}
+__device__ __forceinline__ u64 redux_sum_u64(u64 v) {
+    const unsigned s0 = __reduce_add_sync(0xffffffffu, (unsigned)(v & 0x3fffffu));
+    const unsigned s1 = __reduce_add_sync(0xffffffffu, (unsigned)((v >> 22) & 0x3fffffu));
+    const unsigned s2 = __reduce_add_sync(0xffffffffu, (unsigned)(v >> 44));
+    return (u64)s0 + ((u64)s1 << 22) + ((u64)s2 << 44);
 }
 
 __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, const int16_t* gam) {
@@ -99,52 +115,90 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, c
     for (int j = 0; j < SG_NV; ++j)
         v[j] = (j < nv && gt + j * gn < nvec) ? *(const int4*)(xr + (gt + j * gn) * 4)
                                               : make_int4(0, 0, 0, 0);
-    // pass 1: max |x|
-    u64 ax = 0;
+    // pass 1: max |x|; for NormQuant also max |x gamma| and the sum of x^2
+    // (modulo 2^64), which are the normalised row's max |x' gamma| and sum of
+    // squares up to the exact power-of-two factor whenever the row needs no
+    // right shift (every |x| < 2^24: then each x^2 < 2^48 and the sum is exact)
+    unsigned ax = 0;                        // |x| <= 2^31
+    u64 ag = 0, sq = 0;
     for (int j = 0; j < nv; ++j) {
         if (gt + j * gn >= nvec) break;
-        const int4 w = sg_vec(v, xr, j, (gt + j * gn) * 4);
-        ax = umax64(ax, umax64(umax64(absu(w.x), absu(w.y)), umax64(absu(w.z), absu(w.w))));
+        const int i = (gt + j * gn) * 4;
+        const int4 w = sg_vec(v, xr, j, i);
+        const int xv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ax = max(ax, (unsigned)absu(xv[q]));
+        if (norm) {
+            const short4 gm = *(const short4*)(gam + i);
+            const int gv[4] = {gm.x, gm.y, gm.z, gm.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ag = umax64(ag, absu((i64)xv[q] * (i64)gv[q]));
+                sq += (u64)((i64)xv[q] * (i64)xv[q]);
+            }
+        }
     }
-    ax = warp_max_u64(ax);
-    if (lane == 0) sh.red64[warp][0] = (long long)ax;
+    ax = __reduce_max_sync(0xffffffffu, ax);
+    if (norm) {
+        ag = redux_max_u64(ag);
+        sq = redux_sum_u64(sq);
+    }
+    if (lane == 0) {
+        sh.red64[warp][0] = ax;
+        sh.red64[warp][1] = (long long)ag;
+        sh.red64[warp][2] = (long long)sq;
+    }
     bar_named(bar, gn);
-    ax = 0;
-    for (int w = 0; w < wpr; ++w) ax = umax64(ax, (u64)sh.red64[w0 + w][0]);
-    if (ax == 0) {
+    u64 axl = 0;
+    for (int w = 0; w < wpr; ++w) axl = umax64(axl, (u64)sh.red64[w0 + w][0]);
+    if (axl == 0) {
         for (int i = gt * 16; i < K; i += gn * 16) *(int4*)(qr + i) = make_int4(0, 0, 0, 0);
         if (gt == 0) { sh.mt[r] = 0; sh.kt[r] = 0; }
         return;
     }
     int sig = 0;
     if (norm) {
-        sig = bitlen_u64(ax) - 24;
-        // pass 2: sum of squares of the 24-bit row and max |x' gamma|
-        i64 ss = 0;
-        u64 az = 0;
-        for (int j = 0; j < nv; ++j) {
-            if (gt + j * gn >= nvec) break;
-            const int i = (gt + j * gn) * 4;
-            const int4 w = sg_vec(v, xr, j, i);
-            const short4 gm = *(const short4*)(gam + i);
-            const int xv[4] = {w.x, w.y, w.z, w.w};
-            const int gv[4] = {gm.x, gm.y, gm.z, gm.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const i64 xp = norm24(xv[q], sig);
-                ss += xp * xp;
-                az = umax64(az, absu(xp * (i64)gv[q]));
+        sig = bitlen_u64(axl) - 24;
+        i64 ss;
+        u64 az;
+        if (sig <= 0) {
+            // x' = x 2^-sig exactly: scale the pass-1 maximum and sum
+            ss = 0;
+            az = 0;
+            for (int w = 0; w < wpr; ++w) {
+                ss += sh.red64[w0 + w][2];
+                az = umax64(az, (u64)sh.red64[w0 + w][1]);
             }
-        }
-        ss = warp_sum_i64(ss);
-        az = warp_max_u64(az);
-        if (lane == 0) { sh.red64[warp][1] = ss; sh.red64[warp][2] = (long long)az; }
-        bar_named(bar, gn);
-        ss = 0;
-        az = 0;
-        for (int w = 0; w < wpr; ++w) {
-            ss += sh.red64[w0 + w][1];
-            az = umax64(az, (u64)sh.red64[w0 + w][2]);
+            ss <<= -2 * sig;
+            az <<= -sig;
+        } else {
+            // pass 2: sum of squares of the 24-bit row and max |x' gamma|
+            ss = 0;
+            az = 0;
+            for (int j = 0; j < nv; ++j) {
+                if (gt + j * gn >= nvec) break;
+                const int i = (gt + j * gn) * 4;
+                const int4 w = sg_vec(v, xr, j, i);
+                const short4 gm = *(const short4*)(gam + i);
+                const int xv[4] = {w.x, w.y, w.z, w.w};
+                const int gv[4] = {gm.x, gm.y, gm.z, gm.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const i64 xp = norm24(xv[q], sig);
+                    ss += xp * xp;
+                    az = umax64(az, absu(xp * (i64)gv[q]));
+                }
+            }
+            ss = (i64)redux_sum_u64((u64)ss);
+            az = redux_max_u64(az);
+            if (lane == 0) { sh.red64[warp][3] = ss; sh.red64[warp][4] = (long long)az; }
+            bar_named(bar, gn);
+            ss = 0;
+            az = 0;
+            for (int w = 0; w < wpr; ++w) {
+                ss += sh.red64[w0 + w][3];
+                az = umax64(az, (u64)sh.red64[w0 + w][4]);
+            }
         }
         const int e = bitlen_u64(az);
         if (gw == 0) {
@@ -161,14 +215,14 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, c
             if (lane == 0) { sh.bc[r][0] = (long long)R; sh.bc[r][1] = e + 16; }
         }
     } else {
-        const int e = bitlen_u64(ax);
+        const int e = bitlen_u64(axl);
         if (gw == 0) {
-            const u64 R = warp_udiv64(127ull << (e + 16), ax);
+            const u64 R = warp_udiv64(127ull << (e + 16), axl);
             if (lane == 0) { sh.bc[r][0] = (long long)R; sh.bc[r][1] = e + 16; }
         }
         if (gw == (wpr > 1 ? 1 : 0)) {
             int m, k;
-            warp_dyadic(ax, 127ull, &m, &k);
+            warp_dyadic(axl, 127ull, &m, &k);
             if (lane == 0) { sh.mt[r] = m; sh.kt[r] = k + a.F; }
         }
     }
@@ -512,6 +566,8 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
     int32_t* mcs = hold + 256;
     const bool mc_pre = a.ep.mc && (g1 - g0) * 16 <= 256;
     if (mc_pre && tid < (g1 - g0) * 16) mcs[tid] = a.ep.mc[min(g0 * 16 + tid, a.N - 1)];
+    // the prologue's first pass reads gamma elements that other warps copied
+    bar_named(1, 256);
     pdl_wait();
     // residual add: issue the loads of this CTA's old residual values now so
     // they overlap the quantisation prologue
