@@ -138,11 +138,11 @@ __device__ void pd_gemv(const PdArgs& a, const SgArgs& s, SgShared& sh, unsigned
         const int tk = tid & 7, n = g0 * 16 + (tid >> 3);
         if (tk < s.M && n < s.N) hv = s.ep.out[(size_t)tk * s.ep.ldo + n];
     }
-    sg_prologue(s, sh, xs, XP, gam);
+    sg_prologue(s, sh, xs, XP, gam, false);
     if (pre && tid < (g1 - g0) * 128) hold[tid] = hv;
     bar_named(1, 256);
     sg_consume(s, sh, smem, P, PD_SB, 1 << a.lg_ns, a.lg_ns, xs, XP, red, g0, g1, u,
-               pre ? hold : nullptr, mc_pre ? mcs : nullptr);
+               pre ? hold : nullptr, mc_pre ? mcs : nullptr, false);
 }
 
 // attention of token t's q heads of kv group g (compute warps of one CTA):

@@ -89,7 +89,45 @@ __device__ __forceinline__ u64 redux_sum_u64(u64 v) {
     return (u64)s0 + ((u64)s1 << 22) + ((u64)s2 << 44);
 }
 
-__device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, const int16_t* gam) {
+// token scale (m_t, k_t) of row r, by one warp, from the prologue's partial
+// reductions of the row's warp group w0 .. w0 + wpr - 1; only the epilogue
+// needs it
+__device__ void sg_token_scale(const SgArgs& a, SgShared& sh, int r, int w0, int wpr) {
+    u64 axl = 0;
+    for (int w = 0; w < wpr; ++w) axl = umax64(axl, (u64)sh.red64[w0 + w][0]);
+    int m = 0, k = 0;
+    if (axl != 0) {
+        if (a.pro == PRO_NORMQUANT) {
+            const int sig = bitlen_u64(axl) - 24;
+            i64 ss = 0;
+            u64 az = 0;
+            const int js = sig <= 0 ? 2 : 3, jz = sig <= 0 ? 1 : 4;
+            for (int w = 0; w < wpr; ++w) {
+                ss += sh.red64[w0 + w][js];
+                az = umax64(az, (u64)sh.red64[w0 + w][jz]);
+            }
+            if (sig <= 0) {
+                ss <<= -2 * sig;
+                az <<= -sig;
+            }
+            i64 eps_s;
+            if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (a.eps >> (2 * sig));
+            else eps_s = a.eps * (1LL << (-2 * sig));
+            const u64 rr = warp_isqrt64((u64)((ss >> a.lg_k) + eps_s));
+            warp_dyadic(az, 127ull * rr, &m, &k);
+            k += 12;
+        } else {
+            warp_dyadic(axl, 127ull, &m, &k);
+            k += a.F;
+        }
+    }
+    if ((threadIdx.x & 31) == 0) { sh.mt[r] = m; sh.kt[r] = k; }
+}
+
+// sp: the token scales are left to the producer warp (sg_token_scale after
+// the prologue), off the path to the dot products
+__device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, const int16_t* gam,
+                            bool sp) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int M = a.M, K = a.K;
     const bool norm = a.pro == PRO_NORMQUANT;
@@ -157,24 +195,18 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, c
         return;
     }
     int sig = 0;
+    u64 amax = axl;                         // the maximum the int8 codes are scaled to
     if (norm) {
         sig = bitlen_u64(axl) - 24;
-        i64 ss;
-        u64 az;
         if (sig <= 0) {
-            // x' = x 2^-sig exactly: scale the pass-1 maximum and sum
-            ss = 0;
-            az = 0;
-            for (int w = 0; w < wpr; ++w) {
-                ss += sh.red64[w0 + w][2];
-                az = umax64(az, (u64)sh.red64[w0 + w][1]);
-            }
-            ss <<= -2 * sig;
-            az <<= -sig;
+            // x' = x 2^-sig exactly: max |x' gamma| is the pass-1 maximum scaled
+            amax = 0;
+            for (int w = 0; w < wpr; ++w) amax = umax64(amax, (u64)sh.red64[w0 + w][1]);
+            amax <<= -sig;
         } else {
             // pass 2: sum of squares of the 24-bit row and max |x' gamma|
-            ss = 0;
-            az = 0;
+            i64 ss = 0;
+            u64 az = 0;
             for (int j = 0; j < nv; ++j) {
                 if (gt + j * gn >= nvec) break;
                 const int i = (gt + j * gn) * 4;
@@ -193,38 +225,17 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, c
             az = redux_max_u64(az);
             if (lane == 0) { sh.red64[warp][3] = ss; sh.red64[warp][4] = (long long)az; }
             bar_named(bar, gn);
-            ss = 0;
-            az = 0;
-            for (int w = 0; w < wpr; ++w) {
-                ss += sh.red64[w0 + w][3];
-                az = umax64(az, (u64)sh.red64[w0 + w][4]);
-            }
+            amax = 0;
+            for (int w = 0; w < wpr; ++w) amax = umax64(amax, (u64)sh.red64[w0 + w][4]);
         }
-        const int e = bitlen_u64(az);
-        if (gw == 0) {
-            i64 eps_s;
-            if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (a.eps >> (2 * sig));
-            else eps_s = a.eps * (1LL << (-2 * sig));
-            const u64 rr = warp_isqrt64((u64)((ss >> a.lg_k) + eps_s));
-            int m, k;
-            warp_dyadic(az, 127ull * rr, &m, &k);
-            if (lane == 0) { sh.mt[r] = m; sh.kt[r] = k + 12; }
-        }
-        if (gw == (wpr > 1 ? 1 : 0)) {
-            const u64 R = warp_udiv64(127ull << (e + 16), az);
-            if (lane == 0) { sh.bc[r][0] = (long long)R; sh.bc[r][1] = e + 16; }
-        }
-    } else {
-        const int e = bitlen_u64(axl);
-        if (gw == 0) {
-            const u64 R = warp_udiv64(127ull << (e + 16), axl);
-            if (lane == 0) { sh.bc[r][0] = (long long)R; sh.bc[r][1] = e + 16; }
-        }
-        if (gw == (wpr > 1 ? 1 : 0)) {
-            int m, k;
-            warp_dyadic(axl, 127ull, &m, &k);
-            if (lane == 0) { sh.mt[r] = m; sh.kt[r] = k + a.F; }
-        }
+    }
+    // the quantisation multiplier on one warp, the token scale (unless the
+    // producer warp takes it) on another where the group has two
+    if (!sp && gw == 0) sg_token_scale(a, sh, r, w0, wpr);
+    if (gw == (sp || wpr == 1 ? 0 : 1)) {
+        const int e = bitlen_u64(amax);
+        const u64 R = warp_udiv64(127ull << (e + 16), amax);
+        if (lane == 0) { sh.bc[r][0] = (long long)R; sh.bc[r][1] = e + 16; }
     }
     bar_named(bar, gn);
     const i64 R = sh.bc[r][0];
@@ -405,7 +416,8 @@ __device__ __forceinline__ void sg_produce(const SgArgs& a, SgShared& sh, unsign
 __device__ __forceinline__ void sg_consume(const SgArgs& a, SgShared& sh, const unsigned char* ring,
                                            int P, size_t SB, int NS, int lg_ns, const int8_t* xs,
                                            int XP, int32_t* red, int g0, int g1, int& u,
-                                           const int32_t* hold, const int32_t* mcs) {
+                                           const int32_t* hold, const int32_t* mcs,
+                                           bool wait_scale) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
     const int nch = a.KC >> 6;
@@ -481,6 +493,7 @@ __device__ __forceinline__ void sg_consume(const SgArgs& a, SgShared& sh, const 
                     red[b * 1024 + r * 8 + hl] = v;
                 }
             }
+            if (wait_scale && gb == g0) bar_named(15, 288);    // token scales from the producer
             bar_named(1, 256);
             sg_epilogue(a, sh, red, gb, nb, hold, g0, mcs, 1);
             bar_named(1, 256);
@@ -514,6 +527,7 @@ __device__ __forceinline__ void sg_consume(const SgArgs& a, SgShared& sh, const 
             rw[(g + 8) * 8 + 2 * tq] = acc[2];
             rw[(g + 8) * 8 + 2 * tq + 1] = acc[3];
         }
+        if (wait_scale && gb == g0) bar_named(15, 288);
         bar_named(1, 256);
         sg_epilogue(a, sh, red, gb, nb, hold, g0, mcs, 8);
         bar_named(1, 256);
@@ -550,10 +564,21 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
     __syncthreads();
     pdl_launch();
 
+    // with at most two token rows and the CTA's whole weight run fitting the
+    // ring, the producer warp is idle once its copies are issued: it then
+    // computes the token scales while the compute warps quantise and multiply
+    const bool sp = a.pro != PRO_NONE && a.M <= 2 && units <= NS && g1 > g0;
     if (warp == 8) {
         const uint64_t pol = l2_evict_first();
         int u = 0;
         sg_produce(a, sh, ring, P, (size_t)16 * P, NS, a.lg_ns, g0, g1, u, pol);
+        if (sp) {
+            bar_named(14, 288);                     // the prologue's partial reductions are final
+            const int lgw = a.M > 1 ? 2 : 3;        // the prologue's warps per row
+            for (int r = 0; r < a.M; ++r) sg_token_scale(a, sh, r, r << lgw, 1 << lgw);
+            __syncwarp();
+            bar_arrive_named(15, 288);
+        }
         return;
     }
 
@@ -578,13 +603,14 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
         if (tk < a.M && n < a.N) hv = a.ep.out[(size_t)tk * a.ep.ldo + n];
     }
     if (a.pro == PRO_NONE) sg_load_x8(a, sh, xs, XP);
-    else sg_prologue(a, sh, xs, XP, gam);
+    else sg_prologue(a, sh, xs, XP, gam, sp);
+    if (sp) bar_arrive_named(14, 288);
     if (pre && tid < (g1 - g0) * 128) hold[tid] = hv;
     bar_named(1, 256);
 
     int u = 0;
     sg_consume(a, sh, ring, P, (size_t)16 * P, NS, a.lg_ns, xs, XP, red, g0, g1, u,
-               pre ? hold : nullptr, mc_pre ? mcs : nullptr);
+               pre ? hold : nullptr, mc_pre ? mcs : nullptr, sp);
     // every issued copy has completed before the CTA exits (bounded wait;
     // normally these phases completed long ago)
     if (tid == 0) {

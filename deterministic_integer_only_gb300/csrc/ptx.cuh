@@ -69,5 +69,10 @@ __device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.laun
 __device__ __forceinline__ void bar_named(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// signal a named barrier without waiting (the producer side of a
+// producer / consumer pair; the consumers bar.sync on it)
+__device__ __forceinline__ void bar_arrive_named(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 }  // namespace detint
