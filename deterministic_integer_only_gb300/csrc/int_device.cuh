@@ -90,11 +90,35 @@ __device__ __forceinline__ int exp2q_dev(i64 delta) {
     return rshr32(p2, (int)(-ip));
 }
 
-// per-row quantisation multiplier R = floor(127 2^(e+16) / a), e = bitlen(a)
-__device__ __forceinline__ u64 quant_mult(u64 a, int* e_out) {
-    int e = bitlen_u64(a);
-    *e_out = e;
-    return udiv64(127ull << (e + 16), a);
+// floor(c 2^(e+s) / v) for v >= 1 with e = bitlen(v) <= 40, c 2^(e+s) < 2^63
+// and c 2^s < 2^30, s <= 30 (the quotient lies in (c 2^s, c 2^(s+1)]): the
+// per-row quantisation multiplier (c = 127, s = 16) and the row-sum
+// reciprocals (c = 1, s = 23). Newton-Raphson division (as in Goldschmidt's
+// and Newton's reciprocal iterations, all in integers): d = the leading 32
+// bits of v; y ~ 2^62 / d from the linear minimax seed 48/17 - 32/17 d' of
+// 1/d' on [1/2, 1) (relative error <= 1/17) and three Newton steps
+// y += y (2^62 - d y) / 2^62 in Q30 (error ~1/17 -> 2^-8 -> 2^-16 -> a few
+// units of 2^-30); q = c y / 2^(30 - s) is then within one of the quotient
+// (within one more when v has more than 32 bits), and an exact check of
+// q v against c 2^(e+s) settles it. Every product stays below 2^64.
+__host__ __device__ __forceinline__ u64 pow2_recip(u64 v, int e, u64 c, int s) {
+    const u64 d = e <= 32 ? v << (32 - e) : v >> (e - 32);     // [2^31, 2^32)
+    u64 y = 3031741621ull - ((2021161080ull * d) >> 32);         // Q30, (0.94, 1.89] * 2^30
+#pragma unroll
+    for (int it = 0; it < 3; ++it) {
+        const u64 p = d * y;                                      // ~2^62, < 2^63
+        const bool over = p > (1ull << 62);
+        const u64 t = over ? p - (1ull << 62) : (1ull << 62) - p;
+        const u64 corr = (y * (t >> 31)) >> 31;
+        y = over ? y - corr : y + corr;
+    }
+    const u64 N = c << (e + s);
+    u64 q = (c * y) >> (30 - s);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) q -= (q * v > N) ? 1 : 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) q += ((q + 1) * v <= N) ? 1 : 0;
+    return q;
 }
 
 // Q15 sigmoid of the SwiGLU gate from z = Q10 of |g| log2 e: with

@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_dec_staged(AttnArgs a, QkvP
             i64 v = 0;
             for (int w2 = 0; w2 < 8; ++w2) v += red_l[w2][hh];
             const int bl = bitlen_u64((u64)v);
-            const i64 rs = (i64)warp_udiv64(1ull << (bl + 23), (u64)v);
+            const i64 rs = (i64)pow2_recip((u64)v, bl, 1, 23);
             if (lane == 0) { rs_s[hh] = rs; bl_s[hh] = bl; }
         }
     } else {

@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const i64 sg = (i64)r_sum2[0][r] + (i64)r_sum2[1][r];   // >= 32767 for a valid row
         const int bl = bitlen_u64((u64)sg);
         i64 rs = 0;
-        if (tig == 0 && sg > 0) rs = (i64)udiv64(1ull << (bl + 23), (u64)sg);
+        if (tig == 0 && sg > 0) rs = (i64)pow2_recip((u64)sg, bl, 1, 23);
         rs = __shfl_sync(0xffffffffu, rs, lane & ~3, 32);
         if (r_pos[r] < 0) continue;
         const int i = r & ((1 << lgBQ) - 1), hh = r >> lgBQ;

@@ -252,7 +252,7 @@ __device__ void pd_attention(const PdArgs& a, const PdLayer& L, int t, int g, un
         i64 v = 0;
         for (int w2 = 0; w2 < 8; ++w2) v += red_l[w2][w];
         const int bl = bitlen_u64((u64)v);
-        const i64 rs = (i64)warp_udiv64(1ull << (bl + 23), (u64)v);
+        const i64 rs = (i64)pow2_recip((u64)v, bl, 1, 23);
         if (lane == 0) { rs_s[w] = rs; bl_s[w] = bl; }
     }
     // ---- P·V: lane (channel c of 8, key chunk q of 4) of warp w

@@ -51,7 +51,6 @@ struct SgShared {
     unsigned long long empty[SG_STAGES];
     int mt[8], kt[8];
     long long red64[8][5];     // prologue group reductions (per warp)
-    long long bc[8][2];        // per-row quantisation multiplier and shift
 };
 
 __device__ __forceinline__ size_t sg_ring_bytes(int KC, int ns) { return (size_t)ns * 16 * (KC + 64); }
@@ -229,17 +228,12 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, c
             for (int w = 0; w < wpr; ++w) amax = umax64(amax, (u64)sh.red64[w0 + w][4]);
         }
     }
-    // the quantisation multiplier on one warp, the token scale (unless the
-    // producer warp takes it) on another where the group has two
+    // the token scale on one warp (unless the producer warp takes it); the
+    // quantisation multiplier in every thread, from the maximum it already holds
     if (!sp && gw == 0) sg_token_scale(a, sh, r, w0, wpr);
-    if (gw == (sp || wpr == 1 ? 0 : 1)) {
-        const int e = bitlen_u64(amax);
-        const u64 R = warp_udiv64(127ull << (e + 16), amax);
-        if (lane == 0) { sh.bc[r][0] = (long long)R; sh.bc[r][1] = e + 16; }
-    }
-    bar_named(bar, gn);
-    const i64 R = sh.bc[r][0];
-    const int shq = (int)sh.bc[r][1];
+    const int e = bitlen_u64(amax);
+    const i64 R = (i64)pow2_recip(amax, e, 127, 16);
+    const int shq = e + 16;
     // pass 3: quantise
     for (int j = 0; j < nv; ++j) {
         if (gt + j * gn >= nvec) break;

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(256) k_normquant(const int32_t* __restrict__ x
         if (tid == 0) { mt[r] = m; kt[r] = k + 12; }
     } else if (tid < 64) {
         const int e = bitlen_u64(az);
-        const u64 R = warp_udiv64(127ull << (e + 16), az);
+        const u64 R = pow2_recip(az, e, 127, 16);
         if (tid == 32) { bc[0] = (i64)R; bc[1] = e; }
     }
     __syncthreads();
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(256) k_actquant(const int32_t* __restrict__ x,
     }
     if (tid < 32) {
         const int e = bitlen_u64(a);
-        const u64 R = warp_udiv64(127ull << (e + 16), a);
+        const u64 R = pow2_recip(a, e, 127, 16);
         if (tid == 0) { bc[0] = (i64)R; bc[1] = e; }
     } else if (tid < 64) {
         int m, k;
@@ -209,7 +209,7 @@ __device__ void qk_norm_warp(i64 (&y)[EPL], const int16_t* gamma, int lane, int 
     if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (eps >> (2 * sig));
     else eps_s = eps * (1LL << (-2 * sig));
     const i64 rr = (i64)warp_isqrt64((u64)((ss >> lg_d) + eps_s));
-    const i64 Rr = (i64)warp_udiv64(1ull << (bitlen_u64((u64)rr) + 23), (u64)rr);
+    const i64 Rr = (i64)pow2_recip((u64)rr, bitlen_u64((u64)rr), 1, 23);
     const int sh = bitlen_u64((u64)rr) + 21;
 #pragma unroll
     for (int j = 0; j < EPL; ++j) y[j] = rshr(xp[j] * (i64)gamma[lane + 32 * j] * Rr, sh);
@@ -293,7 +293,7 @@ __device__ void qkv_head_p(const QkvPostArgs& a, int t, int slot, int8_t* q_dst,
             return;
         }
         const int e = bitlen_u64(am);
-        const i64 R = (i64)warp_udiv64(127ull << (e + 16), am);
+        const i64 R = (i64)pow2_recip(am, e, 127, 16);
         int m, k;
         warp_dyadic(am, 127ull, &m, &k);
         if (lane == 0) {
@@ -462,7 +462,7 @@ __device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs
             i64 v = 0;
             for (int w2 = 0; w2 < 8; ++w2) v += red[w2 * MAXG + hh];
             const int bl = bitlen_u64((u64)v);
-            const i64 rs = (i64)warp_udiv64(1ull << (bl + 23), (u64)v);
+            const i64 rs = (i64)pow2_recip((u64)v, bl, 1, 23);
             if ((tid & 31) == 0) { sig_s[hh] = v; rs_s[hh] = rs; }
         }
         __syncthreads();
