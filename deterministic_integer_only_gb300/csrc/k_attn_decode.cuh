@@ -65,7 +65,11 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_dec_staged(AttnArgs a, QkvP
     unsigned char* Ehi = Elo + (size_t)G * cap;
     int32_t* pv = (int32_t*)(Ehi + (size_t)G * cap);           // [G][D][2]
 
-    // ---- before the wait: everything that does not depend on this step
+    // ---- before the wait: everything that does not depend on this step.
+    // The sequence length, block table and cache rows below p0 were written
+    // by earlier steps; every step starts with a launch in plain stream order
+    // (the embedding), so all of those writes are complete here even though
+    // the kernels of this step overlap one another under PDL.
     if (tid < dh2) {
         s_cos[tid] = qa.rope_cos[(size_t)p0 * dh2 + tid];
         s_sin[tid] = qa.rope_sin[(size_t)p0 * dh2 + tid];
