@@ -1,4 +1,6 @@
-// Integer primitives for the detint kernels (device side).
+// Integer primitives for the detint kernels. The scalar routines also build
+// for the host (tests compare that build with the oracle); the warp-
+// cooperative forms at the end are device-only.
 //
 // Every rule here is the frozen arithmetic of the integer-only forward pass:
 // round-to-nearest shifts with ties toward +infinity, floor divisions of
@@ -10,7 +12,9 @@
 // No floating-point type, literal or intrinsic appears in this file or in any
 // kernel file, and there is no division or remainder by a value known only at
 // run time: CUDA may lower those through a floating-point reciprocal, so
-// divisions go through udiv64 below (restoring long division).
+// divisions go through udiv64 below (restoring long division), its
+// warp-parallel form, or pow2_recip (Newton-Raphson) for power-of-two
+// numerators.
 #pragma once
 #include <stdint.h>
 
@@ -20,21 +24,27 @@ typedef long long i64;
 typedef unsigned long long u64;
 
 // number of binary digits (bitlen(0) = 0)
-__device__ __forceinline__ int bitlen_u64(u64 x) { return 64 - __clzll((long long)x); }
+__host__ __device__ __forceinline__ int bitlen_u64(u64 x) {
+#ifdef __CUDA_ARCH__
+    return 64 - __clzll((long long)x);
+#else
+    return x ? 64 - __builtin_clzll(x) : 0;    // host build of this header (tests)
+#endif
+}
 
 // x / 2^s rounded to nearest, ties toward +infinity; s in [0, 62]
-__device__ __forceinline__ i64 rshr(i64 x, int s) {
+__host__ __device__ __forceinline__ i64 rshr(i64 x, int s) {
     return s <= 0 ? x : ((x + (1LL << (s - 1))) >> s);
 }
-__device__ __forceinline__ int rshr32(int x, int s) {
+__host__ __device__ __forceinline__ int rshr32(int x, int s) {
     return s <= 0 ? x : ((x + (1 << (s - 1))) >> s);
 }
-__device__ __forceinline__ i64 sat_b(i64 x, i64 b) { return x > b ? b : (x < -b ? -b : x); }
-__device__ __forceinline__ int sat32(i64 x) { return (int)sat_b(x, 2147483647LL); }
-__device__ __forceinline__ int sat127(i64 x) { return (int)sat_b(x, 127); }
+__host__ __device__ __forceinline__ i64 sat_b(i64 x, i64 b) { return x > b ? b : (x < -b ? -b : x); }
+__host__ __device__ __forceinline__ int sat32(i64 x) { return (int)sat_b(x, 2147483647LL); }
+__host__ __device__ __forceinline__ int sat127(i64 x) { return (int)sat_b(x, 127); }
 
 // floor(n / d) for d >= 1, by restoring long division over the quotient bits
-static __device__ __noinline__ u64 udiv64(u64 n, u64 d) {
+static __host__ __device__ __noinline__ u64 udiv64(u64 n, u64 d) {
     if (n < d) return 0;
     int sh = bitlen_u64(n) - bitlen_u64(d);
     u64 dd = d << sh;
@@ -48,7 +58,7 @@ static __device__ __noinline__ u64 udiv64(u64 n, u64 d) {
 }
 
 // floor(sqrt(n)), digit by digit
-static __device__ __noinline__ u64 isqrt_u64(u64 n) {
+static __host__ __device__ __noinline__ u64 isqrt_u64(u64 n) {
     u64 r = 0, bit = 1ull << 62;
     while (bit > n) bit >>= 2;
     while (bit) {
@@ -60,7 +70,7 @@ static __device__ __noinline__ u64 isqrt_u64(u64 n) {
 }
 
 // (m, k): m = round(N 2^k / D) (ties up) with 2^14 <= N 2^k / D < 2^15
-static __device__ __noinline__ void dyadic_dev(u64 N, u64 D, int* m_out, int* k_out) {
+static __host__ __device__ __noinline__ void dyadic_dev(u64 N, u64 D, int* m_out, int* k_out) {
     int k = 14 + bitlen_u64(D) - bitlen_u64(N);
     for (int it = 0; it < 4; ++it) {   // the estimate is within one of k
         u64 lhs, lo;
@@ -80,7 +90,7 @@ static __device__ __noinline__ void dyadic_dev(u64 N, u64 D, int* m_out, int* k_
 // 2^(delta/1024) in Q15 for delta <= 0: a cubic on the fraction of the
 // base-2 exponent (Horner form, one rounding shift per step) and a right
 // shift for its integer part (DetLLM README, "Layout": DI-Exp)
-__device__ __forceinline__ int exp2q_dev(i64 delta) {
+__host__ __device__ __forceinline__ int exp2q_dev(i64 delta) {
     i64 ip = delta >> 10;                 // floor
     if (ip <= -24) return 0;
     int f = (int)(delta & 1023);
@@ -125,7 +135,7 @@ __host__ __device__ __forceinline__ u64 pow2_recip(u64 v, int e, u64 c, int s) {
 // D = 2^15 + exp2q(-z), round(2^30 / D) = floor((2^31 + D) / 2D) <= 2^15,
 // = 2^15 only for D = 2^15 (every z > 23552); otherwise 15 quotient bits by
 // restoring division in 32 bits
-__device__ __forceinline__ unsigned sigmoid_q15(i64 z) {
+__host__ __device__ __forceinline__ unsigned sigmoid_q15(i64 z) {
     const int Ez = exp2q_dev(-z);
     const unsigned D = 32768u + (unsigned)Ez;            // [2^15, 2^16]
     unsigned q = 32768u;
@@ -142,19 +152,19 @@ __device__ __forceinline__ unsigned sigmoid_q15(i64 z) {
     return q;
 }
 
-__device__ __forceinline__ i64 swiglu_z(int g) {
+__host__ __device__ __forceinline__ i64 swiglu_z(int g) {
     const i64 ag = g < 0 ? -(i64)g : (i64)g;
     return rshr(ag * 47274LL, 17);
 }
 
-__device__ __forceinline__ int swiglu_finish(int g, int u, unsigned q) {
+__host__ __device__ __forceinline__ int swiglu_finish(int g, int u, unsigned q) {
     const i64 sg = g >= 0 ? (i64)q : 32768LL - (i64)q;
     const i64 silu = rshr((i64)g * sg, 15);
     return sat32(rshr(silu * (i64)u, 14));
 }
 
 // one SwiGLU channel from saturated Q12 gate/up values (Q10 result)
-__device__ __forceinline__ int swiglu_dev(int g, int u) {
+__host__ __device__ __forceinline__ int swiglu_dev(int g, int u) {
     return swiglu_finish(g, u, sigmoid_q15(swiglu_z(g)));
 }
 

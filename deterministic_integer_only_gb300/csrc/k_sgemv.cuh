@@ -533,7 +533,7 @@ template <int MINB>
 __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ SgShared sh;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     // ring row pitch: a whole 16-row group arrives in one bulk copy when the
     // rows are not chunked (pitch K); chunked rows get a 64-byte pad so
     // fragment loads of neighbouring rows fall in different banks
