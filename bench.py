@@ -157,9 +157,26 @@ def cpu_baseline(seconds: float = 12.0):
         tok, _ = s.feed([tok])
         n += 1
     dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
+    cores = oracle.max_threads()
+    # the same workload on one core: a fresh sequence, ~seconds/3 of steps
+    oracle.set_threads(1)
+    try:
+        s1 = m.new_seq(PROMPT_LEN + 4096)
+        tok1, _ = s1.feed(prompt)
+        n1 = 0
+        t1 = time.perf_counter()
+        while time.perf_counter() - t1 < seconds / 3:
+            tok1, _ = s1.feed([tok1])
+            n1 += 1
+        dt1 = time.perf_counter() - t1
+    finally:
+        oracle.set_threads(cores)
+    return {"value": n / dt, "unit": "tok/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} B=1 decode steps after the {PROMPT_LEN}-token prefill "
-                      f"(~{seconds:.0f} s of CPU work)"}
+                      f"(~{seconds:.0f} s of CPU work)",
+            "single_core": {"value": n1 / dt1, "unit": "tok/s", "cores": 1,
+                            "sample": f"{n1} B=1 decode steps after the {PROMPT_LEN}-token prefill "
+                                      f"(~{seconds / 3:.0f} s)"}}
 
 
 # int8 tensor-pipe peak of this GPU: mma.sync m16n8k32 s8, measured with a
