@@ -196,7 +196,10 @@ static int stage_copies(detint_model* m, cudaStream_t s,
 static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 static int ilog2i(int n) { int l = 0; while ((1 << l) < n) ++l; return l; }
 
+// every captured step graph; waits for the device first, since one may be in flight
 static void free_graphs(detint_model* m) {
+    if (m->graphs.empty()) return;
+    cudaDeviceSynchronize();
     for (auto& kv : m->graphs) {
         if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
         if (kv.second.seq_dev) cudaFree(kv.second.seq_dev);
@@ -883,6 +886,8 @@ int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const
         for (int i = 0; i < n_seq; ++i) k += std::to_string(seq_ids[i]) + ",";
         auto it = m->graphs.find(k);
         if (it == m->graphs.end()) {
+            // one graph per (batch composition, mode, buffers): bound the cache
+            if (m->graphs.size() >= 512) free_graphs(m);
             GraphEntry ge;
             CK(cudaMalloc(&ge.seq_dev, (size_t)n_seq * 4));
             CK(cudaMemcpy(ge.seq_dev, seq_ids, (size_t)n_seq * 4, cudaMemcpyHostToDevice));
@@ -893,7 +898,11 @@ int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const
             rc = run_forward(m, n_seq, tok, 1, n_seq, nullptr, logits, next_tok, s);
             cudaError_t ce = cudaStreamEndCapture(s, &gph);
             m->tok_seq = saved;
-            if (rc) { cudaFree(ge.seq_dev); return rc; }
+            if (rc) {
+                if (ce == cudaSuccess) cudaGraphDestroy(gph);
+                cudaFree(ge.seq_dev);
+                return rc;
+            }
             if (ce != cudaSuccess) { cudaFree(ge.seq_dev); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
             ce = cudaGraphInstantiate(&ge.exec, gph, 0);
             cudaGraphDestroy(gph);
