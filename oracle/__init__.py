@@ -142,6 +142,21 @@ def requant(acc, mt, kt, mc, f_out):
     return out
 
 
+def requant_wide(acc, mt, kt, mc, f_out):
+    """Requantisation of an int64 accumulator of 16-bit weights (scale
+    m_c / 2^30), one exact 128-bit product and one rounding shift."""
+    acc = np.ascontiguousarray(acc, dtype=np.int64).ravel()
+    n = acc.size
+    mt = np.broadcast_to(np.asarray(mt, np.int32), (n,)).copy()
+    kt = np.broadcast_to(np.asarray(kt, np.int32), (n,)).copy()
+    mc = np.broadcast_to(np.asarray(mc, np.int32), (n,)).copy()
+    out = np.empty(n, np.int64)
+    lib().or_requant_wide_vec(_p(acc, C.c_int64), _p(mt, C.c_int32), _p(kt, C.c_int32),
+                              _p(mc, C.c_int32), C.c_int(f_out), _p(out, C.c_int64), C.c_int(n))
+    check()
+    return out
+
+
 def actquant(x, F):
     x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.int32)
     rows, n = x.shape
@@ -260,7 +275,7 @@ class Model:
         info = np.zeros(16, np.int32)
         L.or_model_info(self._h, _p(info, C.c_int32))
         (self.n_layers, self.hidden, self.n_q, self.n_kv, self.head_dim, self.ffn,
-         self.vocab, self.max_pos, self.qk_norm) = [int(v) for v in info[:9]]
+         self.vocab, self.max_pos, self.qk_norm, self.wbits) = [int(v) for v in info[:10]]
 
     def close(self):
         if self._h:

@@ -317,6 +317,25 @@ i64 or_requant(i64 acc, int32_t mt, int32_t kt, int32_t mc, int Fout) {
     return or_rshr(acc * M, kt + 22 - Fout);
 }
 
+/* GEMM requantisation for 16-bit weights (the exact mode of the BitExact
+ * post, "Three execution paths": wide weights against fixed-point
+ * activations): the int64 accumulator times m_t m_c as one exact 128-bit
+ * product, then one rounding shift; the weight scale is m_c / 2^30 */
+i64 or_requant_wide(i64 acc, int32_t mt, int32_t kt, int32_t mc, int Fout) {
+    const i64 M = (i64)mt * (i64)mc;
+    CHECK(M >= 0 && M < P2(31));
+    CHECK(acc < P2(36) && acc > -P2(36));
+    const int s = kt + 30 - Fout;
+    CHECK(s >= 1 && s <= 100);
+    const __int128 p = (__int128)acc * (__int128)M;
+    /* floor((p + 2^(s-1)) / 2^s) without relying on the sign behaviour of >> */
+    const __int128 q = p + ((__int128)1 << (s - 1));
+    const __int128 one = (__int128)1 << s;
+    __int128 f = q >= 0 ? q / one : -((-q + one - 1) / one);
+    CHECK(f < (__int128)P2(62) && f > -(__int128)P2(62));
+    return (i64)f;
+}
+
 /* SwiGLU of one channel ([README] "Layout": DI-SwiGLU) */
 int32_t or_swiglu(int32_t g, int32_t u) {
     CHECK(g <= (1 << 24) && g >= -(1 << 24) && u <= (1 << 24) && u >= -(1 << 24));
@@ -500,20 +519,22 @@ int or_sample(const int32_t* logits, int n, int32_t inv_temp, int32_t top_k, int
 }
 
 /* ------------------------------------------------------------- the model */
+/* weight matrices are int8 (wbits 8) or int16 (wbits 16, the exact mode);
+ * the pointers below address either, by the model's wbits */
 typedef struct {
     const int16_t *attn_gamma, *ffn_gamma, *q_gamma, *k_gamma;
-    const int8_t* w_qkv; const int32_t* m_qkv;
-    const int8_t* w_o; const int32_t* m_o;
-    const int8_t* w_gate; const int32_t* m_gate;
-    const int8_t* w_up; const int32_t* m_up;
-    const int8_t* w_down; const int32_t* m_down;
+    const void* w_qkv; const int32_t* m_qkv;
+    const void* w_o; const int32_t* m_o;
+    const void* w_gate; const int32_t* m_gate;
+    const void* w_up; const int32_t* m_up;
+    const void* w_down; const int32_t* m_down;
     const int32_t* kvp;
 } or_layer;
 
 typedef struct {
-    int L, H, nq, nkv, d, F, V, max_pos, qk_norm;
+    int L, H, nq, nkv, d, F, V, max_pos, qk_norm, wbits;
     i64 eps_h, eps_qk;
-    const int8_t* embed; const int32_t* embed_m; const int16_t* final_gamma;
+    const void* embed; const int32_t* embed_m; const int16_t* final_gamma;
     const int16_t *rope_cos, *rope_sin;
     or_layer* layers;
     uint8_t* blob; size_t size;
@@ -548,9 +569,11 @@ void* or_model_load(const char* path, int* err) {
     m->blob = (uint8_t*)malloc(m->size);
     if (fread(m->blob, 1, m->size, f) != m->size) { fclose(f); *err = 2; free(m->blob); free(m); return NULL; }
     fclose(f);
-    if (m->size < 256 || memcmp(m->blob, "DETINT01", 8) != 0 || rd32(m->blob + 8) != 1) {
+    if (m->size < 256 || memcmp(m->blob, "DETINT01", 8) != 0 ||
+        (rd32(m->blob + 8) != 1 && !(rd32(m->blob + 8) == 2 && rd32(m->blob + 72) == 16))) {
         *err = 3; free(m->blob); free(m); return NULL;
     }
+    m->wbits = rd32(m->blob + 8) == 2 ? 16 : 8;
     const uint8_t* h = m->blob;
     m->L = rd32(h + 12); m->H = rd32(h + 16); m->nq = rd32(h + 20); m->nkv = rd32(h + 24);
     m->d = rd32(h + 28); m->F = rd32(h + 32); m->V = rd32(h + 36); m->max_pos = rd32(h + 40);
@@ -559,7 +582,8 @@ void* or_model_load(const char* path, int* err) {
     int ok = 1;
     size_t cur = 256;
     int H = m->H, d = m->d, F = m->F, V = m->V, nqkv = (m->nq + 2 * m->nkv) * d;
-    m->embed = (const int8_t*)take(m, &cur, (size_t)V * H, &ok);
+    const size_t wb = (size_t)m->wbits / 8;
+    m->embed = take(m, &cur, (size_t)V * H * wb, &ok);
     m->embed_m = (const int32_t*)take(m, &cur, (size_t)V * 4, &ok);
     m->final_gamma = (const int16_t*)take(m, &cur, (size_t)H * 2, &ok);
     m->rope_cos = (const int16_t*)take(m, &cur, (size_t)m->max_pos * (d / 2) * 2, &ok);
@@ -571,15 +595,15 @@ void* or_model_load(const char* path, int* err) {
         y->ffn_gamma = (const int16_t*)take(m, &cur, (size_t)H * 2, &ok);
         y->q_gamma = (const int16_t*)take(m, &cur, (size_t)d * 2, &ok);
         y->k_gamma = (const int16_t*)take(m, &cur, (size_t)d * 2, &ok);
-        y->w_qkv = (const int8_t*)take(m, &cur, (size_t)nqkv * H, &ok);
+        y->w_qkv = take(m, &cur, (size_t)nqkv * H * wb, &ok);
         y->m_qkv = (const int32_t*)take(m, &cur, (size_t)nqkv * 4, &ok);
-        y->w_o = (const int8_t*)take(m, &cur, (size_t)H * m->nq * d, &ok);
+        y->w_o = take(m, &cur, (size_t)H * m->nq * d * wb, &ok);
         y->m_o = (const int32_t*)take(m, &cur, (size_t)H * 4, &ok);
-        y->w_gate = (const int8_t*)take(m, &cur, (size_t)F * H, &ok);
+        y->w_gate = take(m, &cur, (size_t)F * H * wb, &ok);
         y->m_gate = (const int32_t*)take(m, &cur, (size_t)F * 4, &ok);
-        y->w_up = (const int8_t*)take(m, &cur, (size_t)F * H, &ok);
+        y->w_up = take(m, &cur, (size_t)F * H * wb, &ok);
         y->m_up = (const int32_t*)take(m, &cur, (size_t)F * 4, &ok);
-        y->w_down = (const int8_t*)take(m, &cur, (size_t)H * F, &ok);
+        y->w_down = take(m, &cur, (size_t)H * F * wb, &ok);
         y->m_down = (const int32_t*)take(m, &cur, (size_t)H * 4, &ok);
         y->kvp = (const int32_t*)take(m, &cur, (size_t)m->nkv * (8 + d / 2) * 4, &ok);
     }
@@ -593,11 +617,11 @@ void or_model_free(void* p) {
     free(m->layers); free(m->blob); free(m);
 }
 
-/* info: L, H, nq, nkv, d, F, V, max_pos, qk_norm */
+/* info: L, H, nq, nkv, d, F, V, max_pos, qk_norm, wbits */
 void or_model_info(void* p, int32_t* info) {
     or_model* m = (or_model*)p;
     info[0] = m->L; info[1] = m->H; info[2] = m->nq; info[3] = m->nkv; info[4] = m->d;
-    info[5] = m->F; info[6] = m->V; info[7] = m->max_pos; info[8] = m->qk_norm;
+    info[5] = m->F; info[6] = m->V; info[7] = m->max_pos; info[8] = m->qk_norm; info[9] = m->wbits;
 }
 
 void* or_seq_new(void* p, int max_ctx) {
@@ -617,6 +641,26 @@ void or_seq_free(void* p) {
 }
 
 int or_seq_len(void* p) { return ((or_seq*)p)->len; }
+
+/* sum_k x[k] w[row][k] over a weight row of width K (int8 rows: exact in
+ * int32; int16 rows: exact in int64, |sum| < 127 * 2^15 * K) */
+static i64 dot_row(const or_model* m, const void* w, size_t row, int K, const int8_t* x) {
+    if (m->wbits == 16) {
+        const int16_t* r = (const int16_t*)w + row * (size_t)K;
+        i64 acc = 0;
+        for (int k = 0; k < K; k++) acc += (i64)x[k] * (i64)r[k];
+        return acc;
+    }
+    const int8_t* r = (const int8_t*)w + row * (size_t)K;
+    int32_t acc = 0;
+    for (int k = 0; k < K; k++) acc += (int32_t)x[k] * (int32_t)r[k];
+    return acc;
+}
+
+/* requantisation by the model's weight width (section 5 or section 15) */
+static i64 requant_w(const or_model* m, i64 acc, int32_t mt, int32_t kt, int32_t mc, int Fout) {
+    return m->wbits == 16 ? or_requant_wide(acc, mt, kt, mc, Fout) : or_requant(acc, mt, kt, mc, Fout);
+}
 
 /* One token through the whole decoder at position s->len; appends its K/V.
  * Writes the int32 logits (if logits != NULL) and, if hid != NULL, the
@@ -640,9 +684,14 @@ static void forward_token(or_model* m, or_seq* s, int32_t tok, int32_t* logits, 
     CHECK(tok >= 0 && tok < m->V);
     CHECK(pos < s->max_ctx && pos < m->max_pos);
 
-    /* a1 embedding: tied int8 row times its row scale, onto the Q16 grid */
-    for (int i = 0; i < H; i++)
-        h[i] = (int32_t)or_rshr((i64)m->embed[(size_t)tok * H + i] * m->embed_m[tok], 22 - 16);
+    /* a1 embedding: tied int8 row times its row scale, onto the Q16 grid
+     * (int16 rows: scale m / 2^30) */
+    for (int i = 0; i < H; i++) {
+        if (m->wbits == 16)
+            h[i] = (int32_t)or_rshr((i64)((const int16_t*)m->embed)[(size_t)tok * H + i] * m->embed_m[tok], 30 - 16);
+        else
+            h[i] = (int32_t)or_rshr((i64)((const int8_t*)m->embed)[(size_t)tok * H + i] * m->embed_m[tok], 22 - 16);
+    }
     if (hid) memcpy(hid, h, sizeof(int32_t) * H);
 
     for (int l = 0; l < m->L; l++) {
@@ -652,12 +701,8 @@ static void forward_token(or_model* m, or_seq* s, int32_t tok, int32_t* logits, 
 #ifdef _OPENMP
 #pragma omp parallel for schedule(static)
 #endif
-        for (int n = 0; n < nqkv; n++) {
-            int32_t acc = 0;
-            const int8_t* w = ly->w_qkv + (size_t)n * H;
-            for (int k = 0; k < H; k++) acc += (int32_t)x8[k] * (int32_t)w[k];
-            qkv[n] = (int32_t)sat32(or_requant(acc, mt, kt, ly->m_qkv[n], 12));
-        }
+        for (int n = 0; n < nqkv; n++)
+            qkv[n] = (int32_t)sat32(requant_w(m, dot_row(m, ly->w_qkv, n, H, x8), mt, kt, ly->m_qkv[n], 12));
         /* a4: QK-norm, RoPE, per-channel key rescale, quantisation, cache write */
         const int16_t* cr = m->rope_cos + (size_t)pos * half;
         const int16_t* sr = m->rope_sin + (size_t)pos * half;
@@ -713,10 +758,8 @@ static void forward_token(or_model* m, or_seq* s, int32_t tok, int32_t* logits, 
 #pragma omp parallel for schedule(static)
 #endif
         for (int n = 0; n < H; n++) {
-            int32_t acc = 0;
-            const int8_t* w = ly->w_o + (size_t)n * nq * d;
-            for (int k = 0; k < nq * d; k++) acc += (int32_t)x8[k] * (int32_t)w[k];
-            h[n] = (int32_t)sat32((i64)h[n] + sat32(or_requant(acc, mt, kt, ly->m_o[n], 16)));
+            const i64 acc = dot_row(m, ly->w_o, n, nq * d, x8);
+            h[n] = (int32_t)sat32((i64)h[n] + sat32(requant_w(m, acc, mt, kt, ly->m_o[n], 16)));
         }
         /* a7 + a8: NormQuant, gate/up GEMMs, SwiGLU */
         or_normquant(h, H, ly->ffn_gamma, m->eps_h, x8, &mt, &kt);
@@ -724,12 +767,9 @@ static void forward_token(or_model* m, or_seq* s, int32_t tok, int32_t* logits, 
 #pragma omp parallel for schedule(static)
 #endif
         for (int n = 0; n < F; n++) {
-            int32_t ag = 0, au = 0;
-            const int8_t* wg = ly->w_gate + (size_t)n * H;
-            const int8_t* wu = ly->w_up + (size_t)n * H;
-            for (int k = 0; k < H; k++) { ag += (int32_t)x8[k] * wg[k]; au += (int32_t)x8[k] * wu[k]; }
-            g[n] = (int32_t)sat(or_requant(ag, mt, kt, ly->m_gate[n], 12), P2(24));
-            u[n] = (int32_t)sat(or_requant(au, mt, kt, ly->m_up[n], 12), P2(24));
+            const i64 ag = dot_row(m, ly->w_gate, n, H, x8), au = dot_row(m, ly->w_up, n, H, x8);
+            g[n] = (int32_t)sat(requant_w(m, ag, mt, kt, ly->m_gate[n], 12), P2(24));
+            u[n] = (int32_t)sat(requant_w(m, au, mt, kt, ly->m_up[n], 12), P2(24));
             sv[n] = or_swiglu(g[n], u[n]);
         }
         /* a9: ActQuant(s), down projection, residual add */
@@ -738,10 +778,8 @@ static void forward_token(or_model* m, or_seq* s, int32_t tok, int32_t* logits, 
 #pragma omp parallel for schedule(static)
 #endif
         for (int n = 0; n < H; n++) {
-            int32_t acc = 0;
-            const int8_t* w = ly->w_down + (size_t)n * F;
-            for (int k = 0; k < F; k++) acc += (int32_t)x8[k] * (int32_t)w[k];
-            h[n] = (int32_t)sat32((i64)h[n] + sat32(or_requant(acc, mt, kt, ly->m_down[n], 16)));
+            const i64 acc = dot_row(m, ly->w_down, n, F, x8);
+            h[n] = (int32_t)sat32((i64)h[n] + sat32(requant_w(m, acc, mt, kt, ly->m_down[n], 16)));
         }
         if (hid) memcpy(hid + (size_t)(l + 1) * H, h, sizeof(int32_t) * H);
     }
@@ -752,12 +790,8 @@ static void forward_token(or_model* m, or_seq* s, int32_t tok, int32_t* logits, 
 #ifdef _OPENMP
 #pragma omp parallel for schedule(static)
 #endif
-        for (int v = 0; v < m->V; v++) {
-            int32_t acc = 0;
-            const int8_t* w = m->embed + (size_t)v * H;
-            for (int k = 0; k < H; k++) acc += (int32_t)x8[k] * (int32_t)w[k];
-            logits[v] = (int32_t)sat32(or_requant(acc, mt, kt, m->embed_m[v], 16));
-        }
+        for (int v = 0; v < m->V; v++)
+            logits[v] = (int32_t)sat32(requant_w(m, dot_row(m, m->embed, v, H, x8), mt, kt, m->embed_m[v], 16));
     }
     free(h); free(x8); free(qkv); free(q8); free(mq); free(kq); free(o);
     free(g); free(u); free(sv); free(y);
@@ -793,6 +827,10 @@ void or_isqrt_vec(const u64* x, u64* out, int n) {
 }
 void or_dyadic_vec(const i64* N, const i64* D, int32_t* m, int32_t* k, int n) {
     for (int i = 0; i < n; i++) or_dyadic(N[i], D[i], &m[i], &k[i]);
+}
+void or_requant_wide_vec(const i64* acc, const int32_t* mt, const int32_t* kt, const int32_t* mc,
+                         int Fout, i64* out, int n) {
+    for (int i = 0; i < n; i++) out[i] = or_requant_wide(acc[i], mt[i], kt[i], mc[i], Fout);
 }
 void or_requant_vec(const i64* acc, const int32_t* mt, const int32_t* kt, const int32_t* mc,
                     int Fout, i64* out, int n) {

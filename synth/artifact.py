@@ -1,5 +1,6 @@
 """Seeded synthetic int8 model artifacts (format: the artifact section of the
-arithmetic specification in docs/).
+arithmetic specification in docs/), and their wide-weight (int16) variants
+for the exact mode.
 
 Three shapes: a tiny Qwen3-style model, a Qwen3-0.6B-shaped model and a
 Llama-3.2-1B-shaped model. One numpy PCG64 stream per artifact draws every
@@ -7,6 +8,13 @@ random section in file order. The K/V scales and the per-channel key shifts
 are the offline calibration stand-in: they are derived in float64 from the
 drawn weights and gammas (expected channel RMS of a unit-RMS input, clipped at
 four standard deviations), never from running the model.
+
+A wide artifact (version 2, 16-bit weights) of the same shape and seed holds
+w16 = 256 w8 + r for every linear and embedding weight, with w8 the int8
+artifact's weight and r uniform in [-127, 127] from a second PCG64 stream
+(seed + WIDE_SEED_OFFSET) drawn in file order; every other section is the
+int8 artifact's. Rounding w16 / 256 to the nearest integer gives back w8, so
+the int8 artifact is the int8 rounding of the wide one.
 """
 from __future__ import annotations
 
@@ -20,6 +28,8 @@ import numpy as np
 
 MAGIC = b"DETINT01"
 VERSION = 1
+VERSION_WIDE = 2
+WIDE_SEED_OFFSET = 0x5EED0016
 ALIGN = 256
 HEADER_BYTES = 256
 CLIP_SIGMAS = 4.0
@@ -161,31 +171,50 @@ def _kv_params(shape: ModelShape, attn_gamma, k_gamma, w_qkv, m_qkv) -> np.ndarr
     return out
 
 
-def header_bytes(shape: ModelShape, seed: int) -> bytes:
+def header_bytes(shape: ModelShape, seed: int, wide: bool = False) -> bytes:
     eps_h = int(round(shape.eps * 2.0 ** 32))
     eps_qk = int(round(shape.eps * 2.0 ** 24))
-    hdr = MAGIC + struct.pack("<12i", VERSION, shape.n_layers, shape.hidden, shape.n_q,
-                              shape.n_kv, shape.head_dim, shape.ffn, shape.vocab,
+    hdr = MAGIC + struct.pack("<12i", VERSION_WIDE if wide else VERSION, shape.n_layers, shape.hidden,
+                              shape.n_q, shape.n_kv, shape.head_dim, shape.ffn, shape.vocab,
                               shape.max_pos, shape.qk_norm, eps_h, eps_qk)
     hdr += struct.pack("<qq", seed, shape.rope_theta)
     assert len(hdr) == 72
+    if wide:
+        hdr += struct.pack("<i", 16)                 # weight bits
     return hdr + b"\0" * (HEADER_BYTES - len(hdr))
 
 
-def write_artifact(path: str, shape: ModelShape | str, seed: int) -> str:
-    """Write the artifact for `shape` and `seed` to `path` plus `path.sha256`.
+def _widen(rng2, w8: np.ndarray, chunk: int = 1 << 24) -> np.ndarray:
+    """w16 = 256 w8 + r, r uniform in [-127, 127] (row chunks, file order)."""
+    out = np.empty(w8.shape, dtype=np.int16)
+    flat_in, flat_out = w8.reshape(-1), out.reshape(-1)
+    for i0 in range(0, flat_in.size, chunk):
+        i1 = min(flat_in.size, i0 + chunk)
+        r = rng2.integers(-127, 128, size=i1 - i0, dtype=np.int64)
+        flat_out[i0:i1] = (flat_in[i0:i1].astype(np.int64) * 256 + r).astype(np.int16)
+    return out
+
+
+def write_artifact(path: str, shape: ModelShape | str, seed: int, wide: bool = False) -> str:
+    """Write the artifact for `shape` and `seed` to `path` plus `path.sha256`
+    (the wide variant with 16-bit weights when `wide`).
 
     Returns the hex SHA-256 of the file.
     """
     if isinstance(shape, str):
         shape = MODEL_SHAPES[shape]
     rng = np.random.Generator(np.random.PCG64(seed))
+    rng2 = np.random.Generator(np.random.PCG64(seed + WIDE_SEED_OFFSET)) if wide else None
+
+    def wsec(w8):
+        return _widen(rng2, w8) if wide else w8
+
     H, F, V, d = shape.hidden, shape.ffn, shape.vocab, shape.head_dim
     tmp = path + ".tmp"
     with open(tmp, "wb") as f:
         w = _Writer(f)
-        w.write(header_bytes(shape, seed))
-        w.section(_int8_weights(rng, V, H))          # embed
+        w.write(header_bytes(shape, seed, wide))
+        w.section(wsec(_int8_weights(rng, V, H)))    # embed
         w.section(_scales(rng, V))                   # embed_m
         w.section(_gammas(rng, H))                   # final_gamma
         cos, sin = rope_tables(shape)
@@ -207,8 +236,8 @@ def write_artifact(path: str, shape: ModelShape | str, seed: int) -> str:
             w_down = _int8_weights(rng, H, F)
             m_down = _scales(rng, H)
             kvp = _kv_params(shape, attn_gamma, k_gamma, w_qkv, m_qkv)
-            for arr in (attn_gamma, ffn_gamma, q_gamma, k_gamma, w_qkv, m_qkv, w_o, m_o,
-                        w_gate, m_gate, w_up, m_up, w_down, m_down, kvp):
+            for arr in (attn_gamma, ffn_gamma, q_gamma, k_gamma, wsec(w_qkv), m_qkv, wsec(w_o), m_o,
+                        wsec(w_gate), m_gate, wsec(w_up), m_up, wsec(w_down), m_down, kvp):
                 w.section(arr)
         rem = (-w.pos) % ALIGN
         if rem:
@@ -227,24 +256,27 @@ def read_header(path: str) -> dict:
         raise ValueError("not a detint artifact")
     v = struct.unpack("<12i", b[8:56])
     seed, theta = struct.unpack("<qq", b[56:72])
+    wbits = struct.unpack("<i", b[72:76])[0] if v[0] == VERSION_WIDE else 8
     keys = ["version", "n_layers", "hidden", "n_q", "n_kv", "head_dim", "ffn", "vocab",
             "max_pos", "qk_norm", "eps_h", "eps_qk"]
     d = dict(zip(keys, v))
     d["seed"] = seed
     d["rope_theta"] = theta
+    d["wbits"] = wbits
     return d
 
 
-def artifact_path(shape: str, seed: int, root: str | None = None) -> str:
+def artifact_path(shape: str, seed: int, root: str | None = None, wide: bool = False) -> str:
     root = root or os.environ.get("DETINT_ARTIFACT_DIR") or os.path.join(
         os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "_artifacts")
     os.makedirs(root, exist_ok=True)
-    return os.path.join(root, f"{shape}-seed{seed}.detint")
+    return os.path.join(root, f"{shape}-seed{seed}{'-w16' if wide else ''}.detint")
 
 
-def ensure_artifact(shape: str, seed: int, root: str | None = None) -> str:
-    """Path of the artifact for (shape, seed), writing it first if absent."""
-    p = artifact_path(shape, seed, root)
+def ensure_artifact(shape: str, seed: int, root: str | None = None, wide: bool = False) -> str:
+    """Path of the artifact for (shape, seed), writing it first if absent
+    (the wide variant when `wide`)."""
+    p = artifact_path(shape, seed, root, wide)
     if not (os.path.exists(p) and os.path.exists(p + ".sha256")):
-        write_artifact(p, shape, seed)
+        write_artifact(p, shape, seed, wide)
     return p

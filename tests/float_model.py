@@ -19,6 +19,9 @@ def load(path):
     assert blob[:8] == b"DETINT01"
     (ver, L, H, nq, nkv, d, F, V, max_pos, qk_norm, eps_h, eps_qk) = struct.unpack("<12i", blob[8:56])
     seed, theta = struct.unpack("<qq", blob[56:72])
+    # version 2: 16-bit weights (the exact mode's wide weights), scale m / 2^30
+    wide = ver == 2 and struct.unpack("<i", blob[72:76])[0] == 16
+    wt, kc = (np.int16, 30) if wide else (np.int8, 22)
     cur = [256]
 
     def take(dtype, shape):
@@ -29,8 +32,8 @@ def load(path):
         return a
 
     art = dict(L=L, H=H, nq=nq, nkv=nkv, d=d, F=F, V=V, max_pos=max_pos, qk_norm=qk_norm,
-               eps=eps_h / 2.0 ** 32, theta=theta)
-    art["embed"] = take(np.int8, (V, H))
+               eps=eps_h / 2.0 ** 32, theta=theta, kc=kc)
+    art["embed"] = take(wt, (V, H))
     art["embed_m"] = take(np.int32, (V,))
     art["final_gamma"] = take(np.int16, (H,))
     art["rope_cos"] = take(np.int16, (max_pos, d // 2))
@@ -43,15 +46,15 @@ def load(path):
         ly["ffn_gamma"] = take(np.int16, (H,))
         ly["q_gamma"] = take(np.int16, (d,))
         ly["k_gamma"] = take(np.int16, (d,))
-        ly["w_qkv"] = take(np.int8, (nqkv, H))
+        ly["w_qkv"] = take(wt, (nqkv, H))
         ly["m_qkv"] = take(np.int32, (nqkv,))
-        ly["w_o"] = take(np.int8, (H, nq * d))
+        ly["w_o"] = take(wt, (H, nq * d))
         ly["m_o"] = take(np.int32, (H,))
-        ly["w_gate"] = take(np.int8, (F, H))
+        ly["w_gate"] = take(wt, (F, H))
         ly["m_gate"] = take(np.int32, (F,))
-        ly["w_up"] = take(np.int8, (F, H))
+        ly["w_up"] = take(wt, (F, H))
         ly["m_up"] = take(np.int32, (F,))
-        ly["w_down"] = take(np.int8, (H, F))
+        ly["w_down"] = take(wt, (H, F))
         ly["m_down"] = take(np.int32, (H,))
         ly["kvp"] = take(np.int32, (nkv, 8 + d // 2))
         layers.append(ly)
@@ -59,8 +62,8 @@ def load(path):
     return art
 
 
-def _w(w, m):
-    return w.astype(np.float64) * (m.astype(np.float64) / 2.0 ** 22)[:, None]
+def _w(w, m, kc=22):
+    return w.astype(np.float64) * (m.astype(np.float64) / 2.0 ** kc)[:, None]
 
 
 def _rms(x, g, eps):
@@ -73,7 +76,8 @@ def forward(art, tokens):
     eps = art["eps"]
     T = len(tokens)
     grp = nq // nkv
-    E = _w(art["embed"], art["embed_m"])
+    kc = art["kc"]
+    E = _w(art["embed"], art["embed_m"], kc)
     h = E[np.asarray(tokens)]
     half = d // 2
     inv = float(art["theta"]) ** (-2.0 * np.arange(half) / d)
@@ -87,7 +91,7 @@ def forward(art, tokens):
 
     for ly in art["layers"]:
         y = _rms(h, ly["attn_gamma"] / 4096.0, eps)
-        qkv = y @ _w(ly["w_qkv"], ly["m_qkv"]).T
+        qkv = y @ _w(ly["w_qkv"], ly["m_qkv"], kc).T
         q = qkv[:, : nq * d].reshape(T, nq, d)
         k = qkv[:, nq * d: (nq + nkv) * d].reshape(T, nkv, d)
         v = qkv[:, (nq + nkv) * d:].reshape(T, nkv, d)
@@ -105,11 +109,11 @@ def forward(art, tokens):
             p = np.exp(s)
             p /= p.sum(axis=1, keepdims=True)
             o[:, hq, :] = p @ v[:, g, :]
-        h = h + o.reshape(T, nq * d) @ _w(ly["w_o"], ly["m_o"]).T
+        h = h + o.reshape(T, nq * d) @ _w(ly["w_o"], ly["m_o"], kc).T
         y = _rms(h, ly["ffn_gamma"] / 4096.0, eps)
-        gt = y @ _w(ly["w_gate"], ly["m_gate"]).T
-        up = y @ _w(ly["w_up"], ly["m_up"]).T
+        gt = y @ _w(ly["w_gate"], ly["m_gate"], kc).T
+        up = y @ _w(ly["w_up"], ly["m_up"], kc).T
         s = gt / (1.0 + np.exp(-gt)) * up
-        h = h + s @ _w(ly["w_down"], ly["m_down"]).T
+        h = h + s @ _w(ly["w_down"], ly["m_down"], kc).T
     y = _rms(h, art["final_gamma"] / 4096.0, eps)
     return y @ E.T

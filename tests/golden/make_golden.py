@@ -1,8 +1,9 @@
 """Writes oracle_tiny_seed0.json: the CPU oracle's token stream and chain
 hashes for the tiny model (seed 0, 16-token seeded prompt, 16 greedy steps),
-and oracle_qwen06b_demo.json: the same for the Qwen3-0.6B-shaped model on the
-pages' demo workload (64-token seeded prompt, 512 greedy steps; DetLLM
-README, "Demo").
+oracle_tiny_w16_seed0.json: the same for the tiny model's wide-weight
+(exact-mode) artifact, and oracle_qwen06b_demo.json: the same for the
+Qwen3-0.6B-shaped model on the pages' demo workload (64-token seeded prompt,
+512 greedy steps; DetLLM README, "Demo").
 
 It calls only the oracle and the seeded input generator; no value in the
 fixture comes from the CUDA path. Run: python tests/golden/make_golden.py
@@ -19,8 +20,8 @@ import oracle  # noqa: E402
 import synth   # noqa: E402
 
 
-def run(shape, seed, prompt_len, steps, max_ctx):
-    path = synth.ensure_artifact(shape, seed)
+def run(shape, seed, prompt_len, steps, max_ctx, wide=False):
+    path = synth.ensure_artifact(shape, seed, wide=wide)
     oracle.set_threads(oracle.max_threads())
     m = oracle.Model(path)
     ids = synth.prompt_ids(seed, 0, prompt_len, m.vocab)
@@ -32,7 +33,8 @@ def run(shape, seed, prompt_len, steps, max_ctx):
         h = oracle.chain_hash([lg], h)
         toks.append(am)
     return {
-        "what": f"CPU oracle, {shape} model, seed {seed}, prompt index 0, greedy",
+        "what": f"CPU oracle, {shape} model{' (16-bit weights)' if wide else ''}, seed {seed}, "
+                f"prompt index 0, greedy",
         "seed": seed, "prompt_len": prompt_len, "steps": steps,
         "artifact_sha256": open(path + ".sha256").read().strip(),
         "tokens": toks,
@@ -41,8 +43,19 @@ def run(shape, seed, prompt_len, steps, max_ctx):
     }
 
 
+def write_wide(here):
+    wide = run("tiny", 0, 16, 16, 64, wide=True)
+    with open(os.path.join(here, "oracle_tiny_w16_seed0.json"), "w") as f:
+        json.dump(wide, f, indent=1)
+        f.write("\n")
+    print({k: v for k, v in wide.items() if k != "tokens"})
+
+
 def main():
     here = os.path.dirname(os.path.abspath(__file__))
+    write_wide(here)
+    if "--wide-only" in sys.argv:
+        return
     demo = run("qwen3-0.6b", 0, 64, 512, 640)
     with open(os.path.join(here, "oracle_qwen06b_demo.json"), "w") as f:
         json.dump(demo, f, indent=1)
