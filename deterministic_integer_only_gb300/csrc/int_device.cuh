@@ -131,6 +131,37 @@ __host__ __device__ __forceinline__ u64 pow2_recip(u64 v, int e, u64 c, int s) {
     return q;
 }
 
+// rshr(acc * M, s) with the product formed exactly in 128 bits, for the
+// exact mode's int64 accumulators of 16-bit weights (|acc| < 2^36, M < 2^31,
+// 1 <= s <= 100; the result must fit int64): the product as a two's-
+// complement (hi, lo) pair from 32-bit partial products, plus 2^(s-1), then
+// an arithmetic shift of the pair. The same code runs on host and device.
+__host__ __device__ __forceinline__ i64 rshr_mul128(i64 acc, u64 M, int s) {
+    const bool neg = acc < 0;
+    const u64 a = neg ? (u64)(-acc) : (u64)acc;              // < 2^36
+    const u64 a0 = a & 0xffffffffull, a1 = a >> 32, m0 = M & 0xffffffffull, m1 = M >> 32;
+    const u64 p00 = a0 * m0, p01 = a0 * m1, p10 = a1 * m0, p11 = a1 * m1;
+    const u64 mid = (p00 >> 32) + (p01 & 0xffffffffull) + (p10 & 0xffffffffull);
+    u64 lo = (p00 & 0xffffffffull) | (mid << 32);
+    u64 hi = p11 + (p01 >> 32) + (p10 >> 32) + (mid >> 32);
+    if (neg) {                                                // two's complement of (hi, lo)
+        lo = ~lo + 1;
+        hi = ~hi + (lo == 0 ? 1 : 0);
+    }
+    // + 2^(s-1)
+    if (s - 1 < 64) {
+        const u64 h = 1ull << (s - 1);
+        const u64 nlo = lo + h;
+        hi += nlo < lo ? 1 : 0;
+        lo = nlo;
+    } else {
+        hi += 1ull << (s - 1 - 64);
+    }
+    // arithmetic shift right by s of the signed pair
+    if (s < 64) return (i64)((lo >> s) | (hi << (64 - s)));
+    return (i64)hi >> (s - 64);
+}
+
 // Q15 sigmoid of the SwiGLU gate from z = Q10 of |g| log2 e: with
 // D = 2^15 + exp2q(-z), round(2^30 / D) = floor((2^31 + D) / 2D) <= 2^15,
 // = 2^15 only for D = 2^15 (every z > 23552); otherwise 15 quotient bits by

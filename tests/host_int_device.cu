@@ -74,6 +74,14 @@ int main(int argc, char** argv) {
         for (size_t i = 0; i < g.size(); ++i) out[i] = swiglu_dev(g[i], u[i]);
         save(dir, "swiglu_out", out);
     }
+    {   // exact-mode requantisation: rshr(acc * M, s) through a 128-bit product
+        auto acc = load<i64>(dir, "mul128_acc");
+        auto M = load<u64>(dir, "mul128_m");
+        auto sh = load<int32_t>(dir, "mul128_s");
+        std::vector<i64> out(acc.size());
+        for (size_t i = 0; i < acc.size(); ++i) out[i] = rshr_mul128(acc[i], M[i], sh[i]);
+        save(dir, "mul128_out", out);
+    }
     printf("ok\n");
     return 0;
 }

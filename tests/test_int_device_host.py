@@ -1,8 +1,9 @@
 """The scalar integer routines of the kernels' device header, built for the
 host, against the oracle on the same inputs: the rounding shift, floor square
-root, 15-bit dyadic scales, the cubic exp2 in Q15 and the SwiGLU channel
+root, 15-bit dyadic scales, the cubic exp2 in Q15, the SwiGLU channel
 (DetLLM blog, section "DetLLM": fixed rounding rules, integer exp and
-activation). The GPU parity tests cover these routines inside the kernels;
+activation) and the exact mode's 128-bit requantisation (BitExact LLM post,
+"Three execution paths"). The GPU parity tests cover these routines inside the kernels;
 this catches a change to the header without a GPU."""
 import os
 import shutil
@@ -64,8 +65,19 @@ def host_run(tmp_path_factory):
     g[50001:50005] = [1 << 24, -(1 << 24), 0, 1]
     u[50001:50005] = [1 << 24, 1 << 24, -(1 << 24), -(1 << 24)]
     inputs["swiglu_g"], inputs["swiglu_u"] = g, u
+    # exact-mode requantisation: int64 accumulators of 16-bit weights
+    acc = rng.integers(-(1 << 35), 1 << 35, n, dtype=np.int64)
+    acc[:1000] = rng.integers(-4096, 4096, 1000)
+    mt = rng.integers(1 << 14, (1 << 15) + 1, n).astype(np.int32)
+    mc = rng.integers(1 << 14, 1 << 15, n).astype(np.int32)
+    kt = rng.integers(-2, 40, n).astype(np.int32)
+    inputs["mul128_acc"] = acc
+    inputs["mul128_m"] = (mt.astype(np.int64) * mc.astype(np.int64)).astype(np.uint64)
+    inputs["mul128_s"] = (kt + 30 - 16).astype(np.int32)
+    inputs["_mt"], inputs["_mc"], inputs["_kt"] = mt, mc, kt
     for k, v in inputs.items():
-        v.tofile(str(d / f"{k}.bin"))
+        if not k.startswith("_"):
+            v.tofile(str(d / f"{k}.bin"))
     r = subprocess.run([exe, str(d)], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
 
@@ -100,3 +112,9 @@ def test_exp2q(host_run):
 def test_swiglu(host_run):
     inp, out = host_run
     np.testing.assert_array_equal(out("swiglu_out", np.int32), oracle.swiglu(inp["swiglu_g"], inp["swiglu_u"]))
+
+
+def test_requant_mul128(host_run):
+    inp, out = host_run
+    want = oracle.requant_wide(inp["mul128_acc"], inp["_mt"], inp["_kt"], inp["_mc"], 16)
+    np.testing.assert_array_equal(out("mul128_out", np.int64), want)
