@@ -131,3 +131,17 @@ def test_wide_golden_regression(wide_artifact):
         toks.append(am)
     assert toks == g["tokens"]
     assert oracle.chain_hash(rows).hex()[:12] == g["logits_hash12"]
+
+
+def test_wide_no_bound_violation_qwen_shape():
+    # every asserted bound of the 16-bit weight path (accumulator < 2^36,
+    # shift range, 128-bit product, saturations) on the Qwen3-0.6B shape
+    path = synth.ensure_artifact("qwen3-0.6b", 0, wide=True)
+    m = oracle.Model(path)
+    assert m.wbits == 16
+    ids = synth.prompt_ids(0, 0, 6, m.vocab)
+    s = m.new_seq(16)
+    am, lg, hid = s.feed(ids, want_hidden=True)
+    assert np.abs(hid.astype(np.int64)).max() < 2 ** 30
+    am2, _ = s.feed([am])
+    assert 0 <= am2 < m.vocab
