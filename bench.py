@@ -180,10 +180,10 @@ def cpu_baseline(seconds: float = 12.0):
 
 
 # int8 tensor-pipe peak of this GPU: mma.sync m16n8k32 s8, measured with a
-# register-only issue loop on a GB300 (measurement)
+# register-only loop of independent MMAs on a GB300 (a dp4a loop gives 153)
 MMA_S8_PEAK_TOPS = 150.3
 # DRAM traffic of one lm_head GEMV launch at M=1, read + write, from the last
-# ncu capture (profiles/k_sgemv_lmhead_151936x1024.md). The kernel's
+# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum. The kernel's
 # quantisation prologue changed after that capture (one-pass NormQuant, the
 # multiplier by Newton-Raphson), so the line reports traffic as null and
 # keeps this figure only as the last capture's value.
