@@ -108,26 +108,31 @@ __host__ __device__ __forceinline__ int exp2q_dev(i64 delta) {
 // bits of v; y ~ 2^62 / d from the linear minimax seed 48/17 - 32/17 d' of
 // 1/d' on [1/2, 1) (relative error <= 1/17) and three Newton steps
 // y += y (2^62 - d y) / 2^62 in Q30 (error ~1/17 -> 2^-8 -> 2^-16 -> a few
-// units of 2^-30); q = c y / 2^(30 - s) is then within one of the quotient
-// (within one more when v has more than 32 bits), and an exact check of
-// q v against c 2^(e+s) settles it. Every product stays below 2^64.
+// units of 2^-30), every product 32 x 32 bits; q = c y / 2^(30 - s) is then
+// within one of the quotient (within one more when v has more than 32
+// bits), and the exact remainder N - q v (one 64-bit product, |.| < 3 v)
+// settles it by at most two steps each way.
 __host__ __device__ __forceinline__ u64 pow2_recip(u64 v, int e, u64 c, int s) {
-    const u64 d = e <= 32 ? v << (32 - e) : v >> (e - 32);     // [2^31, 2^32)
-    u64 y = 3031741621ull - ((2021161080ull * d) >> 32);         // Q30, (0.94, 1.89] * 2^30
+    const uint32_t d = (uint32_t)(e <= 32 ? v << (32 - e) : v >> (e - 32));   // [2^31, 2^32)
+    uint32_t y = 3031741621u - (uint32_t)(((u64)2021161080u * d) >> 32);     // Q30, (0.94, 1.89] * 2^30
 #pragma unroll
     for (int it = 0; it < 3; ++it) {
-        const u64 p = d * y;                                      // ~2^62, < 2^63
+        const u64 p = (u64)d * y;                                             // ~2^62, < 2^63
         const bool over = p > (1ull << 62);
         const u64 t = over ? p - (1ull << 62) : (1ull << 62) - p;
-        const u64 corr = (y * (t >> 31)) >> 31;
+        const uint32_t corr = (uint32_t)(((u64)y * (uint32_t)(t >> 31)) >> 31);
         y = over ? y - corr : y + corr;
     }
     const u64 N = c << (e + s);
     u64 q = (c * y) >> (30 - s);
+    long long rem = (long long)(N - q * v);                                   // in (-2v, 3v)
+    const long long vv = (long long)v;
 #pragma unroll
-    for (int i = 0; i < 3; ++i) q -= (q * v > N) ? 1 : 0;
+    for (int i = 0; i < 2; ++i)
+        if (rem < 0) { --q; rem += vv; }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) q += ((q + 1) * v <= N) ? 1 : 0;
+    for (int i = 0; i < 3; ++i)
+        if (rem >= vv) { ++q; rem -= vv; }
     return q;
 }
 

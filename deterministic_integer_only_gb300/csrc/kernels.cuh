@@ -7,7 +7,10 @@
 // the CPU oracle and independent of batch composition, tiling and launch
 // shape (DetLLM README, intro and "Layout"; DetLLM blog, section "DetLLM").
 // Integer sums are exact in any order, so no kernel here needs a fixed
-// reduction order; none uses atomics or floating point.
+// reduction order, and none uses floating point. The only atomics are the
+// integer additions of the split-K tiled GEMMs with a raw output (partial
+// tiles added into a zeroed C) and of the exact int8 x int16 GEMM: integer
+// addition is associative, so the result does not depend on their order.
 #pragma once
 #include "kernels.h"
 #include "int_device.cuh"
@@ -790,7 +793,7 @@ __device__ __forceinline__ int swiglu_tab(int g, int u) {
 #include "k_gemm.cuh"
 #include "k_attn_prefill.cuh"
 #include "k_attn_decode.cuh"
-#include "k_persistent.cuh"
+#include "k_decode_step.cuh"
 #include "k_gemm_w16.cuh"
 namespace detint {
 

@@ -145,44 +145,61 @@ cudaError_t launch_attn_prefill(const PfArgs& a, const CUtensorMap& kmap, const 
                                 int d, cudaStream_t s);
 constexpr int PF_ROWS = 64;   // query rows (token x q head) per prefill attention CTA
 
-// one decode step in one cooperative launch (k_persistent.cuh)
+// one decode step in one cooperative launch (k_decode_step.cuh)
 // the layer's weights, scales and caches (a device array of these)
-struct PdLayer {
+struct StepLayer {
     const int8_t *w_qkv, *w_o, *w_gu, *w_d;
     const int32_t *m_qkv, *m_o, *m_gu, *m_d, *kvp;
     const int16_t *attn_gamma, *ffn_gamma, *q_gamma, *k_gamma;
     int8_t *kc, *vc;
 };
 
-struct PdArgs {
-    const PdLayer* layers;
-    int L, T, H, nq, nkv, d, F, V, lg_grp, qk_norm, max_pos, mbs, lg_H;
+struct StepArgs {
+    const StepLayer* layers;
+    int L, T, H, nq, nkv, d, F, V, lg_grp, lg_nkv, qk_norm, max_pos, mbs;
     long long eps_h, eps_qk;
     const int8_t* embed;
     const int32_t* embed_m;
     const int16_t *final_gamma, *rope_cos, *rope_sin;
     const int32_t* block_table;
-    const int32_t* tokens;      // [T] this step's input ids
-    const int32_t* tok_seq;     // [T] sequence of each token
-    int32_t* tok_pos;           // [T] position (written by the embedding phase)
-    int32_t* seq_len;           // [max_batch] advanced by the final phase
-    int32_t *h, *qkv, *o, *sbuf, *logits, *pval, *pidx;
-    int npart;
-    int32_t* next_tok;
-    int32_t* status;
-    unsigned* bar;              // grid barrier arrival counter (zeroed before each launch)
-    int rg[5][2];               // row groups per CTA (q, r) of the five GEMV shapes
-    int lg_ns;                  // log2 ring stages
-    int attn_cap;               // keys the attention scratch holds
-    size_t off_xs, off_red, off_gam, off_hold;   // dynamic shared memory layout
+    const int32_t* tokens;       // [T] this step's input ids (may alias next_tok)
+    const int32_t* tok_seq;      // [T] sequence of each token
+    int32_t* seq_len;            // [max_batch], advanced at the end of the step
+    // tagged rows (value | tag << 32): [8][H], [8][nqkv], [8][nq d], [8][F], [NG][8][2]
+    unsigned long long *xh, *xqkv, *xo, *xs, *xpart;
+    unsigned* ctl;               // [0] base tag of the next step, [1] base tag of a step that timed out
+    const int32_t* rows;         // [5][NG + 1]: first weight row of each GEMV CTA per GEMV kind
+    int32_t *logits, *next_tok, *status;
+    int NG, NA, ipc, lg_ns;      // GEMV CTAs, attention CTAs, items per attention CTA, log2 ring slots
+    int cap;                     // staged keys per attention item (a multiple of 64)
+    int scap;                    // score-row capacity (a multiple of 16 >= every context)
+    int spin;                    // polls before a wait gives up
+    int stall;                   // > 0: the final wait expects a tag nobody writes, bounded by stall polls
+    // dynamic shared memory of a GEMV CTA: weight ring, int8 tile [T][XP],
+    // int32 input rows [T][XP], gamma [H], owned residual rows, channel scales
+    int off_x8, off_xin, off_gs, off_hown, off_mcs;
 };
-
-// d: head_dim, grp: q heads per kv head; cudaErrorNotSupported for shapes
-// without an instantiation
-cudaError_t launch_decode_persistent(const PdArgs& a, int grid, size_t smem, cudaStream_t s);
-bool decode_persistent_supported(int d, int grp);
-// the occupancy check of the cooperative launch (1 CTA per SM with smem bytes)
-bool decode_persistent_fits(int d, int grp, size_t smem);
+constexpr int STEP_THREADS = 320;
+constexpr int STEP_SLOT = 16384;        // weight ring slot bytes
+constexpr int STEP_HOWN = 64;           // residual rows a GEMV CTA owns at most
+constexpr int STEP_MCS = 1024;          // channel scales a GEMV CTA stages per phase
+constexpr int STEP_NP = 64;             // tagged pairs per thread a prologue can track
+// weight rows per ring slot for reduction length K (<= 16)
+__host__ __device__ inline int step_rows_per_slot(int K) {
+    int q = 16;
+    while (q * K > STEP_SLOT) --q;
+    return q;
+}
+// attention CTA shared memory: per item K [cap][d] and V^T [cap/64][d][64];
+// then q [G][d], scores [G][scap] int32, E_lo/E_hi [G][scap], P.V limbs [G][d][2]
+__host__ __device__ inline size_t step_att_bytes(int G, int d, int cap, int ipc, int scap) {
+    return (size_t)ipc * 2 * cap * d + (size_t)G * d + (size_t)G * scap * 6 + (size_t)G * d * 8;
+}
+// d: head_dim, grp: q heads per kv head; false for shapes without an instantiation
+bool decode_step_supported(int d, int grp);
+// sets the kernel's shared-memory limit; true when one CTA of smem bytes fits an SM
+bool decode_step_fits(int d, int grp, size_t smem);
+cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, cudaStream_t s);
 
 cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int rows, int npart,
                                 int32_t* next_tok, const int32_t* tok_seq, int32_t* seq_len,

@@ -432,36 +432,34 @@ int32_t* standalone_status() {
     return addr[dev];
 }
 
-using PdFn = void (*)(PdArgs);
-static PdFn pd_kernel(int d, int grp) {
-    if (d == 128 && grp == 2) return k_decode_persistent<4, 2>;
-    if (d == 64 && grp == 4) return k_decode_persistent<2, 4>;
-    if (d == 64 && grp == 2) return k_decode_persistent<2, 2>;
+using StepFn = void (*)(StepArgs);
+static StepFn step_kernel(int d, int grp) {
+    if (d == 128 && grp == 2) return k_decode_step<4, 2>;
+    if (d == 64 && grp == 4) return k_decode_step<2, 4>;
+    if (d == 64 && grp == 2) return k_decode_step<2, 2>;
     return nullptr;
 }
-bool decode_persistent_supported(int d, int grp) { return pd_kernel(d, grp) != nullptr; }
-bool decode_persistent_fits(int d, int grp, size_t smem) {
-    PdFn k = pd_kernel(d, grp);
+bool decode_step_supported(int d, int grp) { return step_kernel(d, grp) != nullptr; }
+bool decode_step_fits(int d, int grp, size_t smem) {
+    StepFn k = step_kernel(d, grp);
     if (!k || smem > 227 * 1024) return false;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return false;
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, SG_THREADS, smem) != cudaSuccess) return false;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, STEP_THREADS, smem) != cudaSuccess) return false;
     return nb >= 1;
 }
 
-cudaError_t launch_decode_persistent(const PdArgs& a, int grid, size_t smem, cudaStream_t s) {
-    PdFn k = pd_kernel(a.d, 1 << a.lg_grp);
+cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, cudaStream_t s) {
+    StepFn k = step_kernel(a.d, 1 << a.lg_grp);
     if (!k) return cudaErrorNotSupported;
-    cudaError_t e = cudaMemsetAsync(a.bar, 0, sizeof(unsigned), s);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(SG_THREADS);
+    cfg.blockDim = dim3(STEP_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: the grid barriers need it
+    at[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: CTAs poll one another's rows
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;

@@ -147,13 +147,17 @@ struct detint_model {
     int tc_prefill = 1;      // 0: prefill attention through the per-token kernel (tests compare both)
     int staged_decode = 1;   // 0: decode attention through the per-token kernel (tests compare both)
     int dec_cap = 0;         // keys the staged decode attention holds (0: unsupported shape)
-    int dec_staged = 0;      // this step's decode: 0 kernels (global K/V), 1 kernels (staged K/V), 2 one persistent launch
-    int persistent = 0;      // 1: decode steps as one persistent launch where supported (tests compare both)
-    int pd_ok = 0;           // the persistent step supports this shape
-    PdLayer* pd_layers = nullptr;
-    unsigned* pd_bar = nullptr;
-    size_t pd_smem = 0, pd_off[4] = {0, 0, 0, 0};
-    int pd_lg_ns = 0, pd_cap = 0, nsm = 0;
+    int dec_staged = 0;      // this step's decode: 0 kernels (global K/V), 1 kernels (staged K/V), 2 one launch
+    int persistent = 0;      // 1: decode steps of up to 8 sequences as one launch where supported
+    // the one-launch decode step (k_decode_step.cuh): per batch size T = 1..8,
+    // its CTA roles and attention staging; its tagged exchange rows and tags
+    struct StepCfg { int ok, NG, NA, ipc, cap, lg_ns, off[5]; } st_cfg[8] = {};
+    StepLayer* st_layers = nullptr;
+    unsigned long long* st_x = nullptr;
+    unsigned* st_ctl = nullptr;
+    int32_t* st_rows = nullptr;    // [8][5 x (NG + 1), in a stride of 5 (nsm + 1)]
+    size_t st_smem = 0, st_xoff[5] = {0, 0, 0, 0, 0};
+    int st_scap = 0, st_stall = 0, nsm = 0;
     int32_t* gws = nullptr;  // split-K workspace of the short-M tiled GEMMs
     size_t gws_elems = 0;
     int* gcnt = nullptr;     // their tile counters (self-resetting)
@@ -275,12 +279,12 @@ static cudaError_t gemm_epi(detint_model* m, const int8_t* X, const int8_t* W, i
 // m->rows (prefill) or for every token (decode, rows == nullptr).
 // Decode with at most 8 sequences: 5 kernels per layer chained by
 // programmatic dependent launch (weights stream ahead of the dependency).
-static int run_decode_persistent(detint_model* m, int T, const int32_t* tokens, int32_t* logits,
-                                 int32_t* next_tok, cudaStream_t s);
+static int run_decode_step(detint_model* m, int T, const int32_t* tokens, int32_t* logits,
+                           int32_t* next_tok, cudaStream_t s);
 
 static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32_t* logits,
                             int32_t* next_tok, cudaStream_t s) {
-    if (m->dec_staged == 2) return run_decode_persistent(m, T, tokens, logits, next_tok, s);
+    if (m->dec_staged == 2) return run_decode_step(m, T, tokens, logits, next_tok, s);
     const int H = m->H, d = m->d, nq = m->nq, nkv = m->nkv, F = m->F;
     const int nqkv = (nq + 2 * nkv) * d;
     // from 3 sequences on, each row is quantised once by a row kernel (one CTA
@@ -457,85 +461,119 @@ static int sync_block_table(detint_model* m, cudaStream_t s) {
     return rc;
 }
 
-// The persistent decode step: its shared-memory layout (weight ring, int8
-// activation tile, partial sums, gamma, residual/scale staging), the
-// attention scratch capacity, the per-layer pointer table and the grid
-// barrier words. Leaves pd_ok = 0 for shapes it does not cover.
-static int setup_persistent(detint_model* m) {
-    m->pd_ok = 0;
-    const int H = m->H, d = m->d, G = 1 << m->lg_grp, nqd = m->nq * d, F = m->F;
-    if ((H & (H - 1)) || !decode_persistent_supported(d, G)) return DETINT_OK;
+// The one-launch decode step: for each batch size T = 1..8 the CTA roles
+// (NA attention CTAs for T x nkv items, the rest GEMV CTAs), each GEMV CTA's
+// weight rows per GEMV kind, the attention staging capacity; the shared
+// memory layout; the tagged exchange rows (zeroed: tag 0 is never expected)
+// and the tag base (starting at 1). Leaves every st_cfg[].ok = 0 for shapes
+// it does not cover (decode then runs one kernel per phase).
+static int setup_step(detint_model* m) {
+    const int H = m->H, d = m->d, G = 1 << m->lg_grp, nqd = m->nq * d, F = m->F, nkv = m->nkv;
+    const int nqkv = (m->nq + 2 * nkv) * d;
+    if ((H & (H - 1)) || (nkv & (nkv - 1)) || G > 7 || !decode_step_supported(d, G)) return DETINT_OK;
     for (int K : {H, nqd, F})
-        if ((K & 63) || (K > 1024 && (K & 1023))) return DETINT_OK;
-    if (cudaDeviceGetAttribute(&m->nsm, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess) return DETINT_OK;
+        if ((K & 15) || K > STEP_SLOT) return DETINT_OK;
     int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&m->nsm, cudaDevAttrMultiProcessorCount, dev);
-    const size_t Kmax = (size_t)std::max(H, std::max(nqd, F));
-    const size_t xs = 8 * (Kmax + 64), red = 4 * 1024 * 4, gam = ((size_t)H * 2 + 15) & ~(size_t)15;
-    for (int lg = 3; lg >= 1; --lg) {
-        const size_t ring = ((size_t)1 << lg) * 16 * 1088;
-        const size_t o_xs = ring, o_red = o_xs + xs, o_gam = o_red + red, o_hold = o_gam + gam;
-        const size_t total = o_hold + 512 * 4;
-        if (total > 220 * 1024) continue;
-        // attention scratch over the tile and partial sums: q [G][d], S [G][cap]
-        // int32, E_lo/E_hi [G][cap], P.V limbs [G][d][2] int32
-        const size_t region = o_gam - o_xs, fixed = (size_t)G * d + (size_t)G * d * 8;
-        if (region <= fixed) continue;
-        int cap = (int)((region - fixed) / ((size_t)G * 6));
-        cap &= ~15;
-        if (cap < 16 || !decode_persistent_fits(d, G, total)) continue;
-        m->pd_lg_ns = lg;
-        m->pd_smem = total;
-        m->pd_off[0] = o_xs; m->pd_off[1] = o_red; m->pd_off[2] = o_gam; m->pd_off[3] = o_hold;
-        m->pd_cap = std::min(cap, m->max_ctx);
-        break;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&m->nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return DETINT_OK;
+    const size_t dyn = 220 * 1024;
+    if (!decode_step_fits(d, G, dyn)) return DETINT_OK;
+    m->st_smem = dyn;
+    m->st_scap = (m->max_ctx + 15) & ~15;
+    const int nsm = m->nsm;
+    std::vector<int32_t> rows((size_t)8 * 5 * (nsm + 1), 0);
+    const int Ns[5] = {nqkv, H, 2 * F, H, m->V}, unit[5] = {1, 1, 2, 1, 1}, Ks[5] = {H, nqd, H, F, H};
+    bool any = false;
+    for (int T = 1; T <= 8; ++T) {
+        auto& c = m->st_cfg[T - 1];
+        c.ok = 0;
+        const int items = T * nkv;
+        const int NA = items <= 16 ? items : std::min(items, 32);
+        const int ipc = (items + NA - 1) / NA;
+        const int NG = nsm - NA;
+        if (NG < 1 || ipc > 4) continue;
+        bool fit = (H + NG - 1) / NG <= STEP_HOWN;
+        const int lgT = T <= 1 ? 0 : (T <= 2 ? 1 : (T <= 4 ? 2 : 3));
+        const int gn = 32 * (8 >> lgT);
+        for (int k = 0; k < 5; ++k) {
+            if (k < 4 && Ns[k] / unit[k] < NG) fit = false;       // every GEMV CTA owns rows of every layer phase
+            if ((Ks[k] / 2 + gn - 1) / gn > STEP_NP) fit = false;  // prologue pairs per thread
+        }
+        const size_t fixed = (size_t)G * d + (size_t)G * m->st_scap * 6 + (size_t)G * d * 8;
+        if (!fit || fixed > dyn) continue;
+        int cap = (int)((dyn - fixed) / ((size_t)ipc * 2 * d)) & ~(KV_BLK - 1);
+        cap = std::min(cap, (m->st_scap + KV_BLK - 1) & ~(KV_BLK - 1));
+        // GEMV CTA layout: ring of 8 (else 4) slots, the int8 tile and the
+        // int32 input rows of T tokens, gamma, owned residual rows, scales
+        const int Kmax = std::max(H, std::max(nqd, F)), XP = Kmax + 16;
+        const size_t x8b = (size_t)T * XP, xinb = (size_t)T * XP * 4, gsb = ((size_t)H * 2 + 15) & ~(size_t)15;
+        const size_t rest = x8b + xinb + gsb + (size_t)8 * STEP_HOWN * 4 + (size_t)2 * STEP_MCS * 4;
+        int lg_ns = 3;
+        while (lg_ns > 2 && ((size_t)STEP_SLOT << lg_ns) + rest > dyn) --lg_ns;
+        if (((size_t)STEP_SLOT << lg_ns) + rest > dyn) continue;
+        c.lg_ns = lg_ns;
+        c.off[0] = STEP_SLOT << lg_ns;
+        c.off[1] = (int)(c.off[0] + x8b);
+        c.off[2] = (int)(c.off[1] + xinb);
+        c.off[3] = (int)(c.off[2] + gsb);
+        c.off[4] = (int)(c.off[3] + (size_t)8 * STEP_HOWN * 4);
+        c.NG = NG; c.NA = NA; c.ipc = ipc; c.cap = std::max(cap, 0);
+        int32_t* rt = rows.data() + (size_t)(T - 1) * 5 * (nsm + 1);
+        for (int k = 0; k < 5; ++k)
+            for (int i = 0; i <= NG; ++i)
+                rt[k * (NG + 1) + i] = (int32_t)(unit[k] * (((long long)i * (Ns[k] / unit[k])) / NG));
+        c.ok = 1;
+        any = true;
     }
-    if (m->pd_smem == 0) return DETINT_OK;
-    std::vector<PdLayer> pl(m->L);
+    if (!any) return DETINT_OK;
+    std::vector<StepLayer> pl(m->L);
     for (int l = 0; l < m->L; ++l) {
         const LayerW& w = m->layers[l];
-        PdLayer& p = pl[l];
+        StepLayer& p = pl[l];
         p.w_qkv = w.w_qkv; p.w_o = w.w_o; p.w_gu = w.w_gu; p.w_d = w.w_d;
         p.m_qkv = w.m_qkv; p.m_o = w.m_o; p.m_gu = w.m_gu; p.m_d = w.m_d; p.kvp = w.kvp;
         p.attn_gamma = w.attn_gamma; p.ffn_gamma = w.ffn_gamma; p.q_gamma = w.q_gamma; p.k_gamma = w.k_gamma;
         p.kc = m->kcache + (size_t)l * m->kv_layer_elems;
         p.vc = m->vcache + (size_t)l * m->kv_layer_elems;
     }
-    if (cudaMalloc(&m->pd_layers, sizeof(PdLayer) * pl.size()) != cudaSuccess ||
-        cudaMalloc(&m->pd_bar, 2 * sizeof(unsigned)) != cudaSuccess)
-        return fail(DETINT_E_OOM, "persistent decode tables");
-    if (cudaMemcpy(m->pd_layers, pl.data(), sizeof(PdLayer) * pl.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemset(m->pd_bar, 0, 2 * sizeof(unsigned)) != cudaSuccess)
-        return fail(DETINT_E_CUDA, "persistent decode tables");
-    m->pd_ok = 1;
+    const size_t nx[5] = {(size_t)8 * H, (size_t)8 * nqkv, (size_t)8 * nqd, (size_t)8 * F, (size_t)nsm * 16};
+    size_t tot = 0;
+    for (int k = 0; k < 5; ++k) { m->st_xoff[k] = tot; tot += (nx[k] + 1) & ~(size_t)1; }
+    const unsigned ctl0[2] = {1u, 0u};
+    if (cudaMalloc(&m->st_layers, sizeof(StepLayer) * pl.size()) != cudaSuccess ||
+        cudaMalloc(&m->st_x, tot * 8) != cudaSuccess || cudaMalloc(&m->st_ctl, 2 * sizeof(unsigned)) != cudaSuccess ||
+        cudaMalloc(&m->st_rows, rows.size() * 4) != cudaSuccess)
+        return fail(DETINT_E_OOM, "decode step tables");
+    if (cudaMemcpy(m->st_layers, pl.data(), sizeof(StepLayer) * pl.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(m->st_x, 0, tot * 8) != cudaSuccess ||
+        cudaMemcpy(m->st_ctl, ctl0, sizeof ctl0, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(m->st_rows, rows.data(), rows.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+        return fail(DETINT_E_CUDA, "decode step tables");
     return DETINT_OK;
 }
 
-static int run_decode_persistent(detint_model* m, int T, const int32_t* tokens, int32_t* logits,
-                                 int32_t* next_tok, cudaStream_t s) {
-    PdArgs a{};
-    a.layers = m->pd_layers;
+static int run_decode_step(detint_model* m, int T, const int32_t* tokens, int32_t* logits,
+                           int32_t* next_tok, cudaStream_t s) {
+    const auto& c = m->st_cfg[T - 1];
+    StepArgs a{};
+    a.layers = m->st_layers;
     a.L = m->L; a.T = T; a.H = m->H; a.nq = m->nq; a.nkv = m->nkv; a.d = m->d; a.F = m->F; a.V = m->V;
-    a.lg_grp = m->lg_grp; a.qk_norm = m->qk_norm; a.max_pos = m->max_ctx; a.mbs = m->mbs;
-    a.lg_H = ilog2i(m->H);
-    a.eps_h = m->eps_h; a.eps_qk = m->eps_qk;
+    a.lg_grp = m->lg_grp; a.lg_nkv = ilog2i(m->nkv); a.qk_norm = m->qk_norm; a.max_pos = m->max_ctx;
+    a.mbs = m->mbs; a.eps_h = m->eps_h; a.eps_qk = m->eps_qk;
     a.embed = m->embed; a.embed_m = m->embed_m; a.final_gamma = m->final_gamma;
     a.rope_cos = m->rope_cos; a.rope_sin = m->rope_sin; a.block_table = m->block_table;
-    a.tokens = tokens; a.tok_seq = m->tok_seq; a.tok_pos = m->tok_pos; a.seq_len = m->seq_len_dev;
-    a.h = m->h; a.qkv = m->qkv; a.o = m->o; a.sbuf = m->sbuf; a.logits = logits ? logits : m->logits_int;
-    a.pval = m->pval; a.pidx = m->pidx; a.npart = m->npart; a.next_tok = next_tok; a.status = m->status;
-    a.bar = m->pd_bar;
-    const int nqkv = (m->nq + 2 * m->nkv) * m->d;
-    const int Ns[5] = {nqkv, m->H, 2 * m->F, m->H, m->V};
-    for (int p = 0; p < 5; ++p) {
-        const int Gp = (Ns[p] + 15) / 16;
-        a.rg[p][0] = Gp / m->nsm;
-        a.rg[p][1] = Gp % m->nsm;
-    }
-    a.lg_ns = m->pd_lg_ns;
-    a.attn_cap = m->pd_cap;
-    a.off_xs = m->pd_off[0]; a.off_red = m->pd_off[1]; a.off_gam = m->pd_off[2]; a.off_hold = m->pd_off[3];
-    CK(launch_decode_persistent(a, m->nsm, m->pd_smem, s));
+    a.tokens = tokens; a.tok_seq = m->tok_seq; a.seq_len = m->seq_len_dev;
+    a.xh = m->st_x + m->st_xoff[0]; a.xqkv = m->st_x + m->st_xoff[1]; a.xo = m->st_x + m->st_xoff[2];
+    a.xs = m->st_x + m->st_xoff[3]; a.xpart = m->st_x + m->st_xoff[4];
+    a.ctl = m->st_ctl;
+    a.rows = m->st_rows + (size_t)(T - 1) * 5 * (m->nsm + 1);
+    a.logits = logits ? logits : m->logits_int; a.next_tok = next_tok; a.status = m->status;
+    a.NG = c.NG; a.NA = c.NA; a.ipc = c.ipc; a.lg_ns = c.lg_ns; a.cap = c.cap; a.scap = m->st_scap;
+    a.spin = 1 << 20;
+    a.stall = m->st_stall;
+    a.off_x8 = c.off[0]; a.off_xin = c.off[1]; a.off_gs = c.off[2]; a.off_hown = c.off[3]; a.off_mcs = c.off[4];
+    CK(launch_decode_step(a, c.NG + c.NA, m->st_smem, s));
     return DETINT_OK;
 }
 
@@ -572,10 +610,12 @@ void detint_free(detint_model* m) {
     if (m->block_table) cudaFree(m->block_table);
     if (m->seq_len_dev) cudaFree(m->seq_len_dev);
     if (m->status) cudaFree(m->status);
-    if (m->pd_layers) cudaFree(m->pd_layers);
+    if (m->st_layers) cudaFree(m->st_layers);
+    if (m->st_x) cudaFree(m->st_x);
+    if (m->st_ctl) cudaFree(m->st_ctl);
+    if (m->st_rows) cudaFree(m->st_rows);
     if (m->gws) cudaFree(m->gws);
     if (m->gcnt) cudaFree(m->gcnt);
-    if (m->pd_bar) cudaFree(m->pd_bar);
     if (m->pinned) cudaFreeHost(m->pinned);
     if (m->pinned_done) cudaEventDestroy(m->pinned_done);
     delete m;
@@ -758,7 +798,7 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
     if (rc != DETINT_OK) { detint_free(m); return rc; }
     ce = kernels_init();
     if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
-    rc = setup_persistent(m);
+    rc = setup_step(m);
     if (rc != DETINT_OK) { detint_free(m); return rc; }
     {
         // split-K workspace for GEMMs of at most 64 rows: 8 splits of 64 x N
@@ -869,7 +909,8 @@ int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const
         int mx = 0;
         for (int i = 0; i < n_seq; ++i) mx = std::max(mx, m->seq_len[seq_ids[i]] + 1);
         m->dec_staged = (m->staged_decode && m->dec_cap > 0 && mx <= m->dec_cap) ? 1 : 0;
-        if (m->persistent && m->pd_ok && m->fused_decode && n_seq <= 8 && mx <= m->pd_cap) m->dec_staged = 2;
+        if (m->persistent && n_seq <= 8 && m->st_cfg[n_seq - 1].ok && m->fused_decode && mx <= m->st_scap)
+            m->dec_staged = 2;
     }
     const bool graph = m->use_graph && s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread;
     if (!graph) {
@@ -1056,7 +1097,14 @@ int detint_set_graph(detint_model* m, int enable) {
 }
 
 int detint_set_option(detint_model* m, int option, int value) {
-    if (!m || (value != 0 && value != 1)) return fail(DETINT_E_ARG, "bad argument");
+    if (!m) return fail(DETINT_E_ARG, "bad argument");
+    if (option == DETINT_OPT_WAIT_TEST) {
+        if (value < 0) return fail(DETINT_E_ARG, "bad argument");
+        m->st_stall = value;
+        free_graphs(m);
+        return DETINT_OK;
+    }
+    if (value != 0 && value != 1) return fail(DETINT_E_ARG, "bad argument");
     if (option == DETINT_OPT_GRAPH) m->use_graph = value;
     else if (option == DETINT_OPT_FUSED_DECODE) { m->fused_decode = value; free_graphs(m); }
     else if (option == DETINT_OPT_TC_PREFILL) m->tc_prefill = value;

@@ -66,7 +66,9 @@ int detint_load(const char* artifact_path, int max_batch, int max_ctx, detint_st
  * distinct sequences and return the logits of each sequence's last new
  * position (DetLLM blog, "DetLLM": prefill and decode see the same cached
  * bits). seq_ids: host int32[n_seq], each in [0, max_batch), distinct.
- * cu_lens: host int32[n_seq + 1], cu_lens[0] = 0, non-decreasing, each
+ * cu_lens: host int32[n_seq + 1] (a host array, not a device one: the
+ * library plans KV blocks and attention query blocks from the lengths
+ * before it enqueues any kernel), cu_lens[0] = 0, non-decreasing, each
  * length >= 1; tokens of sequence i are tokens[cu_lens[i] .. cu_lens[i+1]).
  * tokens: device int32[cu_lens[n_seq]]. logits: device int32[n_seq][vocab]
  * or NULL. next_tok: device int32[n_seq] (argmax, ties to the lowest id).
@@ -76,11 +78,16 @@ int detint_load(const char* artifact_path, int max_batch, int max_ctx, detint_st
 int detint_prefill(detint_model* m, int n_seq, const int32_t* seq_ids, const int32_t* cu_lens,
                    const int32_t* tokens, int32_t* logits, int32_t* next_tok, detint_stream_t s);
 
-/* One greedy decode step: one new token per sequence. seq_ids: host
- * int32[n_seq]; tok: device int32[n_seq]; logits: device int32[n_seq][vocab]
- * or NULL; next_tok: device int32[n_seq] (may alias tok). With graphs
- * enabled (default) the step is one CUDA-graph launch, re-captured when the
- * sequence set or a pointer changes. Errors: ARG, SEQ, CTX, CUDA. */
+/* One greedy decode step: one new token per sequence, appended to its KV
+ * cache, then int32 logits and the tie-low argmax of the new position
+ * (DetLLM blog, "DetLLM": decode reads the same cached integers a prefill
+ * writes, and argmax prefers the smallest token id on ties; README, "Usage":
+ * generate(ids, max_new, use_graph) is a prefill followed by such steps).
+ * seq_ids: host int32[n_seq]; tok: device int32[n_seq]; logits: device
+ * int32[n_seq][vocab] or NULL; next_tok: device int32[n_seq] (may alias
+ * tok). With graphs enabled (default) the step is one CUDA-graph launch,
+ * re-captured when the sequence set or a pointer changes.
+ * Errors: ARG, SEQ, CTX, CUDA. */
 int detint_decode_step(detint_model* m, int n_seq, const int32_t* seq_ids, const int32_t* tok,
                        int32_t* logits, int32_t* next_tok, detint_stream_t s);
 
@@ -114,8 +121,12 @@ int detint_gemm_i8(const int8_t* A, const int8_t* B, int32_t* C, int M, int N, i
 #define DETINT_ARGMAX_NOALLOC_MAX_COLS 1048576
 int detint_argmax_noalloc(const int32_t* logits, int rows, int n, int32_t* out, detint_stream_t s);
 
-/* Forget a sequence's cached context (length back to 0). Synchronises the
- * device first. Errors: ARG, SEQ, CUDA. */
+/* Forget a sequence's cached context (length back to 0) and return its KV
+ * blocks to the pool. No passage of the pages defines this: it is library
+ * housekeeping for reusing a sequence slot (the scheduler cases of the
+ * BitExact LLM post, "What the checks actually compare": preemption then
+ * recomputation, start from an emptied slot). Synchronises the device
+ * first. Errors: ARG, SEQ, CUDA. */
 int detint_reset_seq(detint_model* m, int seq_id);
 
 /* Current length of a sequence (host-side bookkeeping). */
@@ -124,7 +135,8 @@ int detint_seq_len(detint_model* m, int seq_id, int32_t* len);
 /* Read and clear the device status word after synchronising `s`.
  * flags: host int32[8] or NULL; slots 0 token id out of range, 1 context
  * clamp, 2 residual saturation, 3 gate/up saturation, 4 logit saturation,
- * 5 q/k/v saturation. Returns DETINT_E_TOKEN if slot 0 is set, else
+ * 5 q/k/v saturation, 6 a bounded wait of a kernel timed out (its results
+ * are invalid). Returns DETINT_E_TOKEN if slot 0 is set, else
  * DETINT_E_CTX if slot 1 is set, else DETINT_OK. */
 int detint_status(detint_model* m, int32_t* flags, detint_stream_t s);
 
@@ -197,20 +209,31 @@ int detint_sample(const int32_t* logits, int rows, int n, const detint_sampling_
  * ready, the default while every context fits that copy; 0 = the attention
  * kernel that reads the cache from global memory) and DETINT_OPT_PERSISTENT
  * (1 = a fused decode step of up to 8 sequences runs as one cooperative
- * launch of one CTA per SM with grid barriers between its phases, where the
- * shape and context fit; 0 = one kernel per phase, the default, measured
- * faster on GB300). Every setting gives bit-identical results. Errors: ARG. */
+ * launch of one CTA per SM whose phases hand rows to one another as tagged
+ * words, where the shape fits; 0 = one kernel per phase). Every setting gives
+ * bit-identical results.
+ * DETINT_OPT_WAIT_TEST (value >= 0) exercises the failure path of the
+ * one-launch step's bounded waits: while it is positive, the step's final
+ * wait expects a tag that no CTA writes and gives up after `value` polls,
+ * so the step ends with status slot 6 (a wait timed out) set and an invalid
+ * token, without hanging; 0 (the default) turns it off. No passage of the
+ * pages: a test hook of the library's failure detection.
+ * Errors: ARG. */
 enum { DETINT_OPT_GRAPH = 0, DETINT_OPT_FUSED_DECODE = 1, DETINT_OPT_TC_PREFILL = 2,
-       DETINT_OPT_STAGED_DECODE = 3, DETINT_OPT_PERSISTENT = 4 };
+       DETINT_OPT_STAGED_DECODE = 3, DETINT_OPT_PERSISTENT = 4, DETINT_OPT_WAIT_TEST = 5 };
 int detint_set_option(detint_model* m, int option, int value);
 
 /* Shape of the loaded model: info[0..9] = n_layers, hidden, n_q, n_kv,
  * head_dim, ffn, vocab, max_pos, qk_norm, max_batch; info[10] = max_ctx. */
 int detint_model_info(detint_model* m, int32_t* info);
 
-/* Release everything the model owns. NULL is a no-op. */
+/* Release everything the model owns. NULL is a no-op. No passage of the
+ * pages: library housekeeping. */
 void detint_free(detint_model* m);
 
+/* A static English name of an error code ("unknown error" for other
+ * values); detint_last_error gives the detail of this thread's last
+ * failure. No passage of the pages: library housekeeping. */
 const char* detint_strerror(int code);
 const char* detint_last_error(void);
 

@@ -1,12 +1,28 @@
 """GPU parity at the configured workload sizes (the pages' demo: 64-token
 prompt, 512 greedy steps, per-step logits chain hash; DetLLM README "Demo"):
-the CUDA path against the CPU oracle where the oracle finishes in seconds,
-and the invariances that hold at any size (batch composition, split
-prefill) where it does not."""
+the CUDA path against the CPU oracle, run live where it finishes in seconds
+and through fixtures the oracle wrote (tests/golden/make_golden.py --full)
+where it needs minutes, plus the invariances that hold at any size (batch
+composition, split prefill)."""
+import json
+import os
+
 import numpy as np
 import pytest
 
 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _sha(path):
+    with open(path + ".sha256") as f:
+        return f.read().strip()
 
 pytestmark = pytest.mark.gpu
 
@@ -69,20 +85,24 @@ def test_config3_batch8_row0_equals_batch1_512_steps(torch_cuda, qwen_artifact):
 
 def test_config4_split_prefill_equals_single_pass(torch_cuda, qwen_artifact):
     """2048-token prompt: 1024 prefilled at once and the rest fed one token at
-    a time, then 512 decode steps, equals the single 2048-token prefill."""
+    a time, then 512 decode steps, equals the single 2048-token prefill, and
+    both equal the oracle's tokens and logits chain hash (fixture)."""
+    import hashlib
     import deterministic_integer_only_gb300 as pkg
     torch = torch_cuda
     dev = torch.device("cuda")
-    prompt = synth.prompt_ids(0, 7, 2048, QWEN_V)
-    steps = 512
+    g = _golden("oracle_qwen06b_split2048.json")
+    assert g["artifact_sha256"] == _sha(qwen_artifact)
+    prompt = synth.prompt_ids(g["prompt_seed"], g["index"], g["prompt_len"], QWEN_V)
+    steps = g["steps"]
     m = pkg.Model(qwen_artifact, max_batch=2, max_ctx=2048 + steps)
     lg = torch.empty((1, QWEN_V), dtype=torch.int32, device=dev)
     tok = torch.empty(1, dtype=torch.int32, device=dev)
 
     def run(split):
-        import hashlib
         h = b"\0" * 32
         out = []
+        first = None
         with torch.cuda.stream(m.stream):
             if split:
                 m.prefill([0], torch.tensor(prompt[:1024], device=dev), [0, 1024], lg, tok)
@@ -94,13 +114,42 @@ def test_config4_split_prefill_equals_single_pass(torch_cuda, qwen_artifact):
                 if step:
                     m.decode_step([0], tok, lg, tok)
                 out.append(int(tok.item()))
-                h = hashlib.sha256(h + lg.cpu().numpy().astype("<i4").tobytes()).digest()
-        return out, h
+                row = lg.cpu().numpy().astype("<i4").tobytes()
+                if first is None:
+                    first = hashlib.sha256(b"\0" * 32 + row).hexdigest()[:12]
+                h = hashlib.sha256(h + row).digest()
+        return out, h.hex()[:12], first
 
     a = run(False)
     m.reset_seq(0)
     b = run(True)
     assert a == b
+    assert a[0] == g["tokens"]
+    assert a[1] == g["logits_hash12"]
+    assert a[2] == g["prefill_logits_hash12"]
+    assert not m.status().any()
+    m.close()
+
+
+def test_prefill_4096_matches_oracle(torch_cuda, qwen_artifact):
+    """One 4096-token prefill (the zero-tolerance suite's 4k context: DetLLM
+    blog footnote): the last position's logits hash and token equal the
+    oracle's token-by-token run (fixture)."""
+    import deterministic_integer_only_gb300 as pkg
+    torch = torch_cuda
+    dev = torch.device("cuda")
+    g = _golden("oracle_qwen06b_prefill4096.json")
+    assert g["artifact_sha256"] == _sha(qwen_artifact)
+    prompt = synth.prompt_ids(g["prompt_seed"], g["index"], g["prompt_len"], QWEN_V)
+    m = pkg.Model(qwen_artifact, max_batch=1, max_ctx=4096)
+    lg = torch.empty((1, QWEN_V), dtype=torch.int32, device=dev)
+    tok = torch.empty(1, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(m.stream):
+        m.prefill([0], torch.tensor(prompt, device=dev), [0, 4096], lg, tok)
+    m.stream.synchronize()
+    assert int(tok.item()) == g["tokens"][0]
+    assert pkg.chain_hash([lg.cpu().numpy()[0]]).hex()[:12] == g["prefill_logits_hash12"]
+    assert not m.status().any()
     m.close()
 
 
@@ -127,13 +176,18 @@ def test_llama_shape_matches_oracle(torch_cuda, llama_artifact):
 
 def test_config5_llama_batch32_rows_equal_batch1(torch_cuda, llama_artifact):
     """Llama-3.2-1B shape, batch 32 of 1024-token contexts: sampled rows of
-    the batch-32 decode equal batch-1 runs of the same prompts (tokens and
-    logits hash over 16 steps)."""
+    the batch-32 decode equal batch-1 runs of the same prompts and the
+    oracle's tokens and logits chain hash over 16 steps (fixture)."""
     import deterministic_integer_only_gb300 as pkg
+    g = _golden("oracle_llama1b_ctx1024.json")
     prompts = [synth.prompt_ids(9, i, 1024, LLAMA_V) for i in range(32)]
     m = pkg.Model(llama_artifact, max_batch=32, max_ctx=1024 + 32)
     t32, h32 = m.generate(prompts, 16, keep_logits="hash")
     for b in (0, 17):
+        ref = g["rows"][str(b)]
+        assert ref["artifact_sha256"] == _sha(llama_artifact)
+        assert t32[b].tolist() == ref["tokens"], b
+        assert h32[b].hex()[:12] == ref["logits_hash12"], b
         for sid in range(32):
             m.reset_seq(sid)
         t1, h1 = m.generate([prompts[b]], 16, keep_logits="hash")
