@@ -50,7 +50,8 @@ constexpr int MG_W = 8;                  // compute warps (+ producer warp 8 + s
 constexpr int MG_MAXS = 16;              // ring slots at most
 constexpr int MG_IPC = 4;                // attention items per attention CTA at most
 
-enum { MG_BAR_STAT = 1, MG_BAR_Q = 2, MG_BAR_TS = 3, MG_BAR_ATT = 4, MG_BAR_END = 5, MG_BAR_STAT2 = 6 };
+enum { MG_BAR_STAT = 1, MG_BAR_Q = 2, MG_BAR_TS = 3, MG_BAR_ATT = 4, MG_BAR_END = 5, MG_BAR_STAT2 = 6,
+       MG_BAR_INIT = 8 };
 enum { MG_K_QKV = 0, MG_K_O = 1, MG_K_GU = 2, MG_K_D = 3, MG_K_LM = 4 };
 
 // ---- tagged words
@@ -83,6 +84,7 @@ struct MgShared {
     int pos[8];
     unsigned base;
     int abort;
+    int rw[5][2];                 // this GEMV CTA's weight rows per GEMV kind
 };
 
 // ---- bounded waits: poll until `ok`, else record the timeout and abort the step
@@ -357,10 +359,10 @@ __device__ __forceinline__ void mg_epilogue(const StepArgs& a, MgShared& sh, con
                                             int& besti) {
     const i64 mt = sh.mt[t];
     const int shf = sh.kt[t] + 22 - P.fout;
-    const i64 mca = (n - P.r0 < STEP_MCS) ? mcs[n - P.r0] : P.mc[n];
+    const i64 mca = mcs[n - P.r0];
     const i64 y = rshr((i64)sa * (mt * mca), shf);
     if (P.kind == MG_K_GU) {
-        const i64 mcb = (n + 1 - P.r0 < STEP_MCS) ? mcs[n + 1 - P.r0] : P.mc[n + 1];
+        const i64 mcb = mcs[n + 1 - P.r0];
         const i64 yu = rshr((i64)sb * (mt * mcb), shf);
         if (y > (1 << 24) || y < -(1 << 24) || yu > (1 << 24) || yu < -(1 << 24)) a.status[ST_SAT_GU] = 1;
         ll_put(P.dst + (size_t)t * P.ldo + (n >> 1), swiglu_dev((int)sat_b(y, 1 << 24), (int)sat_b(yu, 1 << 24)),
@@ -546,12 +548,21 @@ __device__ void mg_poll_head(const StepArgs& a, MgShared& sh, const u64* p, unsi
     }
 }
 
+// offsets of the parameter rows in an item's staging region (after K and V)
+template <int D>
+struct MgAux {
+    static constexpr int KVP = 0, QG = (8 + D / 2) * 4, KG = QG + 2 * D, CS = KG + 2 * D, SN = CS + D, BT = SN + D;
+};
+
 // one attention item (token t, kv head g) of layer l on warps 0..8 of an
-// attention CTA; the sequence's earlier K/V blocks are in Ks / Vs when staged
+// attention CTA; the sequence's earlier K/V blocks are in Ks / Vs when
+// staged, the item's parameter rows in aux (both completing on kvb)
 template <int EPL, int G>
 __device__ void mg_attention(const StepArgs& a, MgShared& sh, const StepLayer& Lw, int l, int t, int g,
-                             int8_t* Ks, int8_t* Vs, bool staged, uint32_t kvb, unsigned char* scr) {
+                             int8_t* Ks, int8_t* Vs, const unsigned char* aux, bool staged, uint32_t kvb,
+                             unsigned char* scr) {
     constexpr int D = EPL * 32, NC = D >> 4, DH2 = D / 2;
+    using X = MgAux<D>;
     __shared__ int32_t mqs[G], kqs[G];
     __shared__ unsigned long long amq[G];
     __shared__ int red_i[8][G];
@@ -569,14 +580,15 @@ __device__ void mg_attention(const StepArgs& a, MgShared& sh, const StepLayer& L
     const int pos = sh.pos[t];
     const int ctx = pos + 1, ctx16 = (ctx + 15) & ~15;
     const int nb = (ctx + KV_BLK - 1) >> 6;
-    const int32_t* kvp = Lw.kvp + (size_t)g * (8 + DH2);
-    const int* bt = a.block_table + (size_t)a.tok_seq[t] * a.mbs;
+    const int32_t* kvp = (const int32_t*)(aux + X::KVP);
+    const int* bt = (const int*)(aux + X::BT);
     const u64* row = a.xqkv + (size_t)t * nqkv;
 
     // ---- q heads (warps 0..G-1) and the new key / value (warp G)
     if (w <= G) {
-        const int16_t* cr = a.rope_cos + (size_t)pos * DH2;
-        const int16_t* sr = a.rope_sin + (size_t)pos * DH2;
+        const int16_t* cr = (const int16_t*)(aux + X::CS);
+        const int16_t* sr = (const int16_t*)(aux + X::SN);
+        if (!mbar_wait(kvb, l & 1)) a.status[ST_TIMEOUT] = 1;    // parameter rows (and K/V) staged
         int E = 0;
         for (int i = lane; i < DH2; i += 32) E = max(E, kvp[8 + i]);
         E = __reduce_max_sync(0xffffffffu, (unsigned)E);
@@ -584,7 +596,7 @@ __device__ void mg_attention(const StepArgs& a, MgShared& sh, const StepLayer& L
         if (w < G) {
             const int hq = (g << a.lg_grp) + w;
             mg_poll_head<EPL>(a, sh, row + (size_t)hq * D, tag, y);
-            if (a.qk_norm) mg_qk_norm<EPL>(y, Lw.q_gamma, lane, a.eps_qk);
+            if (a.qk_norm) mg_qk_norm<EPL>(y, (const int16_t*)(aux + X::QG), lane, a.eps_qk);
             else {
 #pragma unroll
                 for (int j = 0; j < EPL; ++j) y[j] *= 4;
@@ -610,7 +622,7 @@ __device__ void mg_attention(const StepArgs& a, MgShared& sh, const StepLayer& L
         } else {
             i64 v[EPL];
             mg_poll_head<EPL>(a, sh, row + (size_t)(a.nq + g) * D, tag, y, row + (size_t)(a.nq + a.nkv + g) * D, v);
-            if (a.qk_norm) mg_qk_norm<EPL>(y, Lw.k_gamma, lane, a.eps_qk);
+            if (a.qk_norm) mg_qk_norm<EPL>(y, (const int16_t*)(aux + X::KG), lane, a.eps_qk);
             else {
 #pragma unroll
                 for (int j = 0; j < EPL; ++j) y[j] *= 4;
@@ -622,8 +634,6 @@ __device__ void mg_attention(const StepArgs& a, MgShared& sh, const StepLayer& L
             int8_t* vd = Lw.vc + ((size_t)blk * a.nkv + g) * D * KV_BLK + off;
             const i64 KQM = kvp[0], VQM = kvp[2];
             const int KQS = kvp[1], VQS = kvp[3];
-            // the staged block must have landed before its new row is written
-            if (staged && !mbar_wait(kvb, l & 1)) a.status[ST_TIMEOUT] = 1;
             int8_t* ks = Ks + (size_t)pos * D;
             int8_t* vs = Vs + (size_t)(nb - 1) * KV_BLK * D + off;
 #pragma unroll
@@ -641,7 +651,7 @@ __device__ void mg_attention(const StepArgs& a, MgShared& sh, const StepLayer& L
             }
         }
     }
-    if (staged && w > G && lane == 0 && !mbar_wait(kvb, l & 1)) a.status[ST_TIMEOUT] = 1;
+    if (w > G && lane == 0 && !mbar_wait(kvb, l & 1)) a.status[ST_TIMEOUT] = 1;
     bar_named(MG_BAR_ATT, 288);
 
     const i64 CSTM = kvp[6], MV = kvp[4];
@@ -785,18 +795,31 @@ __device__ void mg_attention(const StepArgs& a, MgShared& sh, const StepLayer& L
     bar_named(MG_BAR_ATT, 288);
 }
 
-// the K/V blocks of positions before this step's of item (t, g), layer l,
-// into Ks / Vs (thread 0; completion on kvb)
+// item (t, g) of layer l, by thread 0: its parameter rows into aux (the
+// block-table row by plain loads, the rest by 1D bulk copies) and, when
+// staged, the K/V blocks of every position before this step's into Ks / Vs;
+// the copies complete on kvb (one phase per layer)
 template <int D>
 __device__ void mg_stage(const StepArgs& a, MgShared& sh, const StepLayer& Lw, int t, int g, int8_t* Ks,
-                         int8_t* Vs, uint32_t kvb) {
+                         int8_t* Vs, unsigned char* aux, bool staged, uint32_t kvb) {
+    using X = MgAux<D>;
+    constexpr int DH2 = D / 2;
+    constexpr uint32_t BLK = (uint32_t)KV_BLK * D;
+    constexpr uint32_t PAR = (uint32_t)X::BT;            // parameter bytes copied in bulk
     const int pos = sh.pos[t];
     const int nb = (pos + 1 + KV_BLK - 1) >> 6;
-    constexpr uint32_t BLK = (uint32_t)KV_BLK * D;
     const int* bt = a.block_table + (size_t)a.tok_seq[t] * a.mbs;
-    mbar_arrive_expect_tx(kvb, (uint32_t)nb * 2u * BLK);
+    int* bts = (int*)(aux + X::BT);
+    for (int b = 0; b < nb; ++b) bts[b] = bt[b];
+    mbar_arrive_expect_tx(kvb, PAR + (staged ? (uint32_t)nb * 2u * BLK : 0u));
+    bulk_g2s(smem_u32(aux + X::KVP), Lw.kvp + (size_t)g * (8 + DH2), (8 + DH2) * 4, kvb);
+    bulk_g2s(smem_u32(aux + X::QG), Lw.q_gamma, 2 * D, kvb);
+    bulk_g2s(smem_u32(aux + X::KG), Lw.k_gamma, 2 * D, kvb);
+    bulk_g2s(smem_u32(aux + X::CS), a.rope_cos + (size_t)pos * DH2, 2 * DH2, kvb);
+    bulk_g2s(smem_u32(aux + X::SN), a.rope_sin + (size_t)pos * DH2, 2 * DH2, kvb);
+    if (!staged) return;
     for (int b = 0; b < nb; ++b) {
-        const size_t unit = (size_t)bt[b] * a.nkv + g;
+        const size_t unit = (size_t)bts[b] * a.nkv + g;
         bulk_g2s(smem_u32(Ks + (size_t)b * BLK), Lw.kc + unit * BLK, BLK, kvb);
         bulk_g2s(smem_u32(Vs + (size_t)b * BLK), Lw.vc + unit * BLK, BLK, kvb);
     }
@@ -839,32 +862,21 @@ __global__ void __launch_bounds__(STEP_THREADS, 1) k_decode_step(StepArgs a) {
         const int ai = c - a.NG;
         const int items = a.T << a.lg_nkv;
         int8_t* att = (int8_t*)smem;
-        unsigned char* scr = (unsigned char*)(att + (size_t)a.ipc * 2 * a.cap * D);
-        // staging of layer 0
-        if (tid == 0) {
-            for (int j = 0; j < a.ipc; ++j) {
-                const int it = ai + j * a.NA;
-                if (it >= items) break;
-                const int t = it >> a.lg_nkv, g = it & ((1 << a.lg_nkv) - 1);
-                if (sh.pos[t] + 1 <= a.cap) {
-                    int8_t* Ks = att + (size_t)j * 2 * a.cap * D;
-                    mg_stage<D>(a, sh, a.layers[0], t, g, Ks, Ks + (size_t)a.cap * D, smem_u32(&sh.kvbar[j]));
-                }
-            }
-        }
-        for (int l = 0; l < a.L; ++l) {
-            const StepLayer& Lw = a.layers[l];
+        const size_t ist = 2 * (size_t)a.cap * D + step_aux_bytes(D, a.mbs);   // item region stride
+        unsigned char* scr = (unsigned char*)(att + (size_t)a.ipc * ist);
+        for (int l = -1; l < a.L; ++l) {
             for (int j = 0; j < a.ipc; ++j) {
                 const int it = ai + j * a.NA;
                 if (it >= items) break;
                 const int t = it >> a.lg_nkv, g = it & ((1 << a.lg_nkv) - 1);
                 const bool staged = sh.pos[t] + 1 <= a.cap;
-                int8_t* Ks = att + (size_t)j * 2 * a.cap * D;
+                int8_t* Ks = att + (size_t)j * ist;
                 int8_t* Vs = Ks + (size_t)a.cap * D;
+                unsigned char* aux = (unsigned char*)(Vs + (size_t)a.cap * D);
                 const uint32_t kvb = smem_u32(&sh.kvbar[j]);
-                mg_attention<EPL, G>(a, sh, Lw, l, t, g, Ks, Vs, staged, kvb, scr);
-                // this item's blocks of the next layer (the region is free again)
-                if (tid == 0 && staged && l + 1 < a.L) mg_stage<D>(a, sh, a.layers[l + 1], t, g, Ks, Vs, kvb);
+                if (l >= 0) mg_attention<EPL, G>(a, sh, a.layers[l], l, t, g, Ks, Vs, aux, staged, kvb, scr);
+                // this item's next layer (the region is free again)
+                if (tid == 0 && l + 1 < a.L) mg_stage<D>(a, sh, a.layers[l + 1], t, g, Ks, Vs, aux, staged, kvb);
             }
         }
         return;
@@ -881,11 +893,33 @@ __global__ void __launch_bounds__(STEP_THREADS, 1) k_decode_step(StepArgs a) {
     const int XP = Kmax + 16;
     int8_t* x8 = (int8_t*)(smem + a.off_x8);
     int32_t* xin = (int32_t*)(smem + a.off_xin);
-    int16_t* gs = (int16_t*)(smem + a.off_gs);
+    int16_t* gs = (int16_t*)(smem + a.off_gs);           // [H]
     int32_t* hown = (int32_t*)(smem + a.off_hown);
-    int32_t* mcs = (int32_t*)(smem + a.off_mcs);
+    StepLayer* lay = (StepLayer*)(smem + a.off_lay);
+    int32_t* mct = (int32_t*)(smem + a.off_mct);
+    // ---- everything small the phases read, staged once per step (a global
+    // read of a small parameter under the weight stream can cost a microsecond
+    // or two on the critical path): this CTA's row bounds per GEMV kind, the
+    // layer table, and by asynchronous copies every phase's channel scales of
+    // this CTA's rows
+    if (tid < 10) sh.rw[tid >> 1][tid & 1] = a.rows[(tid >> 1) * (a.NG + 1) + c + (tid & 1)];
+    if (warp < 8)                                         // threads 0..255 (warp 8 has left)
+        for (int i = tid; i < a.L * (int)(sizeof(StepLayer) / 8); i += 256)
+            ((u64*)lay)[i] = ((const u64*)a.layers)[i];
+    bar_named(MG_BAR_INIT, 288);
+    if (warp < 8) {
+        for (int l = 0; l < a.L; ++l)
+            for (int k = 0, off = l * a.ms; k < 4; ++k) {
+                const int32_t* m = k == 0 ? lay[l].m_qkv : k == 1 ? lay[l].m_o : k == 2 ? lay[l].m_gu : lay[l].m_d;
+                const int r0 = sh.rw[k][0], n = sh.rw[k][1] - r0;
+                for (int i = tid; i < n; i += 256) cp_async4(mct + off + i, m + r0 + i);
+                off += n;
+            }
+        const int r0 = sh.rw[MG_K_LM][0], n = sh.rw[MG_K_LM][1] - r0;
+        for (int i = tid; i < n; i += 256) cp_async4(mct + a.L * a.ms + i, a.embed_m + r0 + i);
+    }
     // the residual rows this CTA updates (o_proj and down share the rows), from the embedding
-    const int h0 = a.rows[MG_K_O * (a.NG + 1) + c], h1 = a.rows[MG_K_O * (a.NG + 1) + c + 1];
+    const int h0 = sh.rw[MG_K_O][0], h1 = sh.rw[MG_K_O][1];
     if (warp < 8) {
         for (int e = tid; e < a.T * STEP_HOWN; e += 256) {
             const int t = e / STEP_HOWN, n = h0 + (e - t * STEP_HOWN);
@@ -895,11 +929,13 @@ __global__ void __launch_bounds__(STEP_THREADS, 1) k_decode_step(StepArgs a) {
             }
         }
     }
-    int u = 0, ph = 0;
+    int u = 0;
+    bool first = true;
     int bestv = -2147483647 - 1, besti = 2147483647;
     for (int l = 0; l <= a.L; ++l) {
-        const StepLayer& Lw = a.layers[l < a.L ? l : 0];
+        const StepLayer& Lw = lay[l < a.L ? l : 0];
         const int nph = l < a.L ? 4 : 1;
+        int moff = l * a.ms;                              // this layer's channel scales in mct
         for (int p = 0; p < nph; ++p) {
             MgPhase P{};
             P.kind = l < a.L ? p : MG_K_LM;
@@ -930,19 +966,19 @@ __global__ void __launch_bounds__(STEP_THREADS, 1) k_decode_step(StepArgs a) {
                     P.fout = 16;
                     break;
             }
-            P.r0 = a.rows[P.kind * (a.NG + 1) + c];
-            P.r1 = a.rows[P.kind * (a.NG + 1) + c + 1];
+            P.r0 = sh.rw[P.kind][0];
+            P.r1 = sh.rw[P.kind][1];
             if (warp == 9) {
                 mg_scales(a, sh, P);
                 continue;
             }
-            // this phase's channel scales into shared memory, read by the
-            // epilogues after the statistics barrier; two buffers, since a warp
-            // may fill this phase's while another still reads the previous one's
-            int32_t* mc2 = mcs + (ph++ & 1) * STEP_MCS;
-            for (int i = tid; i < P.r1 - P.r0 && i < STEP_MCS; i += 256) mc2[i] = P.mc[P.r0 + i];
+            const int32_t* mcs = mct + (P.kind == MG_K_LM ? a.L * a.ms : moff);
+            moff += P.r1 - P.r0;
+            // the scale table has landed (each thread its own copies; the
+            // prologue's statistics barrier then publishes them to all)
+            if (first) { cp_async_wait_all(); first = false; }
             mg_prologue(a, sh, P, x8, XP, xin, gs);
-            mg_consume(a, sh, P, ring, x8, XP, hown, mc2, u, bestv, besti);
+            mg_consume(a, sh, P, ring, x8, XP, hown, mcs, u, bestv, besti);
         }
     }
     if (warp == 9) return;

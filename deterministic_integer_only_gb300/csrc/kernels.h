@@ -176,13 +176,15 @@ struct StepArgs {
     int spin;                    // polls before a wait gives up
     int stall;                   // > 0: the final wait expects a tag nobody writes, bounded by stall polls
     // dynamic shared memory of a GEMV CTA: weight ring, int8 tile [T][XP],
-    // int32 input rows [T][XP], gamma [H], owned residual rows, channel scales
-    int off_x8, off_xin, off_gs, off_hown, off_mcs;
+    // int32 input rows [T][XP], gamma [H], owned residual
+    // rows, the layer table [L], the CTA's channel scales of every phase
+    // (ms per layer for the four layer phases, then the lm_head rows)
+    int off_x8, off_xin, off_gs, off_hown, off_lay, off_mct;
+    int ms;
 };
 constexpr int STEP_THREADS = 320;
 constexpr int STEP_SLOT = 16384;        // weight ring slot bytes
 constexpr int STEP_HOWN = 64;           // residual rows a GEMV CTA owns at most
-constexpr int STEP_MCS = 1024;          // channel scales a GEMV CTA stages per phase
 constexpr int STEP_NP = 64;             // tagged pairs per thread a prologue can track
 // weight rows per ring slot for reduction length K (<= 16)
 __host__ __device__ inline int step_rows_per_slot(int K) {
@@ -190,10 +192,17 @@ __host__ __device__ inline int step_rows_per_slot(int K) {
     while (q * K > STEP_SLOT) --q;
     return q;
 }
-// attention CTA shared memory: per item K [cap][d] and V^T [cap/64][d][64];
-// then q [G][d], scores [G][scap] int32, E_lo/E_hi [G][scap], P.V limbs [G][d][2]
-__host__ __device__ inline size_t step_att_bytes(int G, int d, int cap, int ipc, int scap) {
-    return (size_t)ipc * 2 * cap * d + (size_t)G * d + (size_t)G * scap * 6 + (size_t)G * d * 8;
+// an attention item's parameter rows in shared memory: the kv head's
+// parameters [8 + d/2] int32, q and k gammas [d] int16, this position's RoPE
+// cos and sin rows [d/2] int16, the sequence's block-table row [mbs] int32
+__host__ __device__ inline int step_aux_bytes(int d, int mbs) {
+    return (8 + d / 2) * 4 + 4 * d + 2 * d + ((mbs * 4 + 15) & ~15);
+}
+// attention CTA shared memory: per item K [cap][d], V^T [cap/64][d][64] and
+// the parameter rows; then q [G][d], scores [G][scap] int32, E_lo/E_hi
+// [G][scap], P.V limbs [G][d][2]
+__host__ __device__ inline size_t step_att_bytes(int G, int d, int cap, int ipc, int scap, int aux) {
+    return (size_t)ipc * (2 * (size_t)cap * d + aux) + (size_t)G * d + (size_t)G * scap * 6 + (size_t)G * d * 8;
 }
 // d: head_dim, grp: q heads per kv head; false for shapes without an instantiation
 bool decode_step_supported(int d, int grp);

@@ -151,7 +151,7 @@ struct detint_model {
     int persistent = 0;      // 1: decode steps of up to 8 sequences as one launch where supported
     // the one-launch decode step (k_decode_step.cuh): per batch size T = 1..8,
     // its CTA roles and attention staging; its tagged exchange rows and tags
-    struct StepCfg { int ok, NG, NA, ipc, cap, lg_ns, off[5]; } st_cfg[8] = {};
+    struct StepCfg { int ok, NG, NA, ipc, cap, lg_ns, ms, off[6]; } st_cfg[8] = {};
     StepLayer* st_layers = nullptr;
     unsigned long long* st_x = nullptr;
     unsigned* st_ctl = nullptr;
@@ -500,15 +500,33 @@ static int setup_step(detint_model* m) {
             if (k < 4 && Ns[k] / unit[k] < NG) fit = false;       // every GEMV CTA owns rows of every layer phase
             if ((Ks[k] / 2 + gn - 1) / gn > STEP_NP) fit = false;  // prologue pairs per thread
         }
-        const size_t fixed = (size_t)G * d + (size_t)G * m->st_scap * 6 + (size_t)G * d * 8;
+        // the row ranges first: the GEMV layout holds every phase's scales of a CTA's rows
+        int32_t* rt = rows.data() + (size_t)(T - 1) * 5 * (nsm + 1);
+        for (int k = 0; k < 5; ++k)
+            for (int i = 0; i <= NG; ++i)
+                rt[k * (NG + 1) + i] = (int32_t)(unit[k] * (((long long)i * (Ns[k] / unit[k])) / NG));
+        int ms = 0, nlm = 0;
+        for (int i = 0; i < NG; ++i) {
+            int sum = 0;
+            for (int k = 0; k < 4; ++k) sum += rt[k * (NG + 1) + i + 1] - rt[k * (NG + 1) + i];
+            ms = std::max(ms, sum);
+            nlm = std::max(nlm, rt[4 * (NG + 1) + i + 1] - rt[4 * (NG + 1) + i]);
+        }
+        // attention CTA layout: per item K, V and parameter rows, then the score rows
+        const int aux = step_aux_bytes(d, m->mbs);
+        const size_t fixed = (size_t)G * d + (size_t)G * m->st_scap * 6 + (size_t)G * d * 8 + (size_t)ipc * aux;
         if (!fit || fixed > dyn) continue;
         int cap = (int)((dyn - fixed) / ((size_t)ipc * 2 * d)) & ~(KV_BLK - 1);
         cap = std::min(cap, (m->st_scap + KV_BLK - 1) & ~(KV_BLK - 1));
         // GEMV CTA layout: ring of 8 (else 4) slots, the int8 tile and the
-        // int32 input rows of T tokens, gamma, owned residual rows, scales
+        // int32 input rows of T tokens, gamma, owned residual rows,
+        // the layer table, the channel-scale table
         const int Kmax = std::max(H, std::max(nqd, F)), XP = Kmax + 16;
-        const size_t x8b = (size_t)T * XP, xinb = (size_t)T * XP * 4, gsb = ((size_t)H * 2 + 15) & ~(size_t)15;
-        const size_t rest = x8b + xinb + gsb + (size_t)8 * STEP_HOWN * 4 + (size_t)2 * STEP_MCS * 4;
+        auto a16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
+        const size_t x8b = a16((size_t)T * XP), xinb = (size_t)T * XP * 4, gsb = a16((size_t)H * 2),
+                     hownb = (size_t)8 * STEP_HOWN * 4, layb = a16(sizeof(StepLayer) * m->L),
+                     mctb = a16((size_t)4 * ((size_t)m->L * ms + nlm));
+        const size_t rest = x8b + xinb + gsb + hownb + layb + mctb;
         int lg_ns = 3;
         while (lg_ns > 2 && ((size_t)STEP_SLOT << lg_ns) + rest > dyn) --lg_ns;
         if (((size_t)STEP_SLOT << lg_ns) + rest > dyn) continue;
@@ -517,12 +535,10 @@ static int setup_step(detint_model* m) {
         c.off[1] = (int)(c.off[0] + x8b);
         c.off[2] = (int)(c.off[1] + xinb);
         c.off[3] = (int)(c.off[2] + gsb);
-        c.off[4] = (int)(c.off[3] + (size_t)8 * STEP_HOWN * 4);
+        c.off[4] = (int)(c.off[3] + hownb);
+        c.off[5] = (int)(c.off[4] + layb);
+        c.ms = ms;
         c.NG = NG; c.NA = NA; c.ipc = ipc; c.cap = std::max(cap, 0);
-        int32_t* rt = rows.data() + (size_t)(T - 1) * 5 * (nsm + 1);
-        for (int k = 0; k < 5; ++k)
-            for (int i = 0; i <= NG; ++i)
-                rt[k * (NG + 1) + i] = (int32_t)(unit[k] * (((long long)i * (Ns[k] / unit[k])) / NG));
         c.ok = 1;
         any = true;
     }
@@ -572,7 +588,8 @@ static int run_decode_step(detint_model* m, int T, const int32_t* tokens, int32_
     a.NG = c.NG; a.NA = c.NA; a.ipc = c.ipc; a.lg_ns = c.lg_ns; a.cap = c.cap; a.scap = m->st_scap;
     a.spin = 1 << 20;
     a.stall = m->st_stall;
-    a.off_x8 = c.off[0]; a.off_xin = c.off[1]; a.off_gs = c.off[2]; a.off_hown = c.off[3]; a.off_mcs = c.off[4];
+    a.off_x8 = c.off[0]; a.off_xin = c.off[1]; a.off_gs = c.off[2]; a.off_hown = c.off[3];
+    a.off_lay = c.off[4]; a.off_mct = c.off[5]; a.ms = c.ms;
     CK(launch_decode_step(a, c.NG + c.NA, m->st_smem, s));
     return DETINT_OK;
 }
