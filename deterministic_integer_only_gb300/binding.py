@@ -101,7 +101,12 @@ def detint_gemm_i8(A, B, C_out, stream=None):
 def detint_argmax_noalloc(logits, out, stream=None):
     """out[r] = tie-low argmax of logits[r] (int32 cuda tensors), computed
     without any device allocation (partials in a fixed device array)."""
+    import torch
     rows, n = logits.shape
+    if logits.dtype != torch.int32 or out.dtype != torch.int32 or not logits.is_cuda or not out.is_cuda:
+        raise ValueError("detint_argmax_noalloc: int32 cuda tensors expected")
+    if not logits.is_contiguous() or not out.is_contiguous() or out.numel() < rows:
+        raise ValueError("detint_argmax_noalloc: contiguous logits [rows, n] and out [rows] expected")
     _check(lib().detint_argmax_noalloc(_ptr(logits), rows, n, _ptr(out), _stream(stream)),
            "detint_argmax_noalloc")
     return out
@@ -204,6 +209,11 @@ class Model:
 
     def set_persistent(self, enable: bool):
         _check(lib().detint_set_option(self._h, 4, int(bool(enable))), "detint_set_option")
+
+    def set_wait_test(self, polls: int):
+        """While polls > 0, the one-launch decode step's final wait expects a
+        tag no CTA writes and gives up after `polls` polls (status slot 6)."""
+        _check(lib().detint_set_option(self._h, 5, int(polls)), "detint_set_option")
 
     def set_tc_prefill(self, enable: bool):
         _check(lib().detint_set_option(self._h, 2, int(bool(enable))), "detint_set_option")

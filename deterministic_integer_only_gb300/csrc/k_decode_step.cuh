@@ -410,24 +410,22 @@ __device__ void mg_consume(const StepArgs& a, MgShared& sh, const MgPhase& P, co
     const int R = step_rows_per_slot(K);
     const int nch = K >> 4;                        // 16-byte chunks per row
     const bool swi = P.kind == MG_K_GU;
-    const bool half = R >= 16;
-    const int li = half ? (lane & 15) : lane;      // lane within the row's group
-    const int lstep = half ? 16 : 32;
+    const bool hrow = R >= 16;                     // a half-warp per row
+    const int li = hrow ? (lane & 15) : lane;      // lane within the row's group
+    const int lstep = hrow ? 16 : 32;
     // the two rows of this lane in a slot
     int r0, r1;
-    if (half) {
+    if (hrow) {
         const int hw = 2 * wg + (lane >> 4);
-        if (swi) { r0 = 4 * wg + 2 * 0 + (lane >> 4); r1 = r0 + 2; }   // pairs 2wg, 2wg+1: gate in half 0, up in half 1
+        if (swi) { r0 = 4 * wg + (lane >> 4); r1 = r0 + 2; }   // pairs 2wg, 2wg+1: gate in half 0, up in half 1
         else { r0 = hw; r1 = hw + 8; }
     } else {
         if (swi) { r0 = 2 * wg; r1 = 2 * wg + 1; }
         else { r0 = wg; r1 = wg + 4; }
     }
     bool scales = false;
-    const int nslots = (P.r1 - P.r0 + R - 1) / R;
-    for (int k = 0; k < nslots; ++k, ++u) {
+    for (int k = 0, rb = P.r0; rb < P.r1; ++k, rb += R, ++u) {
         if ((u & 1) != grp) continue;              // the other group's slot
-        const int rb = P.r0 + k * R;
         const int s = u & (NS - 1);
         const int nr = min(R, P.r1 - rb);
         const bool h0 = r0 < nr, h1 = r1 < nr;
@@ -442,7 +440,7 @@ __device__ void mg_consume(const StepArgs& a, MgShared& sh, const MgPhase& P, co
             const int8_t* xt = x8 + (size_t)t * XP;
             int a0 = h0 ? mg_dot_part(slot + (size_t)r0 * K, xt, li, lstep, nch) : 0;
             int a1 = h1 ? mg_dot_part(slot + (size_t)r1 * K, xt, li, lstep, nch) : 0;
-            if (half) {
+            if (hrow) {
 #pragma unroll
                 for (int o = 8; o; o >>= 1) {
                     a0 += __shfl_xor_sync(0xffffffffu, a0, o);
@@ -455,7 +453,7 @@ __device__ void mg_consume(const StepArgs& a, MgShared& sh, const MgPhase& P, co
             if (li == t) { s0 = a0; s1 = a1; }
         }
         int u0 = 0, u1 = 0;                        // gate/up in halves: the up rows' sums
-        if (half && swi) {
+        if (hrow && swi) {
             u0 = __shfl_down_sync(0xffffffffu, s0, 16);
             u1 = __shfl_down_sync(0xffffffffu, s1, 16);
         }
@@ -468,7 +466,7 @@ __device__ void mg_consume(const StepArgs& a, MgShared& sh, const MgPhase& P, co
         if (!scales) { bar_named(MG_BAR_TS, 288); scales = true; }
         if (li >= T) continue;
         if (swi) {
-            if (half) {
+            if (hrow) {
                 if (lane >= 16) continue;
                 if (h0) mg_epilogue(a, sh, P, li, rb + r0, s0, u0, hown, mcs, bestv, besti);
                 if (h1) mg_epilogue(a, sh, P, li, rb + r1, s1, u1, hown, mcs, bestv, besti);

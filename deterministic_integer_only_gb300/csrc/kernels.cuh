@@ -523,14 +523,16 @@ __device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs
     }
 }
 
-// prefill: queries already quantised by k_qkv_post
+// per-token prefill attention (the option that turns the tensor-core prefill
+// attention off): queries already quantised by k_qkv_post
 __global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ int32_t mqs[MAXG], kqs[MAXG];
     const int t = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
     const int G = 1 << a.lg_grp, d = a.d;
     int8_t* qs = (int8_t*)sm;
-    for (int i = tid; i < G * d; i += 256) qs[i] = a.q8[((size_t)t * a.nq + (g << a.lg_grp)) * d + i];
+    const int4* qsrc = (const int4*)(a.q8 + ((size_t)t * a.nq + (g << a.lg_grp)) * d);
+    for (int i = tid; i < (G * d) >> 4; i += 256) ((int4*)qs)[i] = qsrc[i];
     if (tid < G) {
         mqs[tid] = a.mq[(size_t)t * a.nq + (g << a.lg_grp) + tid];
         kqs[tid] = a.kq[(size_t)t * a.nq + (g << a.lg_grp) + tid];

@@ -385,12 +385,13 @@ static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode
         aa.block_table = m->block_table; aa.mbs = m->mbs; aa.tok_seq = m->tok_seq;
         aa.tok_pos = m->tok_pos; aa.kvp = w.kvp; aa.o = m->o; aa.T = T; aa.nq = nq; aa.nkv = nkv;
         aa.d = d; aa.lg_grp = m->lg_grp; aa.ctx_cap = m->ctx_cap;
-        if (decode && m->dec_staged == 1) {
-            // one token per sequence: QKV post-processing fused into the
-            // staged decode attention, as in the fused step
-            aa.ctx_cap = m->dec_cap;
+        if (decode) {
+            // one token per sequence: QKV post-processing fused into the decode
+            // attention, the sequence's K/V staged in shared memory while every
+            // context fits, else read from the cache
+            aa.ctx_cap = m->dec_staged == 1 ? m->dec_cap : m->ctx_cap;
             aa.seq_len = m->seq_len_dev; aa.status = m->status;
-            CK(launch_attn_decode(aa, qa, s, true));
+            CK(launch_attn_decode(aa, qa, s, m->dec_staged == 1));
         } else if (!decode && m->pf_ok && m->tc_prefill) {
             CK(launch_qkv_post(qa, s));
             PfArgs pa{};

@@ -81,6 +81,13 @@ int main(int argc, char** argv) {
         std::vector<i64> out(acc.size());
         for (size_t i = 0; i < acc.size(); ++i) out[i] = rshr_mul128(acc[i], M[i], sh[i]);
         save(dir, "mul128_out", out);
+        // the same routine on planted ties and shifts up to 100
+        auto acc2 = load<i64>(dir, "mul128x_acc");
+        auto M2 = load<u64>(dir, "mul128x_m");
+        auto sh2 = load<int32_t>(dir, "mul128x_s");
+        std::vector<i64> out2(acc2.size());
+        for (size_t i = 0; i < acc2.size(); ++i) out2[i] = rshr_mul128(acc2[i], M2[i], sh2[i]);
+        save(dir, "mul128x_out", out2);
     }
     printf("ok\n");
     return 0;

@@ -223,3 +223,38 @@ def test_persistent_decode_equals_kernel_chain(torch_cuda, request, name, B):
         m.close()
     assert np.array_equal(out[True][0], out[False][0])
     assert out[True][1] == out[False][1]
+
+
+@pytest.mark.parametrize("graph", [True, False])
+def test_decode_step_wait_timeout_is_reported_and_recovers(torch_cuda, tiny_artifact, graph):
+    """Failure path of the bounded waits: with the wait test on, the one-launch
+    step's final wait expects a tag that no CTA writes, gives up after a few
+    thousand polls and records status slot 6 instead of hanging. The step's
+    logits (written before that wait) still equal the oracle's, and once the
+    test is off the sequence continues exactly as the oracle does."""
+    torch = torch_cuda
+    dev = torch.device("cuda")
+    prompt = synth.prompt_ids(4, 0, 16, 1024)
+    ot, orows = _oracle_run(tiny_artifact, prompt, 8, 64)
+    m = _load(tiny_artifact, 2, 64)
+    m.set_graph(graph)
+    m.set_persistent(True)
+    lg = torch.empty((1, 1024), dtype=torch.int32, device=dev)
+    tok = torch.empty(1, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(m.stream):
+        m.prefill([0], torch.tensor(prompt, dtype=torch.int32, device=dev), [0, len(prompt)], lg, tok)
+    assert not m.status().any()
+    for step in range(1, 8):
+        stall = step == 3
+        m.set_wait_test(2000 if stall else 0)
+        fed = torch.tensor([int(ot[step - 1])], dtype=torch.int32, device=dev)
+        with torch.cuda.stream(m.stream):
+            m.decode_step([0], fed, lg, tok)
+        st = m.status()
+        assert np.array_equal(lg.cpu().numpy()[0], orows[step]), step
+        if stall:
+            assert st[6] == 1 and st[:6].sum() == 0
+        else:
+            assert not st.any(), step
+            assert int(tok.item()) == int(ot[step]), step
+    m.close()

@@ -3,7 +3,9 @@ actually compare": mixed requests, chunked prefill, shared prefixes and
 preemption leave the outputs unchanged): sequences forked from a shared
 prefix (KV blocks shared by reference count), a batch of forks decoding
 together, preemption with recomputation, and block-pool exhaustion and
-reuse. Every comparison is bit-exact."""
+reuse. Every comparison is bit-exact, and every forked, batched or
+recomputed row is also compared with the CPU oracle fed the same token
+list (its prefill logits, greedy tokens and logits chain hash)."""
 import numpy as np
 import pytest
 
@@ -34,6 +36,22 @@ def _prefill(torch, m, sids, chunks):
         m.prefill(sids, flat, cu, lg, tok)
     m.stream.synchronize()
     return lg.cpu().numpy(), tok
+
+
+def _oracle(path, tokens, steps):
+    """The oracle's last-position logits for the token list, then `steps`
+    greedy tokens and the chain hash of their logits, as _decode reports."""
+    import hashlib
+    import oracle
+    oracle.set_threads(oracle.max_threads())
+    s = oracle.Model(path).new_seq(len(tokens) + steps + 1)
+    am, lg0 = s.feed(np.asarray(tokens, np.int32))
+    toks, h = [], b"\0" * 32
+    for _ in range(steps):
+        am, lg = s.feed([am])
+        toks.append(am)
+        h = hashlib.sha256(h + lg.astype("<i4").tobytes()).digest()
+    return lg0, np.array(toks, np.int32), h
 
 
 def _decode(torch, m, sids, tok, steps):
@@ -79,6 +97,11 @@ def test_fork_equals_fresh_prefill(torch_cuda, request, name, n_shared):
     toks_r2, h_r2 = _decode(torch, m, [3], tok_r2, 6)
     assert np.array_equal(lg_s, lg_r2) and np.array_equal(toks_s, toks_r2) and h_s == h_r2
     m.close()
+    # both rows against the oracle
+    o_lg, o_t, o_h = _oracle(path, np.concatenate([base[:n_shared], tail]), 10)
+    assert np.array_equal(lg_f[0], o_lg) and np.array_equal(toks_f[:, 0], o_t) and h_f[0] == o_h
+    o_lg, o_t, o_h = _oracle(path, np.concatenate([base, tail[:5]]), 6)
+    assert np.array_equal(lg_s[0], o_lg) and np.array_equal(toks_s[:, 0], o_t) and h_s[0] == o_h
 
 
 def test_batch_of_forks_decodes_like_solo_runs(torch_cuda, qwen_artifact):
@@ -103,6 +126,9 @@ def test_batch_of_forks_decodes_like_solo_runs(torch_cuda, qwen_artifact):
         toks_1, h_1 = _decode(torch, m, [i], t1, 12)
         assert np.array_equal(toks_1[:, 0], toks_b[:, i]) and h_1[0] == h_b[i], i
     m.close()
+    for i, c in enumerate(cuts):
+        _, o_t, o_h = _oracle(qwen_artifact, np.concatenate([base[:c], tails[i]]), 12)
+        assert np.array_equal(toks_b[:, i], o_t) and h_b[i] == o_h, i
 
 
 def test_preempt_and_recompute(torch_cuda, tiny_artifact):
@@ -129,6 +155,10 @@ def test_preempt_and_recompute(torch_cuda, tiny_artifact):
     assert np.array_equal(np.concatenate([first[:, 1], rest1[:, 0]]), full[:, 1])
     assert np.array_equal(np.concatenate([first[:, 0], part0[:, 0]]), full[:17, 0])
     m.close()
+    # the uninterrupted runs (which the preempted and recomputed ones equal) against the oracle
+    for b in range(2):
+        _, o_t, _ = _oracle(tiny_artifact, prompts[b], 30)
+        assert np.array_equal(full[:, b], o_t), b
 
 
 def test_fork_arguments_and_block_reuse(torch_cuda, tiny_artifact):

@@ -75,6 +75,25 @@ def host_run(tmp_path_factory):
     inputs["mul128_m"] = (mt.astype(np.int64) * mc.astype(np.int64)).astype(np.uint64)
     inputs["mul128_s"] = (kt + 30 - 16).astype(np.int32)
     inputs["_mt"], inputs["_mc"], inputs["_kt"] = mt, mc, kt
+    # planted exact ties of both signs (acc * M an odd multiple of 2^(s-1))
+    # and shifts 60..100 whose results fit int64
+    xa, xm, xs = [], [], []
+    for i in range(4000):
+        s_ = int(rng.integers(2, 64))
+        j = int(rng.integers(0, min(31, s_ - 1) + 1))       # M = 2^j
+        k = 2 * int(rng.integers(0, 1 << 12)) + 1            # odd
+        a_ = k << (s_ - 1 - j)
+        if abs(a_) >= 1 << 36:
+            continue
+        xa.append(a_ if i % 2 else -a_); xm.append(1 << j); xs.append(s_)
+    for i in range(4000):
+        s_ = int(rng.integers(60, 101))
+        a_ = int(rng.integers(-(1 << 35), 1 << 35))
+        m_ = int(rng.integers(1, 1 << 31))
+        xa.append(a_); xm.append(m_); xs.append(s_)
+    inputs["mul128x_acc"] = np.array(xa, np.int64)
+    inputs["mul128x_m"] = np.array(xm, np.uint64)
+    inputs["mul128x_s"] = np.array(xs, np.int32)
     for k, v in inputs.items():
         if not k.startswith("_"):
             v.tofile(str(d / f"{k}.bin"))
@@ -118,3 +137,13 @@ def test_requant_mul128(host_run):
     inp, out = host_run
     want = oracle.requant_wide(inp["mul128_acc"], inp["_mt"], inp["_kt"], inp["_mc"], 16)
     np.testing.assert_array_equal(out("mul128_out", np.int64), want)
+
+
+def test_mul128_ties_and_wide_shifts(host_run):
+    """rshr_mul128 against the exact definition (Python integers): planted
+    ties of both signs round toward +infinity, and shifts of 60..100."""
+    inp, out = host_run
+    got = out("mul128x_out", np.int64)
+    for a_, m_, s_, g_ in zip(inp["mul128x_acc"].tolist(), inp["mul128x_m"].tolist(),
+                              inp["mul128x_s"].tolist(), got.tolist()):
+        assert g_ == (a_ * m_ + (1 << (s_ - 1))) >> s_, (a_, m_, s_)

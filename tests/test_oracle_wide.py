@@ -133,6 +133,7 @@ def test_wide_golden_regression(wide_artifact):
     assert oracle.chain_hash(rows).hex()[:12] == g["logits_hash12"]
 
 
+@pytest.mark.slow
 def test_wide_no_bound_violation_qwen_shape():
     # every asserted bound of the 16-bit weight path (accumulator < 2^36,
     # shift range, 128-bit product, saturations) on the Qwen3-0.6B shape

@@ -63,3 +63,42 @@ def test_noalloc_argmax_rejects_oversize(torch_cuda):
     with pytest.raises(pkg.DetintError) as e:
         pkg.detint_argmax_noalloc(x, out)
     assert e.value.code == 2
+
+
+def test_noalloc_argmax_across_chunks(torch_cuda):
+    """Rows spanning many 4096-column chunks (151936 columns: 38 chunks, the
+    last one partial) and the largest accepted shapes: equal maxima in
+    different chunks go to the lower column, a row of INT32_MIN gives column
+    0, and every row equals numpy's first maximum, on two calls in a row."""
+    import deterministic_integer_only_gb300 as pkg
+    torch = torch_cuda
+    rng = np.random.default_rng(77)
+    imin, imax = np.iinfo(np.int32).min, np.iinfo(np.int32).max
+    n = 151936
+    x = rng.integers(imin, imax, (64, n), dtype=np.int64).astype(np.int32)
+    x[0, 5 * 4096 + 17] = x[0, 20 * 4096 + 3] = imax            # tie in two chunks
+    x[1, 30 * 4096 + 4000] = x[1, 30 * 4096 + 100] = imax        # tie inside one chunk
+    x[1, 31 * 4096 + 1] = imax                                   # a later chunk ties too
+    x[2, :] = imin                                               # all INT32_MIN
+    x[3, n - 1] = imax                                           # the partial last chunk
+    x[4, 0] = imax
+    x[4, n - 1] = imax
+    for call in range(2):
+        xs = x if call == 0 else x[::-1].copy()
+        t = torch.tensor(xs, device="cuda")
+        out = torch.full((64,), -1, dtype=torch.int32, device="cuda")
+        pkg.detint_argmax_noalloc(t, out)
+        torch.cuda.synchronize()
+        assert out.cpu().tolist() == [int(np.argmax(r)) for r in xs], call
+    # the largest accepted sizes
+    big = torch.tensor(rng.integers(-1000, 1000, (2, 1 << 20), dtype=np.int64).astype(np.int32), device="cuda")
+    out = torch.empty(2, dtype=torch.int32, device="cuda")
+    pkg.detint_argmax_noalloc(big, out)
+    torch.cuda.synchronize()
+    assert out.cpu().tolist() == [int(np.argmax(r)) for r in big.cpu().numpy()]
+    full = torch.zeros((64, 64), dtype=torch.int32, device="cuda")
+    full[:, 63] = 1
+    out = torch.empty(64, dtype=torch.int32, device="cuda")
+    pkg.detint_argmax_noalloc(full, out)
+    torch.cuda.synchronize()
+    assert out.cpu().tolist() == [63] * 64
