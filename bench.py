@@ -179,15 +179,36 @@ def cpu_baseline(seconds: float = 12.0):
                                       f"(~{seconds / 3:.0f} s)"}}
 
 
-# int8 tensor-pipe peak of this GPU: mma.sync m16n8k32 s8, measured with a
-# register-only loop of independent MMAs on a GB300 (a dp4a loop gives 153)
-MMA_S8_PEAK_TOPS = 150.3
-# DRAM traffic of one lm_head GEMV launch at M=1, read + write, from the last
-# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum. The kernel's
-# quantisation prologue changed after that capture (one-pass NormQuant, the
-# multiplier by Newton-Raphson), so the line reports traffic as null and
-# keeps this figure only as the last capture's value.
-LMHEAD_DRAM_BYTES_LAST_CAPTURE = 155664896 + 2895104
+# DRAM bytes (read + write) of one lm_head GEMV launch at M=1, from an ncu
+# capture of dram__bytes_read.sum + dram__bytes_write.sum on the current kernel
+LMHEAD_DRAM_BYTES = None
+
+
+def int8_peak(pkg, dev, iters=4096, reps=5):
+    """Integer-pipe peak of this GPU in TOPS, measured now: the library's loop
+    of independent mma.sync m16n8k32 s8 operations (kind 0) and of dp4a
+    (kind 1) on register operands, 4 CTAs of 256 threads per SM, best of
+    `reps` CUDA-event timings. The tcgen05 tensor cores have no integer kind
+    on sm_103a, so this is the rate an int8 GEMM can reach here."""
+    import torch
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks = 4 * nsm
+    sink = torch.empty(blocks * 256, dtype=torch.int32, device=dev)
+    out = {}
+    for kind, name in ((0, "mma_s8"), (1, "dp4a")):
+        best = None
+        for r in range(reps + 1):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ops = pkg.detint_int8_peak_loop(kind, blocks, iters, sink)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            if r and (best is None or ms < best):
+                best = ms
+        out[name] = ops / (best / 1e3) / 1e12
+    return out
 
 
 def run_gemm_w16(args):
@@ -209,7 +230,8 @@ def run_gemm_w16(args):
             res.append({"M": M, "N": N, "K": K, "us": ms * 1e3, "tops": 2.0 * M * N * K / (ms / 1e3) / 1e12})
             del a, w, hi, lo, c
     print(json.dumps({"metric": "exact int8 x int16 GEMM sweep (two int8 weight limbs, Llama-3.2-1B shapes)",
-                      "unit": "TOPS", "mma_s8_peak_tops": MMA_S8_PEAK_TOPS, "sweep": res}), flush=True)
+                      "unit": "TOPS", "mma_s8_peak_tops": int8_peak(pkg, torch.device("cuda"))["mma_s8"],
+                      "sweep": res}), flush=True)
 
 
 def run_sample(args):
@@ -289,15 +311,13 @@ def run_llama_b32(args):
     model.close()
 
 
-def run_prefill(args):
-    """Prefill throughput: 4 sequences x 4096 seeded tokens on the Qwen3-0.6B
-    shape in one detint_prefill call (last-position logits per sequence)."""
+def prefill_rate(pkg, B, L, steps, warmup, peak_tops):
+    """Prefill of B sequences x L seeded tokens (Qwen3-0.6B shape) in one
+    detint_prefill call: median ms, tok/s, GEMM TOPS and its fraction of the
+    measured int8 peak (the GEMMs' 2MNK; the attention's causal QK^T and two
+    E.V limbs are counted separately)."""
     import torch
     import synth
-    from deterministic_integer_only_gb300 import build
-    build.build()
-    import deterministic_integer_only_gb300 as pkg
-    B, L = args.prefill_seqs, args.prefill_len
     path = synth.ensure_artifact(SHAPE, SEED)
     model = pkg.Model(path, max_batch=B, max_ctx=L)
     dev = torch.device("cuda")
@@ -307,7 +327,7 @@ def run_prefill(args):
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     s = model.stream
     times = []
-    for it in range(args.warmup + args.steps):
+    for it in range(warmup + steps):
         for sid in range(B):
             model.reset_seq(sid)
         e0 = torch.cuda.Event(enable_timing=True)
@@ -317,18 +337,33 @@ def run_prefill(args):
             model.prefill(list(range(B)), flat, cu, None, tok)
             e1.record(s)
         s.synchronize()
-        if it >= args.warmup:
+        if it >= warmup:
             times.append(e0.elapsed_time(e1))
     ms = float(np.median(times))
     H, F, nq, nkv, d, Lyr = model.hidden, model.ffn, model.n_q, model.n_kv, model.head_dim, model.n_layers
     gemm_ops = 2.0 * B * L * Lyr * ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F)
     attn_ops = 2.0 * B * Lyr * nq * d * (L * (L + 1) / 2) * 3    # QK^T + two E.V limbs, causal
-    line = {"metric": f"prefill tok/s (Qwen3-0.6B shape, {B} x {L})", "value": B * L / (ms / 1e3),
-            "unit": "tok/s", "ms": ms, "steps": args.steps, "warmup": args.warmup,
-            "gemm_tops": gemm_ops / (ms / 1e3) / 1e12, "attn_ops_T": attn_ops / 1e12,
-            "gemm_ops_T": gemm_ops / 1e12, "dtype": "int8/int32", "data": "synthetic"}
-    print(json.dumps(line), flush=True)
     model.close()
+    return {"metric": f"prefill tok/s (Qwen3-0.6B shape, {B} x {L})", "value": B * L / (ms / 1e3),
+            "unit": "tok/s", "ms": ms, "steps": steps, "warmup": warmup,
+            "gemm_ops_T": gemm_ops / 1e12, "attn_ops_T": attn_ops / 1e12,
+            "ops_tops_overall": (gemm_ops + attn_ops) / (ms / 1e3) / 1e12,
+            "int8_peak_tops": peak_tops,
+            "overall_frac": (gemm_ops + attn_ops) / (ms / 1e3) / 1e12 / peak_tops,
+            "note": "overall: GEMM plus attention integer operations over the whole prefill time"}
+
+
+def run_prefill(args):
+    """Prefill throughput: 4 sequences x 4096 seeded tokens on the Qwen3-0.6B
+    shape in one detint_prefill call (last-position logits per sequence)."""
+    import torch
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+    pk = int8_peak(pkg, torch.device("cuda"))["mma_s8"]
+    line = prefill_rate(pkg, args.prefill_seqs, args.prefill_len, args.steps, args.warmup, pk)
+    line.update({"dtype": "int8/int32", "data": "synthetic"})
+    print(json.dumps(line), flush=True)
 
 
 def _graph_time(fn, stream, n):
@@ -373,6 +408,86 @@ def run_lmhead(args):
     print(json.dumps({"workload": "lmhead", "launches": args.warmup + args.steps}), flush=True)
 
 
+def run_int8_peak(args):
+    """The integer-pipe peak loops (mma.sync m16n8k32 s8 and dp4a) and, as a
+    library reference, torch._int_mm (cuBLASLt) on 8192^3."""
+    import torch
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+    dev = torch.device("cuda")
+    pk = int8_peak(pkg, dev)
+    lib_tops = None
+    try:
+        a = torch.randint(-127, 128, (8192, 8192), dtype=torch.int8, device=dev)
+        b = torch.randint(-127, 128, (8192, 8192), dtype=torch.int8, device=dev)
+        for _ in range(2):
+            torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(5):
+            torch._int_mm(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        lib_tops = 2 * 8192 ** 3 * 5 / (e0.elapsed_time(e1) / 1e3) / 1e12
+    except (RuntimeError, AttributeError) as e:
+        lib_tops = f"unavailable: {type(e).__name__}"
+    print(json.dumps({"metric": "int8 integer-pipe peak", "unit": "TOPS", "mma_s8": pk["mma_s8"],
+                      "dp4a": pk["dp4a"], "torch_int_mm_8192": lib_tops,
+                      "loop": "4 CTAs x 256 threads per SM, 8 independent operations per warp "
+                              "(mma) or thread (dp4a) per round, 4096 rounds, best of 5"}), flush=True)
+
+
+def run_oracle_configs(args):
+    """The CPU oracle timed on the other configured workloads, on bounded
+    samples (one core and all cores): config 3 (batch 8: row 0 and two
+    co-prompt rows, each row independent by construction), config 4 (the
+    2048-token prompt fed token by token; a split prefill is the same work
+    for the oracle) and config 5 (two of the 32 Llama-shaped sequences at
+    1024-token contexts)."""
+    import oracle
+    import synth
+    cores = oracle.max_threads()
+    res = []
+
+    def timed(shape, prompt, steps, label, threads, budget):
+        oracle.set_threads(threads)
+        m = oracle.Model(synth.ensure_artifact(shape, SEED))
+        s = m.new_seq(len(prompt) + steps + 1)
+        t0 = time.perf_counter()
+        tok, _ = s.feed(prompt)
+        fed = len(prompt)
+        n = 0
+        while n < steps and time.perf_counter() - t0 < budget:
+            tok, _ = s.feed([tok])
+            n += 1
+        dt = time.perf_counter() - t0
+        res.append({"sample": label, "threads": threads, "prompt_tokens": fed, "decode_steps": n,
+                    "seconds": dt, "tok_per_s": (fed + n) / dt})
+
+    q = synth.prompt_ids(SEED, 0, PROMPT_LEN, 151936)
+    lens = synth.coprompt_lengths(SEED, 7)
+    p4 = synth.prompt_ids(SEED, 7, 2048, 151936)
+    for threads, budget, cut in ((cores, 8.0, None), (1, 2.0, 64)):
+        # one core: the prompts cut to `cut` tokens so the run stays within minutes
+        def c(p):
+            return p if cut is None else p[:cut]
+        timed(SHAPE, q, 64, f"config 3 row 0 ({len(c(q))}-token prompt)", threads, budget)
+        for i in (0, 3):
+            pi = c(synth.prompt_ids(SEED, 100 + i, int(lens[i]), 151936))
+            timed(SHAPE, pi, 64, f"config 3 row {i + 1} ({len(pi)} tokens of its co-prompt)", threads, budget)
+        timed(SHAPE, c(p4), 8, f"config 4 ({len(c(p4))} tokens of the 2048-token prompt, token by token)",
+              threads, budget)
+        for b in (0, 17):
+            pb = c(synth.prompt_ids(9, b, 1024, 128256))
+            timed("llama-1b", pb, 8, f"config 5 sequence {b} ({len(pb)}-token context)", threads, budget)
+    oracle.set_threads(cores)
+    print(json.dumps({"metric": "CPU oracle on configs 3-5 (bounded samples)", "unit": "tok/s",
+                      "cores": cores, "samples": res}), flush=True)
+
+
 def run_gemm_sweep(args):
     """Exact int8 GEMM (detint_gemm_i8) over M x (N, K) of the Llama-3.2-1B
     projections: TOPS = 2MNK/t and bytes = MK + NK + 4MN per launch."""
@@ -382,6 +497,7 @@ def run_gemm_sweep(args):
     import deterministic_integer_only_gb300 as pkg
     peak_gbs, _ = _peaks()
     dev = torch.device("cuda")
+    pk = int8_peak(pkg, dev)["mma_s8"]
     s = torch.cuda.Stream()
     rows = []
     for (N, K) in [(2048, 2048), (512, 2048), (3072, 2048), (16384, 2048), (2048, 8192), (128256, 2048)]:
@@ -394,11 +510,12 @@ def run_gemm_sweep(args):
             ops = 2.0 * M * N * K
             byt = M * K + N * K + 4 * M * N
             rows.append({"M": M, "N": N, "K": K, "us": t * 1e6, "tops": ops / t / 1e12,
+                         "int8_frac": ops / t / 1e12 / pk,
                          "gbs": byt / t / 1e9, "hbm_frac": byt / t / 1e9 / peak_gbs})
             del A, C
         del W
     print(json.dumps({"metric": "int8 GEMM sweep (Llama-3.2-1B shapes)", "unit": "TOPS",
-                      "mma_s8_peak_tops": MMA_S8_PEAK_TOPS, "hbm_peak_gbs": peak_gbs,
+                      "mma_s8_peak_tops": pk, "hbm_peak_gbs": peak_gbs,
                       "sweep": rows}), flush=True)
 
 
@@ -457,7 +574,8 @@ def main():
     ap.add_argument("--prefill-seqs", type=int, default=4, help="prefill workload: sequences")
     ap.add_argument("--prefill-len", type=int, default=4096, help="prefill workload: tokens each")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "gemm", "lmhead", "llama-b32", "sample", "gemm-w16"],
+                    choices=["decode", "prefill", "gemm", "lmhead", "llama-b32", "sample", "gemm-w16",
+                             "int8-peak", "oracle-configs"],
                     help="decode (the headline line), prefill (4 x 4096 prompt throughput) or "
                          "gemm (exact int8 GEMM sweep over the Llama-3.2-1B projection shapes)")
     args = ap.parse_args()
@@ -475,6 +593,10 @@ def main():
         return run_gemm_sweep(args)
     if args.workload == "lmhead":
         return run_lmhead(args)
+    if args.workload == "int8-peak":
+        return run_int8_peak(args)
+    if args.workload == "oracle-configs":
+        return run_oracle_configs(args)
 
     import torch
     import synth
@@ -580,12 +702,9 @@ def main():
     achieved = kbytes / (kms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": "k_sgemv (decode streaming GEMV), lm_head shape 151936x1024, M=%d" % B,
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_kind": peak_kind, "traffic": None,
-                "traffic_last_capture": LMHEAD_DRAM_BYTES_LAST_CAPTURE if B == 1 else None,
-                "traffic_source": "null: the kernel's prologue changed since the ncu capture of "
-                                  "dram__bytes_read.sum + dram__bytes_write.sum at M=1 "
-                                  "(profiles/k_sgemv_lmhead_151936x1024.md); its value is "
-                                  "traffic_last_capture",
+                "peak_kind": peak_kind, "traffic": LMHEAD_DRAM_BYTES if B == 1 else None,
+                "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of one launch "
+                                  "from an ncu capture of this kernel at M=1 (LMHEAD_DRAM_BYTES)",
                 "bytes_per_launch": kbytes,
                 "us_per_launch": kms * 1e3, "us_per_launch_l2_warm": kms_warm * 1e3,
                 "timing": "CUDA events around graph replays; L2 evicted before every launch"}
@@ -604,6 +723,10 @@ def main():
     other = None
     if args.companion and B != 8:
         other = _decode_rate(pkg, path, 8, K, W, dev, dist, ws)
+    # companions for the metric's other parts: the measured int8 pipe peak and
+    # the prefill of 4 x 4096 tokens against it
+    pk = int8_peak(pkg, dev)
+    pre = prefill_rate(pkg, 4, 4096, 3, 1, pk["mma_s8"]) if args.companion else None
 
     if rank == 0:
         cb = None
@@ -626,6 +749,9 @@ def main():
         if other is not None:
             line["batch8"] = {"value": other[0], "unit": "tok/s", "ms_per_step": other[1],
                               "config": "same workload, B=8 (7 seeded co-prompts of 16-256 tokens)"}
+        line["int8_peak_tops"] = pk
+        if pre is not None:
+            line["prefill"] = pre
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

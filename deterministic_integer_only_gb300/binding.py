@@ -26,7 +26,7 @@ ERRORS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "token id o
 SYMBOLS = ["detint_load", "detint_prefill", "detint_decode_step", "detint_gemm_i8",
            "detint_reset_seq", "detint_seq_len", "detint_status", "detint_set_graph",
            "detint_set_option", "detint_argmax_noalloc", "detint_sample", "detint_fork_seq", "detint_gemm_w16", "detint_split_w16",
-           "detint_model_info", "detint_free", "detint_strerror", "detint_last_error"]
+           "detint_int8_peak_loop", "detint_model_info", "detint_free", "detint_strerror", "detint_last_error"]
 
 
 class DetintError(RuntimeError):
@@ -59,6 +59,7 @@ def lib():
         L.detint_gemm_w16.argtypes = [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, vp]
         L.detint_split_w16.argtypes = [vp, vp, vp, C.c_longlong, vp]
         L.detint_sample.argtypes = [vp, C.c_int, C.c_int, C.POINTER(SamplingParams), vp, vp]
+        L.detint_int8_peak_loop.argtypes = [C.c_int, C.c_int, C.c_int, vp, C.POINTER(C.c_longlong), vp]
         L.detint_model_info.argtypes = [vp, i32p]
         L.detint_free.argtypes = [vp]
         L.detint_free.restype = None
@@ -159,6 +160,15 @@ def detint_gemm_w16(A, w_hi, w_lo, C=None, stream=None):
     _check(lib().detint_gemm_w16(_ptr(A), _ptr(w_hi), _ptr(w_lo), _ptr(C), M, N, K, _stream(stream)),
            "detint_gemm_w16")
     return C
+
+
+def detint_int8_peak_loop(kind: int, blocks: int, iters: int, sink, stream=None) -> int:
+    """Launch the integer-pipe peak loop (kind 0 mma.sync s8, 1 dp4a); returns
+    the integer operations it performs."""
+    ops = C.c_longlong(0)
+    _check(lib().detint_int8_peak_loop(int(kind), int(blocks), int(iters), _ptr(sink), C.byref(ops),
+                                       _stream(stream)), "detint_int8_peak_loop")
+    return int(ops.value)
 
 
 def chain_hash(rows, prev: bytes | None = None) -> bytes:

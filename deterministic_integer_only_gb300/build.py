@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libdetint.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["launch.cu", "runtime.cu", "noalloc.cu", "sample.cu"]
+SOURCES = ["launch.cu", "runtime.cu", "noalloc.cu", "sample.cu", "peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "--expt-relaxed-constexpr"]

@@ -146,4 +146,55 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         }
 }
 
+// Exact-mode epilogues on the limb GEMM's int64 accumulators (16-bit
+// weights, channel scale m_c / 2^30): y = rshr(acc * (m_t * m_c), k_t + 30 -
+// F_out), the product formed exactly in 128 bits, then the int8 path's
+// consumers: q/k/v saturation, saturating residual add, SwiGLU of an
+// interleaved (gate, up) pair, or int32 logits with per-16-column argmax
+// partials (lowest column on ties). One thread per output (per gate/up pair,
+// per 16 logits).
+__device__ __forceinline__ i64 w16_requant(const int64_t* C, const Epi& ep, int N, int m, int n) {
+    const u64 M = (u64)((i64)ep.mt[m] * (i64)ep.mc[n]);
+    return rshr_mul128((i64)C[(size_t)m * N + n], M, ep.kt[m] + 30 - ep.fout);
+}
+
+// grid: (column blocks of 256, M rows); columns are outputs, gate/up pairs
+// or 16-column logit groups
+__global__ void __launch_bounds__(256) k_epi_w16(const int64_t* __restrict__ C, int N, int mode, Epi ep) {
+    const int m = blockIdx.y;
+    const int j = blockIdx.x * 256 + threadIdx.x;
+    if (mode == EPI_SWIGLU) {
+        if (j >= (N >> 1)) return;                 // channel j: rows 2j (gate), 2j + 1 (up)
+        i64 yg = w16_requant(C, ep, N, m, 2 * j), yu = w16_requant(C, ep, N, m, 2 * j + 1);
+        if (yg > (1 << 24) || yg < -(1 << 24) || yu > (1 << 24) || yu < -(1 << 24)) ep.status[ST_SAT_GU] = 1;
+        ep.out[(size_t)m * ep.ldo + j] = swiglu_dev((int)sat_b(yg, 1 << 24), (int)sat_b(yu, 1 << 24));
+        return;
+    }
+    if (mode == EPI_LOGITS) {
+        if (j >= ((N + 15) >> 4)) return;          // logit group j: columns 16j .. 16j + 15
+        int bv = -2147483647 - 1, bi = 2147483647;
+        for (int n = j * 16; n < min(N, j * 16 + 16); ++n) {
+            const i64 y = w16_requant(C, ep, N, m, n);
+            if (y > 2147483647LL || y < -2147483647LL) ep.status[ST_SAT_LOGIT] = 1;
+            const int v = sat32(y);
+            ep.out[(size_t)m * ep.ldo + n] = v;
+            if (v > bv) { bv = v; bi = n; }
+        }
+        ep.pval[(size_t)m * ep.npart + j] = bv;
+        ep.pidx[(size_t)m * ep.npart + j] = bi;
+        return;
+    }
+    if (j >= N) return;
+    const i64 y = w16_requant(C, ep, N, m, j);
+    if (mode == EPI_QKV) {
+        if (y > 2147483647LL || y < -2147483647LL) ep.status[ST_SAT_QKV] = 1;
+        ep.out[(size_t)m * ep.ldo + j] = sat32(y);
+    } else {
+        int32_t* hp = ep.out + (size_t)m * ep.ldo + j;
+        const i64 s2 = (i64)*hp + (i64)sat32(y);
+        if (s2 > 2147483647LL || s2 < -2147483647LL) ep.status[ST_SAT_RES] = 1;
+        *hp = sat32(s2);
+    }
+}
+
 }  // namespace detint

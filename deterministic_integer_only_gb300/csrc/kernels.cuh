@@ -67,13 +67,16 @@ __device__ __forceinline__ i64 norm24(i64 v, int sig) {
 }
 
 // --------------------------------------------------------------- embedding
-// a1: h0 = rshr(E8[id] * m_e[id], 22 - 16); decode mode also reads each
-// sequence's current length as the token position.
+// a1: h0 = rshr(E8[id] * m_e[id], 22 - 16); with 16-bit weights (the exact
+// mode, E16 = 256 E_hi + E_lo as two limbs) h0 = rshr(E16[id] * m_e[id],
+// 30 - 16). Decode mode also reads each sequence's current length as the
+// token position.
 __global__ void __launch_bounds__(256) k_embed(const int32_t* __restrict__ tokens,
                                                const int32_t* __restrict__ tok_seq,
                                                int32_t* __restrict__ tok_pos,
                                                const int32_t* __restrict__ seq_len, int decode,
                                                int max_pos, const int8_t* __restrict__ E,
+                                               const uint8_t* __restrict__ Elo,
                                                const int32_t* __restrict__ Em, int H, int V,
                                                int32_t* __restrict__ h, int32_t* status) {
     const int t = blockIdx.x;
@@ -90,7 +93,12 @@ __global__ void __launch_bounds__(256) k_embed(const int32_t* __restrict__ token
     const i64 m = Em[id];
     const int8_t* er = E + (size_t)id * H;
     int32_t* hr = h + (size_t)t * H;
-    for (int i = threadIdx.x; i < H; i += 256) hr[i] = (int32_t)rshr((i64)er[i] * m, 6);
+    if (Elo) {
+        const uint8_t* el = Elo + (size_t)id * H;
+        for (int i = threadIdx.x; i < H; i += 256) hr[i] = (int32_t)rshr(((i64)er[i] * 256 + el[i]) * m, 14);
+    } else {
+        for (int i = threadIdx.x; i < H; i += 256) hr[i] = (int32_t)rshr((i64)er[i] * m, 6);
+    }
 }
 
 // ---------------------------------------------------------------- NormQuant

@@ -50,8 +50,8 @@ cudaError_t launch_gemm(const int8_t* A, const int8_t* W, int M, int N, int K, i
 
 cudaError_t launch_embed(const int32_t* tokens, int T, const int32_t* tok_seq, int32_t* tok_pos,
                          const int32_t* seq_len, int decode, int max_pos, const int8_t* E,
-                         const int32_t* Em, int H, int V, int32_t* h, int32_t* status,
-                         cudaStream_t s);
+                         const uint8_t* Elo, const int32_t* Em, int H, int V, int32_t* h,
+                         int32_t* status, cudaStream_t s);
 
 cudaError_t launch_normquant(const int32_t* x, const int32_t* rows, int R, int n,
                              const int16_t* gamma, long long eps, int8_t* q, int32_t* mt,
@@ -219,6 +219,10 @@ cudaError_t launch_argmax_final(const int32_t* pval, const int32_t* pidx, int ro
 cudaError_t launch_gemm_w16(const int8_t* A, const int8_t* Wh, const uint8_t* Wl, int64_t* C, int M,
                             int N, int K, int32_t* status, cudaStream_t s);
 cudaError_t launch_split_w16(const int16_t* W, int8_t* hi, uint8_t* lo, long long n, cudaStream_t s);
+// exact-mode epilogue of a limb GEMM's int64 output C [M][N] (EPI_QKV,
+// EPI_RESADD, EPI_SWIGLU of interleaved gate/up rows, EPI_LOGITS with
+// argmax partials): the 128-bit requantisation with channel shift 30
+cudaError_t launch_epi_w16(const int64_t* C, int M, int N, int mode, const Epi& ep, cudaStream_t s);
 // a status word in device memory for the entry points that take no model
 int32_t* standalone_status();
 

@@ -69,9 +69,9 @@ cudaError_t launch_gemv(const int8_t* W, const int8_t* X, int M, int N, int K, i
 // ------------------------------------------------------------- launchers
 cudaError_t launch_embed(const int32_t* tokens, int T, const int32_t* tok_seq, int32_t* tok_pos,
                          const int32_t* seq_len, int decode, int max_pos, const int8_t* E,
-                         const int32_t* Em, int H, int V, int32_t* h, int32_t* status,
-                         cudaStream_t s) {
-    k_embed<<<T, 256, 0, s>>>(tokens, tok_seq, tok_pos, seq_len, decode, max_pos, E, Em, H, V, h,
+                         const uint8_t* Elo, const int32_t* Em, int H, int V, int32_t* h,
+                         int32_t* status, cudaStream_t s) {
+    k_embed<<<T, 256, 0, s>>>(tokens, tok_seq, tok_pos, seq_len, decode, max_pos, E, Elo, Em, H, V, h,
                               status);
     return cudaGetLastError();
 }
@@ -392,6 +392,13 @@ cudaError_t launch_split_w16(const int16_t* W, int8_t* hi, uint8_t* lo, long lon
     if (n < 1) return cudaErrorInvalidValue;
     const long long blocks = std::min<long long>((n + 255) / 256, (long long)std::max(g_num_sms, 1) * 16);
     k_split_w16<<<(unsigned)blocks, 256, 0, s>>>(W, hi, lo, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_epi_w16(const int64_t* C, int M, int N, int mode, const Epi& ep, cudaStream_t s) {
+    if (M < 1 || M > 65535 || N < 1) return cudaErrorInvalidValue;
+    const int cols = mode == EPI_SWIGLU ? (N >> 1) : mode == EPI_LOGITS ? ((N + 15) >> 4) : N;
+    k_epi_w16<<<dim3((cols + 255) / 256, M), 256, 0, s>>>(C, N, mode, ep);
     return cudaGetLastError();
 }
 

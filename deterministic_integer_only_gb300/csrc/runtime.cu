@@ -105,7 +105,8 @@ struct Sha256 {
 // ---------------------------------------------------------------- model
 struct LayerW {
     int16_t *attn_gamma, *ffn_gamma, *q_gamma, *k_gamma;
-    int8_t *w_qkv, *w_o, *w_gu, *w_d;
+    int8_t *w_qkv, *w_o, *w_gu, *w_d;          // int8 weights, or the high limbs of 16-bit ones
+    uint8_t *l_qkv, *l_o, *l_gu, *l_d;          // exact mode: the low limbs (else null)
     int32_t *m_qkv, *m_o, *m_gu, *m_d, *kvp;
 };
 
@@ -119,7 +120,9 @@ struct detint_model {
     long long eps_h, eps_qk;
     int max_batch, max_ctx, mbs, nblocks, ctx_cap;
     unsigned char* wblob = nullptr;
+    int wide = 0;            // exact mode: 16-bit weights as two limbs, channel shift 30
     int8_t* embed;
+    uint8_t* embed_lo = nullptr;
     int32_t* embed_m;
     int16_t *final_gamma, *rope_cos, *rope_sin;
     std::vector<LayerW> layers;
@@ -140,6 +143,7 @@ struct detint_model {
     int32_t *h, *qkv, *o, *sbuf, *mt, *kt, *mq, *kq, *tok_seq, *tok_pos, *rows;
     int8_t *x8, *q8;
     int32_t *pval, *pidx, *logits_int;
+    int64_t* c64 = nullptr;  // exact mode: the limb GEMM's int64 accumulators
     int npart;
     int32_t* status = nullptr;
     int use_graph = 1;
@@ -233,7 +237,9 @@ static int ensure_scratch(detint_model* m, int T) {
            o_x8 = take((size_t)Tn * wmax), o_q8 = take((size_t)Tn * m->nq * m->d),
            o_pv = take((size_t)rows_out * m->npart * 4), o_pi = take((size_t)rows_out * m->npart * 4),
            o_lg = take((size_t)rows_out * m->V * 4),
-           o_qb = take((size_t)(Tn + m->max_batch) * 16);
+           o_qb = take((size_t)(Tn + m->max_batch) * 16),
+           o_c64 = m->wide ? take(std::max((size_t)Tn * std::max(std::max(nqkv, m->H), 2 * m->F),
+                                           (size_t)rows_out * m->V) * 8) : 0;
     cudaError_t e = cudaMalloc(&m->scratch, off);
     if (e != cudaSuccess) { m->scratch = nullptr; m->Tcap = 0; return fail(DETINT_E_OOM, "scratch allocation failed"); }
     unsigned char* b = m->scratch;
@@ -244,6 +250,7 @@ static int ensure_scratch(detint_model* m, int T) {
     m->x8 = (int8_t*)(b + o_x8); m->q8 = (int8_t*)(b + o_q8);
     m->pval = (int32_t*)(b + o_pv); m->pidx = (int32_t*)(b + o_pi); m->logits_int = (int32_t*)(b + o_lg);
     m->qblk = (int32_t*)(b + o_qb);
+    m->c64 = m->wide ? (int64_t*)(b + o_c64) : nullptr;
     m->Tcap = Tn;
     return DETINT_OK;
 }
@@ -271,6 +278,14 @@ static cudaError_t gemm_epi(detint_model* m, const int8_t* X, const int8_t* W, i
     // short M: small grids split K through the model's workspace
     if (M <= 64) return launch_gemm(X, W, M, N, K, mode, ep, s, m->gws, m->gws_elems, m->gcnt, m->gcnt_n);
     return launch_gemm(X, W, M, N, K, mode, ep, s);
+}
+
+// exact mode: the limb GEMM (int64 accumulators) then the 128-bit epilogue
+static cudaError_t gemm_wide(detint_model* m, const int8_t* X, const int8_t* Whi, const uint8_t* Wlo, int M,
+                             int N, int K, int mode, const Epi& ep, cudaStream_t s) {
+    cudaError_t e = launch_gemm_w16(X, Whi, Wlo, m->c64, M, N, K, m->status, s);
+    if (e != cudaSuccess) return e;
+    return launch_epi_w16(m->c64, M, N, mode, ep, s);
 }
 
 // The forward pass of T tokens whose (sequence, position) are in tok_seq /
@@ -302,7 +317,7 @@ static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32
         return DETINT_OK;
     };
     CK(launch_embed(tokens, T, m->tok_seq, m->tok_pos, m->seq_len_dev, 1, m->max_ctx,
-                    m->embed, m->embed_m, H, m->V, m->h, m->status, s));
+                    m->embed, nullptr, m->embed_m, H, m->V, m->h, m->status, s));
     for (int l = 0; l < m->L; ++l) {
         const LayerW& w = m->layers[l];
         Epi e{};
@@ -343,7 +358,7 @@ static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32
 
 // every shape the fused decode path supports
 static bool decode_fusable(const detint_model* m, int T) {
-    if (T > 8 || m->fused_decode == 0) return false;
+    if (T > 8 || m->fused_decode == 0 || m->wide) return false;
     const int d = m->d, nq = m->nq, nkv = m->nkv;
     const int Ks[4] = {m->H, nq * d, m->H, m->F};
     for (int K : Ks) {
@@ -363,7 +378,13 @@ static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode
     const int nqkv = (nq + 2 * nkv) * d;
     if (decode && decode_fusable(m, T)) return run_decode_fused(m, T, tokens, logits, next_tok, s);
     CK(launch_embed(tokens, T, m->tok_seq, m->tok_pos, m->seq_len_dev, decode, m->max_ctx,
-                    m->embed, m->embed_m, H, m->V, m->h, m->status, s));
+                    m->embed, m->embed_lo, m->embed_m, H, m->V, m->h, m->status, s));
+    // the layer GEMMs: int8 weights (tiled GEMM / GEMV with fused epilogues) or
+    // 16-bit weights as limbs (exact mode)
+    auto gemm = [&](const int8_t* W, const uint8_t* Wl, int M, int N, int K, int mode, const Epi& e) {
+        return m->wide ? gemm_wide(m, m->x8, W, Wl, M, N, K, mode, e, s)
+                       : gemm_epi(m, m->x8, W, M, N, K, mode, e, s);
+    };
     for (int l = 0; l < m->L; ++l) {
         const LayerW& w = m->layers[l];
         int8_t* kc = m->kcache + (size_t)l * m->kv_layer_elems;
@@ -373,7 +394,7 @@ static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode
         e.status = m->status;
         e.mt = m->mt; e.kt = m->kt;
         e.out = m->qkv; e.ldo = nqkv; e.mc = w.m_qkv; e.fout = 12;
-        CK(gemm_epi(m, m->x8, w.w_qkv, T, nqkv, H, EPI_QKV, e, s));
+        CK(gemm(w.w_qkv, w.l_qkv, T, nqkv, H, EPI_QKV, e));
         QkvPostArgs qa{};
         qa.qkv = m->qkv; qa.q_gamma = w.q_gamma; qa.k_gamma = w.k_gamma; qa.qk_norm = m->qk_norm;
         qa.eps_qk = m->eps_qk; qa.rope_cos = m->rope_cos; qa.rope_sin = m->rope_sin; qa.kvp = w.kvp;
@@ -408,20 +429,20 @@ static int run_forward(detint_model* m, int T, const int32_t* tokens, int decode
         }
         CK(launch_actquant(m->o, T, nq * d, 12, m->x8, m->mt, m->kt, s));
         e.out = m->h; e.ldo = H; e.mc = w.m_o; e.fout = 16;
-        CK(gemm_epi(m, m->x8, w.w_o, T, H, nq * d, EPI_RESADD, e, s));
+        CK(gemm(w.w_o, w.l_o, T, H, nq * d, EPI_RESADD, e));
         CK(launch_normquant(m->h, nullptr, T, H, w.ffn_gamma, m->eps_h, m->x8, m->mt, m->kt, s));
         e.out = m->sbuf; e.ldo = F; e.mc = w.m_gu; e.fout = 12;
-        CK(gemm_epi(m, m->x8, w.w_gu, T, 2 * F, H, EPI_SWIGLU, e, s));
+        CK(gemm(w.w_gu, w.l_gu, T, 2 * F, H, EPI_SWIGLU, e));
         CK(launch_actquant(m->sbuf, T, F, 10, m->x8, m->mt, m->kt, s));
         e.out = m->h; e.ldo = H; e.mc = w.m_d; e.fout = 16;
-        CK(gemm_epi(m, m->x8, w.w_d, T, H, F, EPI_RESADD, e, s));
+        CK(gemm(w.w_d, w.l_d, T, H, F, EPI_RESADD, e));
     }
     CK(launch_normquant(m->h, rows, R, H, m->final_gamma, m->eps_h, m->x8, m->mt, m->kt, s));
     Epi e{};
     e.status = m->status; e.mt = m->mt; e.kt = m->kt;
     e.out = logits ? logits : m->logits_int; e.ldo = m->V; e.mc = m->embed_m; e.fout = 16;
     e.pval = m->pval; e.pidx = m->pidx; e.npart = m->npart;
-    CK(gemm_epi(m, m->x8, m->embed, R, m->V, H, EPI_LOGITS, e, s));
+    CK(gemm(m->embed, m->embed_lo, R, m->V, H, EPI_LOGITS, e));
     CK(launch_argmax_final(m->pval, m->pidx, R, m->npart, next_tok, m->tok_seq,
                            decode ? m->seq_len_dev : nullptr, s));
     return DETINT_OK;
@@ -471,7 +492,8 @@ static int sync_block_table(detint_model* m, cudaStream_t s) {
 static int setup_step(detint_model* m) {
     const int H = m->H, d = m->d, G = 1 << m->lg_grp, nqd = m->nq * d, F = m->F, nkv = m->nkv;
     const int nqkv = (m->nq + 2 * nkv) * d;
-    if ((H & (H - 1)) || (nkv & (nkv - 1)) || G > 7 || !decode_step_supported(d, G)) return DETINT_OK;
+    if (m->wide || (H & (H - 1)) || (nkv & (nkv - 1)) || G > 7 || !decode_step_supported(d, G))
+        return DETINT_OK;                           // (16-bit weights: the layer-by-layer path)
     for (int K : {H, nqd, F})
         if ((K & 15) || K > STEP_SLOT) return DETINT_OK;
     int dev = 0;
@@ -670,8 +692,14 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
     sh.update(blob.data(), blob.size());
     if (sh.hex() != want) return fail(DETINT_E_SHA, "artifact sha256 mismatch");
     const unsigned char* hd = blob.data();
-    if (memcmp(hd, "DETINT01", 8) != 0 || rd32(hd + 8) != 1) return fail(DETINT_E_ARTIFACT, "bad magic/version");
+    if (memcmp(hd, "DETINT01", 8) != 0 || (rd32(hd + 8) != 1 && rd32(hd + 8) != 2))
+        return fail(DETINT_E_ARTIFACT, "bad magic/version");
+    // version 2: the exact mode's 16-bit weights (weight bits at byte 72)
+    const int wide = rd32(hd + 8) == 2;
+    if (wide && rd32(hd + 72) != 16) return fail(DETINT_E_ARTIFACT, "unsupported weight width");
+    const size_t wb = wide ? 2 : 1;                 // bytes per weight
     detint_model* m = new detint_model();
+    m->wide = wide;
     m->L = rd32(hd + 12); m->H = rd32(hd + 16); m->nq = rd32(hd + 20); m->nkv = rd32(hd + 24);
     m->d = rd32(hd + 28); m->F = rd32(hd + 32); m->V = rd32(hd + 36); m->max_pos = rd32(hd + 40);
     m->qk_norm = rd32(hd + 44); m->eps_h = rd32(hd + 48); m->eps_qk = rd32(hd + 52);
@@ -704,6 +732,9 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
     // device weight blob layout (same order, gate/up interleaved)
     size_t dsz = 0;
     auto dtake = [&](size_t bytes) { size_t o = dsz; dsz = al256(dsz + bytes); return o; };
+    // kind 0: copied as is; kind 1: gate/up, interleaved below; kind 2: 16-bit
+    // weights, copied then split on the device into the high limbs (int8, at
+    // doff) and the low limbs (uint8, at doff + count)
     struct Sec { const unsigned char* src; size_t bytes; size_t doff; int kind; };
     std::vector<Sec> secs;
     auto add = [&](size_t bytes, int kind = 0) {
@@ -711,50 +742,69 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
         secs.push_back({p, bytes, dtake(bytes), kind});
         return secs.size() - 1;
     };
-    size_t s_embed = add((size_t)V * H), s_em = add((size_t)V * 4), s_fg = add((size_t)H * 2),
+    const int wk = wide ? 2 : 0;                    // kind of a weight section
+    size_t s_embed = add((size_t)V * H * wb, wk), s_em = add((size_t)V * 4), s_fg = add((size_t)H * 2),
            s_rc = add((size_t)m->max_pos * (d / 2) * 2), s_rs = add((size_t)m->max_pos * (d / 2) * 2);
     struct LS { size_t ag, fg, qg, kg, wqkv, mqkv, wo, mo, wg, mg, wu, mu, wd, md, kvp, wgu, mgu; };
     std::vector<LS> ls(m->L);
     for (int l = 0; l < m->L; ++l) {
         LS& x = ls[l];
         x.ag = add((size_t)H * 2); x.fg = add((size_t)H * 2); x.qg = add((size_t)d * 2);
-        x.kg = add((size_t)d * 2); x.wqkv = add((size_t)nqkv * H); x.mqkv = add((size_t)nqkv * 4);
-        x.wo = add((size_t)H * nq * d); x.mo = add((size_t)H * 4);
-        x.wg = secs.size(); secs.push_back({take((size_t)F * H), (size_t)F * H, 0, 1});
+        x.kg = add((size_t)d * 2); x.wqkv = add((size_t)nqkv * H * wb, wk); x.mqkv = add((size_t)nqkv * 4);
+        x.wo = add((size_t)H * nq * d * wb, wk); x.mo = add((size_t)H * 4);
+        x.wg = secs.size(); secs.push_back({take((size_t)F * H * wb), (size_t)F * H * wb, 0, 1});
         x.mg = secs.size(); secs.push_back({take((size_t)F * 4), (size_t)F * 4, 0, 1});
-        x.wu = secs.size(); secs.push_back({take((size_t)F * H), (size_t)F * H, 0, 1});
+        x.wu = secs.size(); secs.push_back({take((size_t)F * H * wb), (size_t)F * H * wb, 0, 1});
         x.mu = secs.size(); secs.push_back({take((size_t)F * 4), (size_t)F * 4, 0, 1});
-        x.wgu = dtake((size_t)2 * F * H);
+        x.wgu = dtake((size_t)2 * F * H * wb);
         x.mgu = dtake((size_t)2 * F * 4);
-        x.wd = add((size_t)H * F); x.md = add((size_t)H * 4);
+        x.wd = add((size_t)H * F * wb, wk); x.md = add((size_t)H * 4);
         x.kvp = add((size_t)nkv * (8 + d / 2) * 4);
     }
     if (!ok) { delete m; return fail(DETINT_E_ARTIFACT, "artifact truncated"); }
     cudaError_t ce = cudaMalloc(&m->wblob, dsz);
     if (ce != cudaSuccess) { m->wblob = nullptr; detint_free(m); return fail(DETINT_E_OOM, "weight allocation failed"); }
-    for (const Sec& sc : secs)
-        if (sc.kind == 0) {
-            ce = cudaMemcpy(m->wblob + sc.doff, sc.src, sc.bytes, cudaMemcpyHostToDevice);
-            if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
-        }
+    // 16-bit weights pass through a device staging buffer and are split there
+    // into limbs: W = 256 hi + lo (hi = W >> 8, lo = W & 255)
+    int16_t* w16 = nullptr;
+    auto put16 = [&](size_t doff, const void* src, size_t count) -> cudaError_t {
+        cudaError_t e = cudaMemcpy(w16, src, count * 2, cudaMemcpyHostToDevice);
+        if (e == cudaSuccess)
+            e = launch_split_w16(w16, (int8_t*)(m->wblob + doff), (uint8_t*)(m->wblob + doff + count),
+                                 (long long)count, nullptr);
+        return e == cudaSuccess ? cudaDeviceSynchronize() : e;
+    };
+    if (wide) {
+        size_t mx = (size_t)2 * F * H;
+        for (const Sec& sc : secs)
+            if (sc.kind == 2) mx = std::max(mx, sc.bytes / 2);
+        if (cudaMalloc(&w16, mx * 2) != cudaSuccess) { detint_free(m); return fail(DETINT_E_OOM, "staging allocation failed"); }
+    }
+    for (const Sec& sc : secs) {
+        if (sc.kind == 0) ce = cudaMemcpy(m->wblob + sc.doff, sc.src, sc.bytes, cudaMemcpyHostToDevice);
+        else if (sc.kind == 2) ce = put16(sc.doff, sc.src, sc.bytes / 2);
+        if (ce != cudaSuccess) { if (w16) cudaFree(w16); detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
+    }
     // gate/up interleaved as rows (gate_i, up_i) so one CTA holds both of a channel
-    std::vector<int8_t> gu((size_t)2 * F * H);
+    std::vector<unsigned char> gu((size_t)2 * F * H * wb);
     std::vector<int32_t> mgu((size_t)2 * F);
     m->layers.resize(m->L);
     for (int l = 0; l < m->L; ++l) {
         const LS& x = ls[l];
-        const int8_t* wg = (const int8_t*)secs[x.wg].src;
-        const int8_t* wu = (const int8_t*)secs[x.wu].src;
+        const unsigned char* wg = secs[x.wg].src;
+        const unsigned char* wu = secs[x.wu].src;
         const int32_t* mg = (const int32_t*)secs[x.mg].src;
         const int32_t* mu = (const int32_t*)secs[x.mu].src;
+        const size_t rb = (size_t)H * wb;             // bytes per weight row
         for (int i = 0; i < F; ++i) {
-            memcpy(&gu[(size_t)(2 * i) * H], wg + (size_t)i * H, H);
-            memcpy(&gu[(size_t)(2 * i + 1) * H], wu + (size_t)i * H, H);
+            memcpy(&gu[(size_t)(2 * i) * rb], wg + (size_t)i * rb, rb);
+            memcpy(&gu[(size_t)(2 * i + 1) * rb], wu + (size_t)i * rb, rb);
             int32_t a, b;
             memcpy(&a, mg + i, 4); memcpy(&b, mu + i, 4);
             mgu[2 * i] = a; mgu[2 * i + 1] = b;
         }
-        ce = cudaMemcpy(m->wblob + x.wgu, gu.data(), gu.size(), cudaMemcpyHostToDevice);
+        ce = wide ? put16(x.wgu, gu.data(), (size_t)2 * F * H)
+                  : cudaMemcpy(m->wblob + x.wgu, gu.data(), gu.size(), cudaMemcpyHostToDevice);
         if (ce == cudaSuccess) ce = cudaMemcpy(m->wblob + x.mgu, mgu.data(), mgu.size() * 4, cudaMemcpyHostToDevice);
         if (ce != cudaSuccess) { detint_free(m); return fail(DETINT_E_CUDA, cudaGetErrorString(ce)); }
         LayerW& w = m->layers[l];
@@ -766,8 +816,17 @@ int detint_load(const char* path, int max_batch, int max_ctx, detint_stream_t st
         w.w_gu = (int8_t*)(m->wblob + x.wgu); w.m_gu = (int32_t*)(m->wblob + x.mgu);
         w.w_d = (int8_t*)P(x.wd); w.m_d = (int32_t*)P(x.md);
         w.kvp = (int32_t*)P(x.kvp);
+        w.l_qkv = w.l_o = w.l_gu = w.l_d = nullptr;
+        if (wide) {
+            w.l_qkv = (uint8_t*)w.w_qkv + (size_t)nqkv * H;
+            w.l_o = (uint8_t*)w.w_o + (size_t)H * nq * d;
+            w.l_gu = (uint8_t*)w.w_gu + (size_t)2 * F * H;
+            w.l_d = (uint8_t*)w.w_d + (size_t)H * F;
+        }
     }
+    if (w16) cudaFree(w16);
     m->embed = (int8_t*)(m->wblob + secs[s_embed].doff);
+    if (wide) m->embed_lo = (uint8_t*)m->embed + (size_t)V * H;
     m->embed_m = (int32_t*)(m->wblob + secs[s_em].doff);
     m->final_gamma = (int16_t*)(m->wblob + secs[s_fg].doff);
     m->rope_cos = (int16_t*)(m->wblob + secs[s_rc].doff);

@@ -223,6 +223,17 @@ enum { DETINT_OPT_GRAPH = 0, DETINT_OPT_FUSED_DECODE = 1, DETINT_OPT_TC_PREFILL 
        DETINT_OPT_STAGED_DECODE = 3, DETINT_OPT_PERSISTENT = 4, DETINT_OPT_WAIT_TEST = 5 };
 int detint_set_option(detint_model* m, int option, int value);
 
+/* Integer-pipe peak loop, the measured denominator of the int8 GEMM and
+ * prefill roofline fractions (no passage of the pages: a measurement
+ * routine). kind 0: blocks x 256 threads of independent mma.sync m16n8k32
+ * s8 operations on register operands; kind 1: the same with dp4a. Each
+ * thread runs `iters` rounds and stores a checksum into sink (device
+ * int32[blocks * 256], caller-owned); *ops (host) receives the integer
+ * operations the launch performs (2 per multiply-add). Time it with events
+ * on `s`. Asynchronous; allocates nothing. Errors: ARG, CUDA. */
+int detint_int8_peak_loop(int kind, int blocks, int iters, int32_t* sink, long long* ops,
+                          detint_stream_t s);
+
 /* Shape of the loaded model: info[0..9] = n_layers, hidden, n_q, n_kv,
  * head_dim, ffn, vocab, max_pos, qk_norm, max_batch; info[10] = max_ctx. */
 int detint_model_info(detint_model* m, int32_t* info);
