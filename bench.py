@@ -181,7 +181,7 @@ def cpu_baseline(seconds: float = 12.0):
 
 # DRAM bytes (read + write) of one lm_head GEMV launch at M=1, from an ncu
 # capture of dram__bytes_read.sum + dram__bytes_write.sum on the current kernel
-LMHEAD_DRAM_BYTES = None
+LMHEAD_DRAM_BYTES = 158290432
 
 
 def int8_peak(pkg, dev, iters=4096, reps=5):
@@ -193,7 +193,7 @@ def int8_peak(pkg, dev, iters=4096, reps=5):
     import torch
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     blocks = 4 * nsm
-    sink = torch.empty(blocks * 256, dtype=torch.int32, device=dev)
+    sink = torch.empty(blocks * 256 * 8, dtype=torch.int32, device=dev)
     out = {}
     for kind, name in ((0, "mma_s8"), (1, "dp4a")):
         best = None
@@ -470,10 +470,12 @@ def run_oracle_configs(args):
     q = synth.prompt_ids(SEED, 0, PROMPT_LEN, 151936)
     lens = synth.coprompt_lengths(SEED, 7)
     p4 = synth.prompt_ids(SEED, 7, 2048, 151936)
-    for threads, budget, cut in ((cores, 8.0, None), (1, 2.0, 64)):
-        # one core: the prompts cut to `cut` tokens so the run stays within minutes
-        def c(p):
-            return p if cut is None else p[:cut]
+    for threads, budget, cut in ((cores, 8.0, 512), (1, 2.0, 64)):
+        # the long prompts cut to `cut` tokens (256 on all cores for the
+        # Llama-shaped contexts) so the run stays within a few minutes
+        def c(p, cap=None):
+            k = cut if cap is None or threads == 1 else cap
+            return p[:k]
         timed(SHAPE, q, 64, f"config 3 row 0 ({len(c(q))}-token prompt)", threads, budget)
         for i in (0, 3):
             pi = c(synth.prompt_ids(SEED, 100 + i, int(lens[i]), 151936))
@@ -481,11 +483,66 @@ def run_oracle_configs(args):
         timed(SHAPE, c(p4), 8, f"config 4 ({len(c(p4))} tokens of the 2048-token prompt, token by token)",
               threads, budget)
         for b in (0, 17):
-            pb = c(synth.prompt_ids(9, b, 1024, 128256))
+            pb = c(synth.prompt_ids(9, b, 1024, 128256), 256)
             timed("llama-1b", pb, 8, f"config 5 sequence {b} ({len(pb)}-token context)", threads, budget)
     oracle.set_threads(cores)
     print(json.dumps({"metric": "CPU oracle on configs 3-5 (bounded samples)", "unit": "tok/s",
                       "cores": cores, "samples": res}), flush=True)
+
+
+def run_all_kernels(args):
+    """Every kernel of the library at least once, on small shapes (for
+    per-kernel counter captures such as the floating-point instruction
+    classes): tiny-model prefill on the tensor-core attention and on the
+    per-token one, decode through the fused step (staged and global K/V
+    reads), the row kernels, the one-launch step and a batch of 12 (tiled
+    GEMMs with split K), the exact mode (limb split, limb GEMM, 128-bit
+    epilogue), integer sampling, the allocation-free argmax, the raw int8
+    GEMMs and the peak loops."""
+    import torch
+    import synth
+    from deterministic_integer_only_gb300 import build
+    build.build()
+    import deterministic_integer_only_gb300 as pkg
+    dev = torch.device("cuda")
+    launched = []
+    for wide in (False, True):
+        path = synth.ensure_artifact("tiny", SEED, wide=wide)
+        for mode in ("fused", "rows", "one-launch", "tc-off", "global-attn"):
+            if wide and mode != "fused":
+                continue
+            m = pkg.Model(path, max_batch=12, max_ctx=128)
+            if mode == "rows":
+                m.set_fused_decode(False)
+            if mode == "one-launch":
+                m.set_persistent(True)
+            if mode == "tc-off":
+                m.set_tc_prefill(False)
+            if mode == "global-attn":
+                m.set_staged_decode(False)
+            prompts = [synth.prompt_ids(SEED, i, 12 + 5 * i, m.vocab) for i in range(2)]
+            m.generate(prompts, 3, keep_logits=False)
+            launched.append(f"{'wide ' if wide else ''}{mode}")
+            m.close()
+    m = pkg.Model(synth.ensure_artifact("tiny", SEED), max_batch=12, max_ctx=128)
+    m.generate([synth.prompt_ids(SEED, 20 + i, 9 + i, m.vocab) for i in range(12)], 3, keep_logits=False)
+    launched.append("batch 12")
+    m.close()
+    lg = torch.randint(-(1 << 20), 1 << 20, (2, 4096), dtype=torch.int32, device=dev)
+    pkg.detint_sample(lg, {"seed": 1, "inv_temp": 65536, "top_k": 50, "top_p": 60000})
+    pkg.detint_argmax_noalloc(lg, torch.empty(2, dtype=torch.int32, device=dev))
+    for M in (4, 96):
+        A = torch.randint(-127, 128, (M, 256), dtype=torch.int8, device=dev)
+        W = torch.randint(-127, 128, (512, 256), dtype=torch.int8, device=dev)
+        pkg.detint_gemm_i8(A, W, torch.empty((M, 512), dtype=torch.int32, device=dev))
+    W16 = torch.randint(-32767, 32768, (512, 256), dtype=torch.int16, device=dev)
+    hi, lo = pkg.detint_split_w16(W16)
+    pkg.detint_gemm_w16(torch.randint(-127, 128, (64, 256), dtype=torch.int8, device=dev), hi, lo)
+    sink = torch.empty(256 * 8, dtype=torch.int32, device=dev)
+    for kind in (0, 1):
+        pkg.detint_int8_peak_loop(kind, 1, 16, sink)
+    torch.cuda.synchronize()
+    print(json.dumps({"workload": "kernels", "model_runs": launched}), flush=True)
 
 
 def run_gemm_sweep(args):
@@ -519,13 +576,15 @@ def run_gemm_sweep(args):
                       "sweep": rows}), flush=True)
 
 
-def _decode_rate(pkg, path, B, K, W, dev, dist, ws):
+def _decode_rate(pkg, path, B, K, W, dev, dist, ws, one_launch=False):
     """(tok/s over all ranks, ms per step) of K graph-replayed decode steps
     of B sequences, inputs resident on the device."""
     import torch
     import synth
     max_ctx = PROMPT_LEN + W + 2 * K + 280
     model = pkg.Model(path, max_batch=B, max_ctx=((max_ctx + 63) // 64) * 64)
+    if one_launch:
+        model.set_persistent(True)
     V = model.vocab
     prompts = [synth.prompt_ids(SEED, 0, PROMPT_LEN, V)]
     prompts += [synth.prompt_ids(SEED, 100 + i, int(n), V)
@@ -567,6 +626,11 @@ def main():
     ap.add_argument("--impl", default="detint", choices=["detint", "reference"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-steps", action="store_true",
+                    help="run the prefill, warm-up and timed decode steps only, print their time "
+                         "(for launch-list captures of the decode step)")
+    ap.add_argument("--one-launch", action="store_true",
+                    help="decode through the one-launch step (cooperative, tagged rows)")
     ap.add_argument("--no-companion", dest="companion", action="store_false",
                     help="skip the B=8 companion measurement of the decode line")
     ap.add_argument("--shape", default=None, help="M,N,K for --workload lmhead (default 1,151936,1024 "
@@ -575,7 +639,7 @@ def main():
     ap.add_argument("--prefill-len", type=int, default=4096, help="prefill workload: tokens each")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "gemm", "lmhead", "llama-b32", "sample", "gemm-w16",
-                             "int8-peak", "oracle-configs"],
+                             "int8-peak", "oracle-configs", "kernels"],
                     help="decode (the headline line), prefill (4 x 4096 prompt throughput) or "
                          "gemm (exact int8 GEMM sweep over the Llama-3.2-1B projection shapes)")
     args = ap.parse_args()
@@ -597,6 +661,8 @@ def main():
         return run_int8_peak(args)
     if args.workload == "oracle-configs":
         return run_oracle_configs(args)
+    if args.workload == "kernels":
+        return run_all_kernels(args)
 
     import torch
     import synth
@@ -636,6 +702,8 @@ def main():
         s.synchronize()
         return tok
 
+    if args.one_launch:
+        model.set_persistent(True)
     # ---- device-resident timed region: K decode steps, one graph each
     tok = start()
     if dist:
@@ -656,6 +724,12 @@ def main():
         ms = max_over_ranks(ms, dist, dev)
         dist.barrier()
     value = B * K * ws / (ms / 1e3)
+    if args.only_steps:
+        if rank == 0:
+            print(json.dumps({"workload": f"decode steps, B={B}", "steps": K, "warmup": W,
+                              "ms_per_step": ms / K, "tok_s": value}), flush=True)
+        model.close()
+        return
 
     # ---- end to end through the public API with host buffers
     for sid in seq_ids:
@@ -722,7 +796,7 @@ def main():
     # with 8 sequences (row 0 = the prompt above, 7 seeded co-prompts)
     other = None
     if args.companion and B != 8:
-        other = _decode_rate(pkg, path, 8, K, W, dev, dist, ws)
+        other = _decode_rate(pkg, path, 8, K, W, dev, dist, ws, args.one_launch)
     # companions for the metric's other parts: the measured int8 pipe peak and
     # the prefill of 4 x 4096 tokens against it
     pk = int8_peak(pkg, dev)

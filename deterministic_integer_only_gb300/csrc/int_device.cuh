@@ -136,6 +136,57 @@ __host__ __device__ __forceinline__ u64 pow2_recip(u64 v, int e, u64 c, int s) {
     return q;
 }
 
+// floor(n / d) for d >= 1 when the quotient is below 2^31 and n < 2^63, by
+// the Newton-Raphson reciprocal of d's leading 32 bits (the steps of
+// pow2_recip), a 128-bit product n y and the exact remainder n - q d, which
+// settles the estimate (within a few units) by single steps
+__host__ __device__ __forceinline__ u64 udiv_small(u64 n, u64 d) {
+    const int e = bitlen_u64(d);
+    const uint32_t d32 = (uint32_t)(e <= 32 ? d << (32 - e) : d >> (e - 32));   // [2^31, 2^32)
+    uint32_t y = 3031741621u - (uint32_t)(((u64)2021161080u * d32) >> 32);     // ~2^62 / d32, Q30
+#pragma unroll
+    for (int it = 0; it < 3; ++it) {
+        const u64 p = (u64)d32 * y;
+        const bool over = p > (1ull << 62);
+        const u64 t = over ? p - (1ull << 62) : (1ull << 62) - p;
+        const uint32_t corr = (uint32_t)(((u64)y * (uint32_t)(t >> 31)) >> 31);
+        y = over ? y - corr : y + corr;
+    }
+    // n / d ~ n y / 2^(30 + e): the 128-bit product's bits from 30 + e up
+    const int sh = 30 + e;                        // in [31, 94]
+#ifdef __CUDA_ARCH__
+    const u64 hi = __umul64hi(n, (u64)y);
+#else
+    const u64 hi = (u64)(((unsigned __int128)n * y) >> 64);
+#endif
+    const u64 lo = n * (u64)y;
+    u64 q = sh >= 64 ? hi >> (sh - 64) : ((hi << (64 - sh)) | (lo >> sh));
+    long long rem = (long long)(n - q * d);
+    const long long dd = (long long)d;
+    for (int i = 0; i < 4 && rem < 0; ++i) { --q; rem += dd; }
+    for (int i = 0; i < 4 && rem >= dd; ++i) { ++q; rem -= dd; }
+    return q;
+}
+
+// dyadic(N, D) in one thread: the exponent by bit lengths and comparisons,
+// the mantissa by udiv_small (quotient <= 2^15)
+__host__ __device__ __forceinline__ void dyadic_fast(u64 N, u64 D, int* m_out, int* k_out) {
+    int k = 14 + bitlen_u64(D) - bitlen_u64(N);
+    for (int it = 0; it < 4; ++it) {
+        u64 lhs, lo;
+        if (k >= 0) { lhs = N << k; lo = D << 14; }
+        else { lhs = N; lo = D << (14 - k); }
+        if (lhs < lo) { ++k; continue; }
+        if (lhs >= (lo << 1)) { --k; continue; }
+        break;
+    }
+    u64 num, den;
+    if (k >= 0) { num = (N << (k + 1)) + D; den = D << 1; }
+    else { num = (N << 1) + (D << (-k)); den = D << (1 - k); }
+    *m_out = (int)udiv_small(num, den);
+    *k_out = k;
+}
+
 // rshr(acc * M, s) with the product formed exactly in 128 bits, for the
 // exact mode's int64 accumulators of 16-bit weights (|acc| < 2^36, M < 2^31,
 // 1 <= s <= 100; the result must fit int64): the product as a two's-
@@ -210,24 +261,6 @@ __host__ __device__ __forceinline__ int swiglu_dev(int g, int u) {
 // largest that still satisfies the defining inequality (exact results,
 // identical to the bit-serial forms above).
 
-// floor(n / d), d >= 1, n < 2^62
-__device__ __forceinline__ u64 warp_udiv64(u64 n, u64 d) {
-    if (n < d) return 0;
-    const u64 lane = threadIdx.x & 31;
-    const int qb = bitlen_u64(n) - bitlen_u64(d) + 1;     // quotient < 2^qb
-    u64 q = 0;
-    for (int sh = qb - 5;; sh -= 5) {
-        const int s = sh < 0 ? 0 : sh;
-        const int nb = sh < 0 ? 5 + sh : 5;
-        const u64 cand = q + (lane << s);
-        const bool ok = lane < (1ull << nb) && cand * d <= n;   // cand*d < 2^(bitlen(n)+1)
-        const unsigned bal = __ballot_sync(0xffffffffu, ok);
-        q += (u64)(31 - __clz((int)bal)) << s;
-        if (sh <= 0) break;
-    }
-    return q;
-}
-
 // floor(sqrt(n)), n < 2^62
 __device__ __forceinline__ u64 warp_isqrt64(u64 n) {
     if (n == 0) return 0;
@@ -246,22 +279,5 @@ __device__ __forceinline__ u64 warp_isqrt64(u64 n) {
     return r;
 }
 
-// dyadic(N, D) computed by a warp
-__device__ __forceinline__ void warp_dyadic(u64 N, u64 D, int* m_out, int* k_out) {
-    int k = 14 + bitlen_u64(D) - bitlen_u64(N);
-    for (int it = 0; it < 4; ++it) {
-        u64 lhs, lo;
-        if (k >= 0) { lhs = N << k; lo = D << 14; }
-        else { lhs = N; lo = D << (14 - k); }
-        if (lhs < lo) { ++k; continue; }
-        if (lhs >= (lo << 1)) { --k; continue; }
-        break;
-    }
-    u64 num, den;
-    if (k >= 0) { num = (N << (k + 1)) + D; den = D << 1; }
-    else { num = (N << 1) + (D << (-k)); den = D << (1 - k); }
-    *m_out = (int)warp_udiv64(num, den);
-    *k_out = k;
-}
 
 }  // namespace detint

@@ -331,10 +331,10 @@ __device__ void mg_scales(const StepArgs& a, MgShared& sh, const MgPhase& P) {
                 if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (a.eps_h >> (2 * sig));
                 else eps_s = a.eps_h * (1LL << (-2 * sig));
                 const u64 rr = warp_isqrt64((u64)((ss >> lg_k) + eps_s));
-                warp_dyadic(az, 127ull * rr, &m, &k);
+                dyadic_fast(az, 127ull * rr, &m, &k);
                 k += 12;
             } else {
-                warp_dyadic(axl, 127ull, &m, &k);
+                dyadic_fast(axl, 127ull, &m, &k);
                 k += P.F_in;
             }
         }
@@ -655,15 +655,14 @@ __device__ void mg_attention(const StepArgs& a, MgShared& sh, const StepLayer& L
     const i64 CSTM = kvp[6], MV = kvp[4];
     const int CSTK = kvp[7], KVS = kvp[5];
     // ---- scores and per-head maxima (warps 0..7); warp 8: the q heads' scales
-    if (w == 8) {
-        for (int hh = 0; hh < G; ++hh) {
-            int m = 0, k = 0;
-            if (amq[hh]) {
-                warp_dyadic(amq[hh], 127ull, &m, &k);
-                k += 14;
-            }
-            if (lane == 0) { mqs[hh] = m; kqs[hh] = k; }
+    if (w == 8 && lane < G) {          // lane hh: head hh
+        int m = 0, k = 0;
+        if (amq[lane]) {
+            dyadic_fast(amq[lane], 127ull, &m, &k);
+            k += 14;
         }
+        mqs[lane] = m;
+        kqs[lane] = k;
     }
     if (tid < 256) {
         int smax[G];

@@ -25,13 +25,23 @@ constexpr int W16_BM = 64;
 constexpr int W16_STAGE = (W16_BM + 2 * GM_BN) * GM_BK;   // A + W_hi + W_lo tiles, 40 KB
 constexpr size_t W16_SMEM = (size_t)GM_STAGES * W16_STAGE + 1024;
 
-__global__ void k_split_w16(const int16_t* __restrict__ W, int8_t* __restrict__ hi,
+// the limbs of little-endian int16 weights are their bytes: the high limb
+// (W >> 8, floor, as int8) is the high byte and the low limb the low byte,
+// so the split only moves bytes
+// Thread i moves the 16 weights from 16 i on (the launch covers n with
+// n / 16 threads rounded up, so no thread loops: a loop with a run-time stride
+// would have its trip count formed by a division)
+constexpr int SPLIT_PER_THREAD = 16;
+__global__ void k_split_w16(const uint8_t* __restrict__ W, uint8_t* __restrict__ hi,
                             uint8_t* __restrict__ lo, long long n) {
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int w = W[i];
-        hi[i] = (int8_t)(w >> 8);          // arithmetic shift: floor(w / 256)
-        lo[i] = (uint8_t)(w & 255);
+    const long long i0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * SPLIT_PER_THREAD;
+#pragma unroll
+    for (int k = 0; k < SPLIT_PER_THREAD; ++k) {
+        const long long i = i0 + k;
+        if (i < n) {
+            lo[i] = W[2 * i];
+            hi[i] = W[2 * i + 1];
+        }
     }
 }
 

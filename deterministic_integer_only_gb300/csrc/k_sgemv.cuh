@@ -113,10 +113,10 @@ __device__ void sg_token_scale(const SgArgs& a, SgShared& sh, int r, int w0, int
             if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (a.eps >> (2 * sig));
             else eps_s = a.eps * (1LL << (-2 * sig));
             const u64 rr = warp_isqrt64((u64)((ss >> a.lg_k) + eps_s));
-            warp_dyadic(az, 127ull * rr, &m, &k);
+            dyadic_fast(az, 127ull * rr, &m, &k);
             k += 12;
         } else {
-            warp_dyadic(axl, 127ull, &m, &k);
+            dyadic_fast(axl, 127ull, &m, &k);
             k += a.F;
         }
     }

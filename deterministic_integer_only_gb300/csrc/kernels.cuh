@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(256) k_normquant(const int32_t* __restrict__ x
         else eps_s = eps * (1LL << (-2 * sig));
         const u64 rr = warp_isqrt64((u64)((ss >> lg_n) + eps_s));
         int m, k;
-        warp_dyadic(az, 127ull * rr, &m, &k);
+        dyadic_fast(az, 127ull * rr, &m, &k);
         if (tid == 0) { mt[r] = m; kt[r] = k + 12; }
     } else if (tid < 64) {
         const int e = bitlen_u64(az);
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(256) k_actquant(const int32_t* __restrict__ x,
         if (tid == 0) { bc[0] = (i64)R; bc[1] = e; }
     } else if (tid < 64) {
         int m, k;
-        warp_dyadic(a, 127ull, &m, &k);
+        dyadic_fast(a, 127ull, &m, &k);
         if (tid == 32) { mt[r] = m; kt[r] = k + F; }
     }
     __syncthreads();
@@ -306,7 +306,7 @@ __device__ void qkv_head_p(const QkvPostArgs& a, int t, int slot, int8_t* q_dst,
         const int e = bitlen_u64(am);
         const i64 R = (i64)pow2_recip(am, e, 127, 16);
         int m, k;
-        warp_dyadic(am, 127ull, &m, &k);
+        dyadic_fast(am, 127ull, &m, &k);
         if (lane == 0) {
             *mq_dst = m;
             *kq_dst = k + 14;
@@ -370,10 +370,12 @@ size_t attention_smem_bytes(int grp, int d, int ctx_cap) {
 
 // attention of token t's q heads of kv group g; qs [G][d], mqs/kqs [G] in
 // shared memory, sm the dynamic shared memory (score row, E bytes, partials)
-__device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs,
+template <int EPL, int G>
+__device__ __noinline__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs,
                                const int32_t* mqs, const int32_t* kqs, unsigned char* sm) {
     const int tid = threadIdx.x;
-    const int d = a.d, G = 1 << a.lg_grp, nkv = a.nkv, cap = a.ctx_cap;
+    constexpr int d = 32 * EPL;
+    const int nkv = a.nkv, cap = a.ctx_cap;
     const int seq = a.tok_seq[t];
     const int ctx = a.tok_pos[t] + 1;
     const int ctx16 = (ctx + 15) & ~15;
@@ -390,19 +392,20 @@ __device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs
     const int* bt = a.block_table + (size_t)seq * a.mbs;
 
     // phase 1: scores and per-head maxima
-    int smax[MAXG];
+    int smax[G];
 #pragma unroll
-    for (int hh = 0; hh < MAXG; ++hh) smax[hh] = -2147483647;
+    for (int hh = 0; hh < G; ++hh) smax[hh] = -2147483647;
     for (int j = tid; j < ctx; j += 256) {
         const int blk = bt[j >> 6];
         const int4* kr = (const int4*)(a.kc + (((size_t)blk * nkv + g) * KV_BLK + (j & 63)) * d);
-        int acc[MAXG];
+        int acc[G];
 #pragma unroll
-        for (int hh = 0; hh < MAXG; ++hh) acc[hh] = 0;
+        for (int hh = 0; hh < G; ++hh) acc[hh] = 0;
+#pragma unroll
         for (int v = 0; v < (d >> 4); ++v) {
             const int4 kw = kr[v];
 #pragma unroll
-            for (int hh = 0; hh < MAXG; ++hh) {
+            for (int hh = 0; hh < G; ++hh) {
                 if (hh < G) {
                     const int4 qw = *(const int4*)(qs + hh * d + v * 16);
                     acc[hh] = __dp4a(kw.x, qw.x, acc[hh]);
@@ -413,13 +416,13 @@ __device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs
             }
         }
 #pragma unroll
-        for (int hh = 0; hh < MAXG; ++hh)
+        for (int hh = 0; hh < G; ++hh)
             if (hh < G) { S[hh * cap + j] = acc[hh]; smax[hh] = max(smax[hh], acc[hh]); }
     }
     {
         const int lane = tid & 31, w = tid >> 5;
 #pragma unroll
-        for (int hh = 0; hh < MAXG; ++hh) {
+        for (int hh = 0; hh < G; ++hh) {
             if (hh < G) {
                 int v = smax[hh];
 #pragma unroll
@@ -439,29 +442,31 @@ __device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs
     }
     // phase 2: E_j (15 bits) split into bytes, and the row sums
     {
-        i64 sum[MAXG];
+        i64 sum[G];
 #pragma unroll
-        for (int hh = 0; hh < MAXG; ++hh) sum[hh] = 0;
-        for (int j = tid; j < ctx16; j += 256) {
+        for (int hh = 0; hh < G; ++hh) sum[hh] = 0;
+        for (int j = tid; j < ctx; j += 256) {
 #pragma unroll
-            for (int hh = 0; hh < MAXG; ++hh) {
-                if (hh < G) {
-                    int E = 0;
-                    if (j < ctx) {
-                        const i64 mq = mqs[hh];
-                        const int kq = kqs[hh];
-                        const i64 u = rshr((i64)S[hh * cap + j] * mq * CSTM, kq + CSTK - 10);
-                        E = min(32767, exp2q_dev(u - umax_s[hh]));
-                    }
-                    Elo[hh * cap + j] = (unsigned char)(E & 255);
-                    Ehi[hh * cap + j] = (unsigned char)(E >> 8);
-                    sum[hh] += E;
-                }
+            for (int hh = 0; hh < G; ++hh) {
+                const i64 u = rshr((i64)S[hh * cap + j] * (i64)mqs[hh] * CSTM, kqs[hh] + CSTK - 10);
+                const int E = min(32767, exp2q_dev(u - umax_s[hh]));
+                Elo[hh * cap + j] = (unsigned char)(E & 255);
+                Ehi[hh * cap + j] = (unsigned char)(E >> 8);
+                sum[hh] += E;
+            }
+        }
+        // keys from ctx to the next multiple of 16 weigh nothing in the P.V
+        // products, which read whole 16-key groups
+        for (int j = ctx + tid; j < ctx16; j += 256) {
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                Elo[hh * cap + j] = 0;
+                Ehi[hh * cap + j] = 0;
             }
         }
         const int lane = tid & 31, w = tid >> 5;
 #pragma unroll
-        for (int hh = 0; hh < MAXG; ++hh) {
+        for (int hh = 0; hh < G; ++hh) {
             if (hh < G) {
                 i64 v = warp_sum_i64(sum[hh]);
                 if (lane == 0) red[w * MAXG + hh] = v;
@@ -483,14 +488,14 @@ __device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs
         const int parts = 256 >> (d == 128 ? 7 : 6);   // threads per channel
         const int c = tid & (d - 1);
         const int p = tid >> (d == 128 ? 7 : 6);
-        int lo[MAXG], hi[MAXG];
+        int lo[G], hi[G];
 #pragma unroll
-        for (int hh = 0; hh < MAXG; ++hh) { lo[hh] = 0; hi[hh] = 0; }
+        for (int hh = 0; hh < G; ++hh) { lo[hh] = 0; hi[hh] = 0; }
         for (int j0 = p * 16; j0 < ctx16; j0 += parts * 16) {
             const int blk = bt[j0 >> 6];
             const int4 vw = *(const int4*)(a.vc + (((size_t)blk * nkv + g) * d + c) * KV_BLK + (j0 & 63));
 #pragma unroll
-            for (int hh = 0; hh < MAXG; ++hh) {
+            for (int hh = 0; hh < G; ++hh) {
                 if (hh < G) {
                     const uint4 el = *(const uint4*)(Elo + hh * cap + j0);
                     const int4 eh = *(const int4*)(Ehi + hh * cap + j0);
@@ -506,7 +511,7 @@ __device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs
             }
         }
 #pragma unroll
-        for (int hh = 0; hh < MAXG; ++hh) {
+        for (int hh = 0; hh < G; ++hh) {
             if (hh < G) {
                 part[(0 * 256 + tid) * MAXG + hh] = lo[hh];
                 part[(1 * 256 + tid) * MAXG + hh] = hi[hh];
@@ -533,11 +538,12 @@ __device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs
 
 // per-token prefill attention (the option that turns the tensor-core prefill
 // attention off): queries already quantised by k_qkv_post
+template <int EPL, int G>
 __global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ int32_t mqs[MAXG], kqs[MAXG];
     const int t = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
-    const int G = 1 << a.lg_grp, d = a.d;
+    constexpr int d = 32 * EPL;
     int8_t* qs = (int8_t*)sm;
     const int4* qsrc = (const int4*)(a.q8 + ((size_t)t * a.nq + (g << a.lg_grp)) * d);
     for (int i = tid; i < (G * d) >> 4; i += 256) ((int4*)qs)[i] = qsrc[i];
@@ -546,18 +552,17 @@ __global__ void __launch_bounds__(256) k_attention(AttnArgs a) {
         kqs[tid] = a.kq[(size_t)t * a.nq + (g << a.lg_grp) + tid];
     }
     __syncthreads();
-    attention_core(a, t, g, qs, mqs, kqs, sm);
+    attention_core<EPL, G>(a, t, g, qs, mqs, kqs, sm);
 }
 
 // decode: one new token per sequence, so this CTA alone produces the K/V of
 // (sequence, position) it then attends to; QK-norm/RoPE/quantisation of its
 // G q heads and its kv head run first, one warp per head.
-template <int EPL>
+template <int EPL, int G>
 __global__ void __launch_bounds__(256) k_attn_decode(AttnArgs a, QkvPostArgs qa) {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ int32_t mqs[MAXG], kqs[MAXG];
     const int t = blockIdx.x, g = blockIdx.y, w = threadIdx.x >> 5;
-    const int G = 1 << a.lg_grp;
     const int dh2 = a.d >> 1;
     int8_t* qs = (int8_t*)sm;
     // RoPE row, QK-norm gammas and this kv head's parameters never depend on
@@ -600,7 +605,7 @@ __global__ void __launch_bounds__(256) k_attn_decode(AttnArgs a, QkvPostArgs qa)
         qkv_head_p<EPL>(qa, t, a.nq + g, nullptr, nullptr, nullptr, s_cos, s_sin, s_kvp, s_gq, s_gk);
     __syncthreads();
     pdl_launch();
-    attention_core(a, t, g, qs, mqs, kqs, sm);
+    attention_core<EPL, G>(a, t, g, qs, mqs, kqs, sm);
 }
 
 // ------------------------------------------------------------- GEMV (M<=32)

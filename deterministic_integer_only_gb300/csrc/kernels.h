@@ -111,7 +111,9 @@ cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xi
                          const int32_t* rows, const int16_t* gamma, long long eps, int F, int pro,
                          int mode, const Epi& ep, cudaStream_t s, const int8_t* x8 = nullptr,
                          const int32_t* mt = nullptr, const int32_t* kt = nullptr,
-                         bool pdl = true);   // pdl: W is immutable (streamed before the wait)
+                         bool pdl = true,    // pdl: W is immutable (streamed before the wait)
+                         int spare_sms = 0); // SMs left free for the next kernel's CTAs, where
+                                             // no CTA then holds more row groups
 // decode attention fused with the QKV post-processing (one token per sequence)
 // staged: the variant that copies the sequence's K/V blocks into shared
 // memory before the wait (a.ctx_cap = its staged key capacity, a multiple of

@@ -106,10 +106,20 @@ cudaError_t launch_qkv_post(const QkvPostArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+using AttnFn = void (*)(AttnArgs);
+static AttnFn attention_kernel(int d, int lg_grp) {
+    static const AttnFn k128[4] = {k_attention<4, 1>, k_attention<4, 2>, k_attention<4, 4>, k_attention<4, 8>};
+    static const AttnFn k64[4] = {k_attention<2, 1>, k_attention<2, 2>, k_attention<2, 4>, k_attention<2, 8>};
+    if (lg_grp < 0 || lg_grp > 3) return nullptr;
+    return d == 128 ? k128[lg_grp] : (d == 64 ? k64[lg_grp] : nullptr);
+}
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
     const size_t smem = attention_smem_bytes(1 << a.lg_grp, a.d, a.ctx_cap);
     dim3 grid(a.T, a.nkv);
-    k_attention<<<grid, 256, smem, s>>>(a);
+    auto k = attention_kernel(a.d, a.lg_grp);
+    if (!k) return cudaErrorInvalidValue;
+    k<<<grid, 256, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -157,7 +167,7 @@ constexpr size_t SG_SMEM_MAX = 200 * 1024;
 cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xin,
                          const int32_t* rows, const int16_t* gamma, long long eps, int F, int pro,
                          int mode, const Epi& ep, cudaStream_t s, const int8_t* x8,
-                         const int32_t* mt, const int32_t* kt, bool pdl) {
+                         const int32_t* mt, const int32_t* kt, bool pdl, int spare_sms) {
     if (M < 1 || M > 8 || N < 1 || K < 64 || (K & 63)) return cudaErrorNotSupported;
     const int KC = K <= 1024 ? K : 1024;
     if (K % KC) return cudaErrorNotSupported;
@@ -183,7 +193,15 @@ cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xi
     while ((1 << lg) < K) ++lg;
     a.lg_k = lg;
     const int G = (N + 15) / 16;
-    const int ncta = G < g_num_sms * cta_per_sm ? G : g_num_sms * cta_per_sm;
+    int ncta = G < g_num_sms * cta_per_sm ? G : g_num_sms * cta_per_sm;
+    if (cta_per_sm == 1 && spare_sms > 0 && spare_sms < ncta) {
+        // spare_sms fewer CTAs when the most row groups a CTA holds stays the
+        // same: the SMs left free take all of the next kernel's CTAs, which
+        // under programmatic dependent launch stage their inputs while this
+        // kernel runs (freeing only some of the SMs it needs measured slower)
+        const int fewer = ncta - spare_sms;
+        if ((G + fewer - 1) / fewer == (G + ncta - 1) / ncta) ncta = fewer;
+    }
     a.rg_q = G / ncta;
     a.rg_r = G % ncta;
     if (pro != PRO_NORMQUANT && pro != PRO_ACTQUANT && pro != PRO_NONE) return cudaErrorNotSupported;
@@ -203,6 +221,17 @@ cudaError_t launch_sgemv(const int8_t* W, int N, int K, int M, const int32_t* xi
 size_t attn_dec_smem(int grp, int d, int cap) { return attn_dec_smem_bytes(grp, d, cap); }
 
 using AttnDecFn = void (*)(AttnArgs, QkvPostArgs);
+// the decode attention that reads K/V from the cache (contexts beyond the
+// staged kernel's shared-memory budget)
+static AttnDecFn attn_dec_global_kernel(int d, int lg_grp) {
+    static const AttnDecFn k128[4] = {k_attn_decode<4, 1>, k_attn_decode<4, 2>, k_attn_decode<4, 4>,
+                                      k_attn_decode<4, 8>};
+    static const AttnDecFn k64[4] = {k_attn_decode<2, 1>, k_attn_decode<2, 2>, k_attn_decode<2, 4>,
+                                     k_attn_decode<2, 8>};
+    if (lg_grp < 0 || lg_grp > 3) return nullptr;
+    return d == 128 ? k128[lg_grp] : (d == 64 ? k64[lg_grp] : nullptr);
+}
+
 static AttnDecFn attn_dec_kernel(int d, int lg_grp) {
     static const AttnDecFn k128[4] = {k_attn_dec_staged<4, 1>, k_attn_dec_staged<4, 2>,
                                       k_attn_dec_staged<4, 4>, k_attn_dec_staged<4, 8>};
@@ -223,9 +252,9 @@ cudaError_t launch_attn_decode(const AttnArgs& a, const QkvPostArgs& qa, cudaStr
     }
     const size_t smem = attention_smem_bytes(1 << a.lg_grp, a.d, a.ctx_cap);
     const dim3 grid(a.T, a.nkv);
-    if (a.d == 128) return launch_pdl(k_attn_decode<4>, grid, dim3(256), smem, s, a, qa);
-    if (a.d == 64) return launch_pdl(k_attn_decode<2>, grid, dim3(256), smem, s, a, qa);
-    return cudaErrorInvalidValue;
+    auto k = attn_dec_global_kernel(a.d, a.lg_grp);
+    if (!k) return cudaErrorInvalidValue;
+    return launch_pdl(k, grid, dim3(256), smem, s, a, qa);
 }
 
 // ------------------------------------------------------------ tiled GEMM
@@ -390,8 +419,10 @@ static cudaError_t gemv_attr_all() {
 
 cudaError_t launch_split_w16(const int16_t* W, int8_t* hi, uint8_t* lo, long long n, cudaStream_t s) {
     if (n < 1) return cudaErrorInvalidValue;
-    const long long blocks = std::min<long long>((n + 255) / 256, (long long)std::max(g_num_sms, 1) * 16);
-    k_split_w16<<<(unsigned)blocks, 256, 0, s>>>(W, hi, lo, n);
+    const long long per_block = 256LL * SPLIT_PER_THREAD;
+    const long long blocks = (n + per_block - 1) / per_block;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    k_split_w16<<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, (uint8_t*)hi, lo, n);
     return cudaGetLastError();
 }
 
@@ -479,12 +510,17 @@ cudaError_t kernels_init() {
     if (e == cudaSuccess) e = gemv_attr_all<EPI_RESADD>();
     if (e == cudaSuccess) e = gemv_attr_all<EPI_SWIGLU>();
     if (e == cudaSuccess) e = gemv_attr_all<EPI_LOGITS>();
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attn_decode<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attn_decode<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    for (int lg = 0; lg < 4 && e == cudaSuccess; ++lg) {
+        e = cudaFuncSetAttribute(attention_kernel(128, lg), cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attention_kernel(64, lg), cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_dec_global_kernel(128, lg), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     220 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_dec_global_kernel(64, lg), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     220 * 1024);
+    }
     const int sgm = (int)SG_SMEM_MAX;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_sgemv<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, sgm);

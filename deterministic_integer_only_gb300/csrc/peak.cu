@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(PK_THREADS) k_peak_mma(int iters, int32_t* sin
     int b0 = 0x0a0b0c0d ^ t, b1 = b0 + 3;
     int c[PK_CHAINS][4];
 #pragma unroll
-    for (int k = 0; k < PK_CHAINS; ++k) c[k][0] = c[k][1] = c[k][2] = c[k][3] = k;
+    for (int k = 0; k < PK_CHAINS; ++k) c[k][0] = c[k][1] = c[k][2] = c[k][3] = t ^ k;
     for (int i = 0; i < iters; ++i) {
 #pragma unroll
         for (int k = 0; k < PK_CHAINS; ++k)
@@ -30,26 +30,28 @@ __global__ void __launch_bounds__(PK_THREADS) k_peak_mma(int iters, int32_t* sin
                 : "+r"(c[k][0]), "+r"(c[k][1]), "+r"(c[k][2]), "+r"(c[k][3])
                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     }
-    int s = 0;
 #pragma unroll
-    for (int k = 0; k < PK_CHAINS; ++k) s += c[k][0] ^ c[k][1] ^ c[k][2] ^ c[k][3];
-    sink[blockIdx.x * PK_THREADS + t] = s;
+    for (int k = 0; k < PK_CHAINS; ++k)
+        sink[(blockIdx.x * PK_THREADS + t) * PK_CHAINS + k] = c[k][0] ^ c[k][1] ^ c[k][2] ^ c[k][3];
 }
 
 __global__ void __launch_bounds__(PK_THREADS) k_peak_dp4a(int iters, int32_t* sink) {
     const int t = threadIdx.x;
-    const int a = 0x01020304 * (t + 1), b = 0x0a0b0c0d ^ t;
-    int c[PK_CHAINS];
+    const int b = 0x0a0b0c0d ^ t;
+    int a[PK_CHAINS], c[PK_CHAINS];
 #pragma unroll
-    for (int k = 0; k < PK_CHAINS; ++k) c[k] = k;
+    for (int k = 0; k < PK_CHAINS; ++k) {
+        a[k] = __byte_perm(0x01020304 ^ t, k, 0x3210);     // one operand word per chain
+        c[k] = t ^ k;
+    }
+#pragma unroll 1
     for (int i = 0; i < iters; ++i) {
 #pragma unroll
-        for (int k = 0; k < PK_CHAINS; ++k) c[k] = __dp4a(a + k, b, c[k]);
+        for (int k = 0; k < PK_CHAINS; ++k)
+            asm volatile("dp4a.s32.s32 %0, %1, %2, %0;" : "+r"(c[k]) : "r"(a[k]), "r"(b));
     }
-    int s = 0;
 #pragma unroll
-    for (int k = 0; k < PK_CHAINS; ++k) s ^= c[k];
-    sink[blockIdx.x * PK_THREADS + t] = s;
+    for (int k = 0; k < PK_CHAINS; ++k) sink[(blockIdx.x * PK_THREADS + t) * PK_CHAINS + k] = c[k];
 }
 
 }  // namespace

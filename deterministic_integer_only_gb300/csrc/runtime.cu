@@ -306,16 +306,22 @@ static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32
     // per row) instead of redundantly by every GEMV CTA
     const bool sep = T >= 3;
     auto gemv = [&](const int8_t* W, int N, int K, const int32_t* xin, const int16_t* gamma, int F_in,
-                    int pro, int mode, const Epi& e) -> int {
+                    int pro, int mode, const Epi& e, int spare = 0) -> int {
         if (sep) {
             if (pro == 1) CK(launch_normquant(xin, nullptr, T, K, gamma, m->eps_h, m->x8, m->mt, m->kt, s, true));
             else CK(launch_actquant(xin, T, K, F_in, m->x8, m->mt, m->kt, s, true));
-            CK(launch_sgemv(W, N, K, T, nullptr, nullptr, nullptr, 0, 0, 0, mode, e, s, m->x8, m->mt, m->kt));
+            CK(launch_sgemv(W, N, K, T, nullptr, nullptr, nullptr, 0, 0, 0, mode, e, s, m->x8, m->mt, m->kt,
+                            true, spare));
         } else {
-            CK(launch_sgemv(W, N, K, T, xin, nullptr, gamma, m->eps_h, F_in, pro, mode, e, s));
+            CK(launch_sgemv(W, N, K, T, xin, nullptr, gamma, m->eps_h, F_in, pro, mode, e, s, nullptr, nullptr,
+                            nullptr, true, spare));
         }
         return DETINT_OK;
     };
+    // the staged attention's CTAs (one per token and kv head) need more shared
+    // memory than is left beside a GEMV CTA: SMs left free by the QKV GEMV
+    // take them early, and they copy the cached K/V while the GEMV runs
+    const int att_ctas = m->dec_staged ? T * nkv : 0;
     CK(launch_embed(tokens, T, m->tok_seq, m->tok_pos, m->seq_len_dev, 1, m->max_ctx,
                     m->embed, nullptr, m->embed_m, H, m->V, m->h, m->status, s));
     for (int l = 0; l < m->L; ++l) {
@@ -323,7 +329,7 @@ static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32
         Epi e{};
         e.status = m->status;
         e.out = m->qkv; e.ldo = nqkv; e.mc = w.m_qkv; e.fout = 12;
-        int rc = gemv(w.w_qkv, nqkv, H, m->h, w.attn_gamma, 0, 1, EPI_QKV, e);
+        int rc = gemv(w.w_qkv, nqkv, H, m->h, w.attn_gamma, 0, 1, EPI_QKV, e, att_ctas);
         if (rc) return rc;
         QkvPostArgs qa{};
         qa.qkv = m->qkv; qa.q_gamma = w.q_gamma; qa.k_gamma = w.k_gamma; qa.qk_norm = m->qk_norm;

@@ -227,8 +227,8 @@ int detint_set_option(detint_model* m, int option, int value);
  * prefill roofline fractions (no passage of the pages: a measurement
  * routine). kind 0: blocks x 256 threads of independent mma.sync m16n8k32
  * s8 operations on register operands; kind 1: the same with dp4a. Each
- * thread runs `iters` rounds and stores a checksum into sink (device
- * int32[blocks * 256], caller-owned); *ops (host) receives the integer
+ * thread runs `iters` rounds and stores its 8 accumulators' checksums
+ * into sink (device int32[blocks * 256 * 8], caller-owned); *ops (host) receives the integer
  * operations the launch performs (2 per multiply-add). Time it with events
  * on `s`. Asynchronous; allocates nothing. Errors: ARG, CUDA. */
 int detint_int8_peak_loop(int kind, int blocks, int iters, int32_t* sink, long long* ops,

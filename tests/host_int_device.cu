@@ -74,6 +74,14 @@ int main(int argc, char** argv) {
         for (size_t i = 0; i < g.size(); ++i) out[i] = swiglu_dev(g[i], u[i]);
         save(dir, "swiglu_out", out);
     }
+    {   // dyadic scales by the single-thread Newton-Raphson form
+        auto n = load<u64>(dir, "dyadic_n");
+        auto dd = load<u64>(dir, "dyadic_d");
+        std::vector<int32_t> mo(n.size()), ko(n.size());
+        for (size_t i = 0; i < n.size(); ++i) dyadic_fast(n[i], dd[i], &mo[i], &ko[i]);
+        save(dir, "dyadicf_m", mo);
+        save(dir, "dyadicf_k", ko);
+    }
     {   // exact-mode requantisation: rshr(acc * M, s) through a 128-bit product
         auto acc = load<i64>(dir, "mul128_acc");
         auto M = load<u64>(dir, "mul128_m");

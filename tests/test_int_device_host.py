@@ -123,6 +123,14 @@ def test_dyadic(host_run):
     np.testing.assert_array_equal(out("dyadic_k", np.int32), k)
 
 
+def test_dyadic_fast(host_run):
+    """The single-thread dyadic (Newton-Raphson division) equals the oracle's."""
+    inp, out = host_run
+    m, k = oracle.dyadic(inp["dyadic_n"].astype(np.int64), inp["dyadic_d"].astype(np.int64))
+    np.testing.assert_array_equal(out("dyadicf_m", np.int32), m)
+    np.testing.assert_array_equal(out("dyadicf_k", np.int32), k)
+
+
 def test_exp2q(host_run):
     inp, out = host_run
     np.testing.assert_array_equal(out("exp2q_out", np.int64), oracle.exp2q(inp["exp2q_d"]))
