@@ -680,13 +680,13 @@ def main():
     B = args.batch
     K, W = args.steps, args.warmup
     path = synth.ensure_artifact(SHAPE, SEED)
-    max_ctx = PROMPT_LEN + W + 2 * K + 16
+    co_lens = [int(n) for n in synth.coprompt_lengths(SEED, B - 1)]
+    max_ctx = max([PROMPT_LEN] + co_lens) + W + 2 * K + 16
     model = pkg.Model(path, max_batch=B, max_ctx=((max_ctx + 63) // 64) * 64)
     V, H = model.vocab, model.hidden
     dev = torch.device("cuda", local)
     prompts = [synth.prompt_ids(SEED, 0, PROMPT_LEN, V)]
-    prompts += [synth.prompt_ids(SEED, 100 + i, int(n), V)
-                for i, n in enumerate(synth.coprompt_lengths(SEED, B - 1))]
+    prompts += [synth.prompt_ids(SEED, 100 + i, n, V) for i, n in enumerate(co_lens)]
     s = model.stream
     seq_ids = list(range(B))
 

@@ -140,9 +140,7 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_dec_staged(AttnArgs a, QkvP
         }
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
-            int v = smax[hh];
-#pragma unroll
-            for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+            const int v = __reduce_max_sync(0xffffffffu, smax[hh]);
             if (lane == 0) red_i[w][hh] = v;
         }
     }

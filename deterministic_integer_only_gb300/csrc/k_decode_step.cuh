@@ -330,7 +330,7 @@ __device__ void mg_scales(const StepArgs& a, MgShared& sh, const MgPhase& P) {
                 i64 eps_s;
                 if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (a.eps_h >> (2 * sig));
                 else eps_s = a.eps_h * (1LL << (-2 * sig));
-                const u64 rr = warp_isqrt64((u64)((ss >> lg_k) + eps_s));
+                const u64 rr = isqrt_fast((u64)((ss >> lg_k) + eps_s));
                 dyadic_fast(az, 127ull * rr, &m, &k);
                 k += 12;
             } else {
@@ -499,7 +499,7 @@ __device__ void mg_qk_norm(i64 (&y)[EPL], const int16_t* gamma, int lane, i64 ep
     i64 eps_s;
     if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (eps >> (2 * sig));
     else eps_s = eps * (1LL << (-2 * sig));
-    const i64 rr = (i64)warp_isqrt64((u64)((ss >> LG_D) + eps_s));
+    const i64 rr = (i64)isqrt_fast((u64)((ss >> LG_D) + eps_s));
     const i64 Rr = (i64)pow2_recip((u64)rr, bitlen_u64((u64)rr), 1, 23);
     const int shn = bitlen_u64((u64)rr) + 21;
 #pragma unroll

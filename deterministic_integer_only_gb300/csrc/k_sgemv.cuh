@@ -72,22 +72,6 @@ __device__ __forceinline__ int4 sg_vec(const int4 (&v)[SG_NV], const int32_t* xr
     return r;
 }
 
-// warp reductions on the redux unit: a 64-bit maximum as two 32-bit maxima
-// (high words, then the low words of the lanes holding the highest high
-// word); a 64-bit sum modulo 2^64 as three sums of 22-bit slices (each
-// below 2^27 over 32 lanes)
-__device__ __forceinline__ u64 redux_max_u64(u64 v) {
-    const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(v >> 32));
-    const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(v >> 32) == hi ? (unsigned)v : 0u);
-    return ((u64)hi << 32) | lo;
-}
-__device__ __forceinline__ u64 redux_sum_u64(u64 v) {
-    const unsigned s0 = __reduce_add_sync(0xffffffffu, (unsigned)(v & 0x3fffffu));
-    const unsigned s1 = __reduce_add_sync(0xffffffffu, (unsigned)((v >> 22) & 0x3fffffu));
-    const unsigned s2 = __reduce_add_sync(0xffffffffu, (unsigned)(v >> 44));
-    return (u64)s0 + ((u64)s1 << 22) + ((u64)s2 << 44);
-}
-
 // token scale (m_t, k_t) of row r, by one warp, from the prologue's partial
 // reductions of the row's warp group w0 .. w0 + wpr - 1; only the epilogue
 // needs it
@@ -112,7 +96,7 @@ __device__ void sg_token_scale(const SgArgs& a, SgShared& sh, int r, int w0, int
             i64 eps_s;
             if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (a.eps >> (2 * sig));
             else eps_s = a.eps * (1LL << (-2 * sig));
-            const u64 rr = warp_isqrt64((u64)((ss >> a.lg_k) + eps_s));
+            const u64 rr = isqrt_fast((u64)((ss >> a.lg_k) + eps_s));
             dyadic_fast(az, 127ull * rr, &m, &k);
             k += 12;
         } else {

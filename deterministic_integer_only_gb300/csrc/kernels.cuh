@@ -21,21 +21,10 @@ namespace detint {
 // ------------------------------------------------------------ reductions
 __device__ __forceinline__ u64 umax64(u64 a, u64 b) { return a > b ? a : b; }
 
-__device__ __forceinline__ u64 warp_max_u64(u64 v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = umax64(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-__device__ __forceinline__ int warp_sum_i32(int v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-__device__ __forceinline__ i64 warp_sum_i64(i64 v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
+__device__ __forceinline__ u64 warp_max_u64(u64 v) { return redux_max_u64(v); }
+__device__ __forceinline__ int warp_sum_i32(int v) { return __reduce_add_sync(0xffffffffu, v); }
+// exact for any int64 whose total fits: the slices add modulo 2^64
+__device__ __forceinline__ i64 warp_sum_i64(i64 v) { return (i64)redux_sum_u64((u64)v); }
 // 256-thread block reductions; `sm` holds 8 slots
 __device__ __forceinline__ u64 block_max_u64(u64 v, u64* sm) {
     v = warp_max_u64(v);
@@ -139,7 +128,7 @@ __global__ void __launch_bounds__(256) k_normquant(const int32_t* __restrict__ x
         i64 eps_s;
         if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (eps >> (2 * sig));
         else eps_s = eps * (1LL << (-2 * sig));
-        const u64 rr = warp_isqrt64((u64)((ss >> lg_n) + eps_s));
+        const u64 rr = isqrt_fast((u64)((ss >> lg_n) + eps_s));
         int m, k;
         dyadic_fast(az, 127ull * rr, &m, &k);
         if (tid == 0) { mt[r] = m; kt[r] = k + 12; }
@@ -219,7 +208,7 @@ __device__ void qk_norm_warp(i64 (&y)[EPL], const int16_t* gamma, int lane, int 
     i64 eps_s;
     if (sig >= 0) eps_s = (2 * sig >= 62) ? 0 : (eps >> (2 * sig));
     else eps_s = eps * (1LL << (-2 * sig));
-    const i64 rr = (i64)warp_isqrt64((u64)((ss >> lg_d) + eps_s));
+    const i64 rr = (i64)isqrt_fast((u64)((ss >> lg_d) + eps_s));
     const i64 Rr = (i64)pow2_recip((u64)rr, bitlen_u64((u64)rr), 1, 23);
     const int sh = bitlen_u64((u64)rr) + 21;
 #pragma unroll
@@ -261,15 +250,18 @@ __device__ void qkv_head_p(const QkvPostArgs& a, int t, int slot, int8_t* q_dst,
     const int pos = a.tok_pos[t];
     const int32_t* row = a.qkv + (size_t)t * nqkv;
     const int kvh = slot < nq ? (slot >> a.lg_grp) : (slot - nq);
-    int E = 0;
-    for (int i = lane; i < dh2; i += 32) E = max(E, kvp[8 + i]);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) E = max(E, __shfl_xor_sync(0xffffffffu, E, o));
-
     i64 y[EPL];
+    int vraw[EPL];            // the value row (kv heads), loaded with the key row
     const int base = slot < nq ? slot * d : (nq + kvh) * d;
 #pragma unroll
     for (int j = 0; j < EPL; ++j) y[j] = row[base + lane + 32 * j];
+    if (slot >= nq) {
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) vraw[j] = row[(nq + nkv + kvh) * d + lane + 32 * j];
+    }
+    int E = 0;
+    for (int i = lane; i < dh2; i += 32) E = max(E, kvp[8 + i]);
+    E = __reduce_max_sync(0xffffffffu, E);
     if (a.qk_norm) {
         qk_norm_warp<EPL>(y, slot < nq ? gq : gk, lane, lg_d, a.eps_qk);
     } else {
@@ -322,13 +314,12 @@ __device__ void qkv_head_p(const QkvPostArgs& a, int t, int slot, int8_t* q_dst,
         int8_t* vd = a.vc + ((size_t)blk * nkv + kvh) * d * KV_BLK + off;
         const i64 KQM = kvp[0], VQM = kvp[2];
         const int KQS = kvp[1], VQS = kvp[3];
-        const int32_t* vrow = row + (nq + nkv + kvh) * d;
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
             const int i = lane + 32 * j;
             const int ec = kvp[8 + (i & (dh2 - 1))];
             const int8_t k8 = (int8_t)sat127(rshr(y[j] * (1LL << ec) * KQM, KQS));
-            const int8_t v8 = (int8_t)sat127(rshr((i64)vrow[i] * VQM, VQS));
+            const int8_t v8 = (int8_t)sat127(rshr((i64)vraw[j] * VQM, VQS));
             kd[i] = k8;
             vd[(size_t)i * KV_BLK] = v8;
             if (ks) {
@@ -371,7 +362,7 @@ size_t attention_smem_bytes(int grp, int d, int ctx_cap) {
 // attention of token t's q heads of kv group g; qs [G][d], mqs/kqs [G] in
 // shared memory, sm the dynamic shared memory (score row, E bytes, partials)
 template <int EPL, int G>
-__device__ __noinline__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs,
+__device__ void attention_core(const AttnArgs& a, int t, int g, const int8_t* qs,
                                const int32_t* mqs, const int32_t* kqs, unsigned char* sm) {
     const int tid = threadIdx.x;
     constexpr int d = 32 * EPL;
@@ -424,9 +415,7 @@ __device__ __noinline__ void attention_core(const AttnArgs& a, int t, int g, con
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
             if (hh < G) {
-                int v = smax[hh];
-#pragma unroll
-                for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+                const int v = __reduce_max_sync(0xffffffffu, smax[hh]);
                 if (lane == 0) red[w * MAXG + hh] = v;
             }
         }

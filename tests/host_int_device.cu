@@ -47,6 +47,10 @@ int main(int argc, char** argv) {
         std::vector<u64> out(x.size());
         for (size_t i = 0; i < x.size(); ++i) out[i] = isqrt_u64(x[i]);
         save(dir, "isqrt_out", out);
+        auto xf = load<u64>(dir, "isqrtf_x");
+        std::vector<u64> of(xf.size());
+        for (size_t i = 0; i < xf.size(); ++i) of[i] = isqrt_fast(xf[i]);
+        save(dir, "isqrtf_out", of);
     }
     {   // 15-bit dyadic scale
         auto N = load<u64>(dir, "dyadic_n");

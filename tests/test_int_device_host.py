@@ -49,6 +49,17 @@ def host_run(tmp_path_factory):
     rt = rng.integers(1, 1 << 31, 20000, dtype=np.uint64)
     q[:60000] = np.concatenate([rt * rt, rt * rt - np.uint64(1), rt * rt + np.uint64(1)])
     inputs["isqrt_x"] = q
+    # the single-thread square root: every bit length (log-uniform), squares
+    # +-1 of every root length, all n below 2^16 and the top of the range
+    bl = rng.integers(1, 63, n).astype(np.uint64)
+    qf = (rng.integers(0, 1 << 62, n, dtype=np.uint64) << np.uint64(2)) >> (np.uint64(64) - bl)
+    rb = rng.integers(1, 32, 30000).astype(np.uint64)
+    rf = (rng.integers(0, 1 << 31, 30000, dtype=np.uint64) >> (np.uint64(31) - rb)) | (np.uint64(1) << (rb - np.uint64(1)))
+    sq = rf * rf
+    qf[:90000] = np.concatenate([sq, sq - np.uint64(1), sq + np.uint64(1)])
+    qf[90000:90000 + (1 << 16)] = np.arange(1 << 16, dtype=np.uint64)
+    qf[-3:] = [(1 << 62) - 1, 1 << 61, (1 << 60) - 1]
+    inputs["isqrtf_x"] = qf
     # dyadic scales over the kernels' ranges (N, D below 2^40, |k| <= 39)
     ln = rng.integers(1, 41, n)
     ld = np.clip(ln - 14 + rng.integers(-39, 40, n), 1, 40)
@@ -114,6 +125,12 @@ def test_rshr(host_run):
 def test_isqrt(host_run):
     inp, out = host_run
     np.testing.assert_array_equal(out("isqrt_out", np.uint64), oracle.isqrt(inp["isqrt_x"]))
+
+
+def test_isqrt_fast(host_run):
+    """The single-thread Newton-Raphson square root equals the oracle's."""
+    inp, out = host_run
+    np.testing.assert_array_equal(out("isqrtf_out", np.uint64), oracle.isqrt(inp["isqrtf_x"]))
 
 
 def test_dyadic(host_run):
