@@ -77,7 +77,9 @@ __device__ __forceinline__ int4 sg_vec(const int4 (&v)[SG_NV], const int32_t* xr
 // needs it
 __device__ void sg_token_scale(const SgArgs& a, SgShared& sh, int r, int w0, int wpr) {
     u64 axl = 0;
-    for (int w = 0; w < wpr; ++w) axl = umax64(axl, (u64)sh.red64[w0 + w][0]);
+#pragma unroll
+    for (int w = 0; w < 8; ++w)
+        if (w < wpr) axl = umax64(axl, (u64)sh.red64[(w0 + w) & 7][0]);
     int m = 0, k = 0;
     if (axl != 0) {
         if (a.pro == PRO_NORMQUANT) {
@@ -85,9 +87,12 @@ __device__ void sg_token_scale(const SgArgs& a, SgShared& sh, int r, int w0, int
             i64 ss = 0;
             u64 az = 0;
             const int js = sig <= 0 ? 2 : 3, jz = sig <= 0 ? 1 : 4;
-            for (int w = 0; w < wpr; ++w) {
-                ss += sh.red64[w0 + w][js];
-                az = umax64(az, (u64)sh.red64[w0 + w][jz]);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                if (w < wpr) {
+                    ss += sh.red64[(w0 + w) & 7][js];
+                    az = umax64(az, (u64)sh.red64[(w0 + w) & 7][jz]);
+                }
             }
             if (sig <= 0) {
                 ss <<= -2 * sig;
@@ -171,8 +176,11 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, c
     }
     bar_named(bar, gn);
     u64 axl = 0;
-    for (int w = 0; w < wpr; ++w) axl = umax64(axl, (u64)sh.red64[w0 + w][0]);
+#pragma unroll
+    for (int w = 0; w < 8; ++w)
+        if (w < wpr) axl = umax64(axl, (u64)sh.red64[(w0 + w) & 7][0]);
     if (axl == 0) {
+        if (sp) bar_arrive_named(14, 288);
         for (int i = gt * 16; i < K; i += gn * 16) *(int4*)(qr + i) = make_int4(0, 0, 0, 0);
         if (gt == 0) { sh.mt[r] = 0; sh.kt[r] = 0; }
         return;
@@ -184,7 +192,9 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, c
         if (sig <= 0) {
             // x' = x 2^-sig exactly: max |x' gamma| is the pass-1 maximum scaled
             amax = 0;
-            for (int w = 0; w < wpr; ++w) amax = umax64(amax, (u64)sh.red64[w0 + w][1]);
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                if (w < wpr) amax = umax64(amax, (u64)sh.red64[(w0 + w) & 7][1]);
             amax <<= -sig;
         } else {
             // pass 2: sum of squares of the 24-bit row and max |x' gamma|
@@ -209,12 +219,17 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, c
             if (lane == 0) { sh.red64[warp][3] = ss; sh.red64[warp][4] = (long long)az; }
             bar_named(bar, gn);
             amax = 0;
-            for (int w = 0; w < wpr; ++w) amax = umax64(amax, (u64)sh.red64[w0 + w][4]);
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                if (w < wpr) amax = umax64(amax, (u64)sh.red64[(w0 + w) & 7][4]);
         }
     }
-    // the token scale on one warp (unless the producer warp takes it); the
-    // quantisation multiplier in every thread, from the maximum it already holds
-    if (!sp && gw == 0) sg_token_scale(a, sh, r, w0, wpr);
+    // the partial reductions are final: the producer warp may start on the
+    // token scale (sp) while this thread quantises; else one warp of the
+    // group takes it. The quantisation multiplier in every thread, from the
+    // maximum it already holds
+    if (sp) bar_arrive_named(14, 288);
+    else if (gw == 0) sg_token_scale(a, sh, r, w0, wpr);
     const int e = bitlen_u64(amax);
     const i64 R = (i64)pow2_recip(amax, e, 127, 16);
     const int shq = e + 16;
@@ -248,15 +263,24 @@ __device__ void sg_prologue(const SgArgs& a, SgShared& sh, int8_t* xs, int XP, c
 __device__ void sg_load_x8(const SgArgs& a, SgShared& sh, int8_t* xs, int XP) {
     const int tid = threadIdx.x;
     const int kv = a.K >> 4;
-    for (int r = 0; r < 8; ++r)
-        for (int v = tid; v < kv; v += 256) {
-            int4 val = make_int4(0, 0, 0, 0);
-            if (r < a.M) val = *(const int4*)(a.x8 + (size_t)r * a.K + v * 16);
-            *(int4*)(xs + (size_t)r * XP + v * 16) = val;
-        }
+    // every load of a pass is issued before its stores, so the L2 round trips
+    // overlap instead of following one another
+    int mt = 0, kt = 0;
+    if (tid < a.M) {
+        if (a.mt_in) mt = a.mt_in[tid];
+        if (a.kt_in) kt = a.kt_in[tid];
+    }
+    for (int v = tid; v < kv; v += 256) {
+        int4 val[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+            val[r] = r < a.M ? *(const int4*)(a.x8 + (size_t)r * a.K + v * 16) : make_int4(0, 0, 0, 0);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) *(int4*)(xs + (size_t)r * XP + v * 16) = val[r];
+    }
     if (tid < 8) {
-        sh.mt[tid] = (tid < a.M && a.mt_in) ? a.mt_in[tid] : 0;
-        sh.kt[tid] = (tid < a.M && a.kt_in) ? a.kt_in[tid] : 0;
+        sh.mt[tid] = mt;
+        sh.kt[tid] = kt;
     }
 }
 
@@ -582,7 +606,6 @@ __global__ void __launch_bounds__(SG_THREADS, MINB) k_sgemv(SgArgs a) {
     }
     if (a.pro == PRO_NONE) sg_load_x8(a, sh, xs, XP);
     else sg_prologue(a, sh, xs, XP, gam, sp);
-    if (sp) bar_arrive_named(14, 288);
     if (pre && tid < (g1 - g0) * 128) hold[tid] = hv;
     bar_named(1, 256);
 
