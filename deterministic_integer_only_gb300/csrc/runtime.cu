@@ -302,11 +302,11 @@ static int run_decode_fused(detint_model* m, int T, const int32_t* tokens, int32
     if (m->dec_staged == 2) return run_decode_step(m, T, tokens, logits, next_tok, s);
     const int H = m->H, d = m->d, nq = m->nq, nkv = m->nkv, F = m->F;
     const int nqkv = (nq + 2 * nkv) * d;
-    // from 5 sequences on, each row is quantised once by a row kernel (one CTA
-    // per row) instead of redundantly by every GEMV CTA (measured: 3 and 4
-    // sequences 1-2 % faster with the fused prologue, 5 to 8 sequences
-    // 20-25 % slower)
-    const bool sep = T >= 5;
+    // from 3 sequences on, each row is quantised once by a row kernel (one CTA
+    // per row) instead of redundantly by every GEMV CTA (measured steps: 2
+    // sequences 868 us fused against 1002 us with row kernels; 3 and 4
+    // sequences 1136 and 1213 us fused against 1052 and 1066 us)
+    const bool sep = T >= 3;
     auto gemv = [&](const int8_t* W, int N, int K, const int32_t* xin, const int16_t* gamma, int F_in,
                     int pro, int mode, const Epi& e, int spare = 0) -> int {
         if (sep) {
