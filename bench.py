@@ -181,7 +181,7 @@ def cpu_baseline(seconds: float = 12.0):
 
 # DRAM bytes (read + write) of one lm_head GEMV launch at M=1, from an ncu
 # capture of dram__bytes_read.sum + dram__bytes_write.sum on the current kernel
-LMHEAD_DRAM_BYTES = 158290432
+LMHEAD_DRAM_BYTES = 158621952
 
 
 def int8_peak(pkg, dev, iters=4096, reps=5):
@@ -535,6 +535,10 @@ def run_all_kernels(args):
         A = torch.randint(-127, 128, (M, 256), dtype=torch.int8, device=dev)
         W = torch.randint(-127, 128, (512, 256), dtype=torch.int8, device=dev)
         pkg.detint_gemm_i8(A, W, torch.empty((M, 512), dtype=torch.int32, device=dev))
+    # a long weight stream (the lm_head-like variant with two CTAs per SM)
+    A = torch.randint(-127, 128, (1, 1024), dtype=torch.int8, device=dev)
+    W = torch.randint(-127, 128, (32768, 1024), dtype=torch.int8, device=dev)
+    pkg.detint_gemm_i8(A, W, torch.empty((1, 32768), dtype=torch.int32, device=dev))
     W16 = torch.randint(-32767, 32768, (512, 256), dtype=torch.int16, device=dev)
     hi, lo = pkg.detint_split_w16(W16)
     pkg.detint_gemm_w16(torch.randint(-127, 128, (64, 256), dtype=torch.int8, device=dev), hi, lo)
