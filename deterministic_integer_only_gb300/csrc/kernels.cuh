@@ -92,8 +92,12 @@ __global__ void __launch_bounds__(256) k_embed(const int32_t* __restrict__ token
 
 // ---------------------------------------------------------------- NormQuant
 // a2/a7/a10: integer RMSNorm folded into the per-token int8 quantisation.
-__global__ void __launch_bounds__(256) k_normquant(const int32_t* __restrict__ x,
-                                                   const int32_t* __restrict__ rows, int n,
+// The row kernels (and the final argmax) run under programmatic dependent
+// launch, so their inputs are written by a kernel that is still running when
+// they start: those pointers carry no __restrict__, which would let the
+// compiler read them through the non-coherent read-only path (valid only
+// for data that stays unchanged for the reader's whole lifetime).
+__global__ void __launch_bounds__(256) k_normquant(const int32_t* x, const int32_t* rows, int n,
                                                    int lg_n, const int16_t* __restrict__ gamma,
                                                    i64 eps, int8_t* __restrict__ q,
                                                    int32_t* __restrict__ mt,
@@ -148,7 +152,7 @@ __global__ void __launch_bounds__(256) k_normquant(const int32_t* __restrict__ x
 
 // ----------------------------------------------------------------- ActQuant
 // a6/a9: per-token int8 quantisation of an int32 row of fixed point F.
-__global__ void __launch_bounds__(256) k_actquant(const int32_t* __restrict__ x, int n, int F,
+__global__ void __launch_bounds__(256) k_actquant(const int32_t* x, int n, int F,
                                                   int8_t* __restrict__ q,
                                                   int32_t* __restrict__ mt,
                                                   int32_t* __restrict__ kt) {
@@ -807,8 +811,7 @@ namespace detint {
 __device__ __forceinline__ void better(int& bv, int& bi, int v, int i) {
     if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
 }
-__global__ void __launch_bounds__(256) k_argmax_final(const int32_t* __restrict__ pval,
-                                                      const int32_t* __restrict__ pidx, int npart,
+__global__ void __launch_bounds__(256) k_argmax_final(const int32_t* pval, const int32_t* pidx, int npart,
                                                       int32_t* __restrict__ next_tok,
                                                       const int32_t* __restrict__ tok_seq,
                                                       int32_t* __restrict__ seq_len) {
