@@ -208,8 +208,9 @@ def test_staged_decode_capacity_crossing(torch_cuda, qwen_artifact):
 @pytest.mark.parametrize("name", ["tiny", "qwen", "llama"])
 @pytest.mark.parametrize("B", [1, 3, 8])
 def test_persistent_decode_equals_kernel_chain(torch_cuda, request, name, B):
-    """The one-launch decode step (cooperative grid, grid barriers between
-    phases) gives the kernel chain's logits and tokens, batch of B."""
+    """The one-launch decode step (cooperative grid, phases handed over
+    through tagged activation words) gives the kernel chain's logits and
+    tokens, batch of B."""
     path = request.getfixturevalue({"tiny": "tiny_artifact", "qwen": "qwen_artifact",
                                     "llama": "llama_artifact"}[name])
     V = {"tiny": 1024, "qwen": 151936, "llama": 128256}[name]
